@@ -1,0 +1,380 @@
+"""Benchmark of the TurboQuantProd hot path on B300: encode a KV cache, then score
+one decode step on the compressed keys.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--bits B]
+
+One step = tq_encode of every key of the workload (E0-E6) + tq_score of one
+query per head against all of them (S0-S4).  The default workload is the
+Qwen2.5-3B-shaped decode step (72 groups x 8,192 fp16 keys, 8 query heads per
+group, d = 128, 3 bits).  The value is keys encoded-and-scored per second over
+the whole step; per-kernel numbers, rooflines, the fp32-key baseline, an
+end-to-end run from pinned host memory and the CPU oracle are reported beside
+it in the same JSON line.  Multi-GPU runs (torchrun) are replicas: every rank
+runs the full workload on its own GPU (weak scaling), no collective on the
+data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import tq_synth  # noqa: E402
+
+METRIC = "tq_score keys scored/s & % HBM roofline at 3-bit d=128; tq_encode vectors/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_traffic(kernel: str, source: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f).get(kernel)
+        with open(os.path.join(ROOT, "vector_quantization_02_b300", "csrc", source), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if t and t.get("source_sha") == sha:
+            return t["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.proc = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, AttributeError, RuntimeError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 7]
+        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[4 + i]})
+        busy = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle timing (CPU)
+
+def oracle_throughput(w, bits, budget_s: float):
+    """Time the oracle (encode + score of one group's keys against H heads) on a
+    bounded sample; returns (keys/s, sample description, threads)."""
+    import numpy as np
+    from threadpoolctl import threadpool_info
+
+    from oracle import tq_oracle as o
+    d = w.d
+    Pi = o.haar_rotation(tq_synth.rotation_gaussian(d, w.seeds["rotation"]).numpy()).astype(np.float32)
+    S = tq_synth.projection(d, w.seeds["projection"]).numpy()
+    c = o.codebook_f32(1 << (bits - 1), d)
+    q = tq_synth.queries(w, G=1).numpy()
+
+    def run(n):
+        keys = tq_synth.keys(w, G=1, N=n)
+        t0 = time.perf_counter()
+        buf, _ = o.encode_pack(keys.double().numpy(), Pi, S, c, bits, "prod", 1, n)
+        o.score_packed(q, buf, Pi, S, c, bits, "prod", 1, n)
+        return time.perf_counter() - t0
+
+    n = 256
+    t = run(n)
+    while t < budget_s / 8 and n < w.N:
+        n = min(w.N, n * 4)
+        t = run(n)
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    return n / t, f"encode+score of {n} keys of group 0 against its {w.H} heads (numpy fp64)", threads
+
+
+# ---------------------------------------------------------------- our path
+
+def _e2e(args, world, plan, keys, q, packed, logits, ws, flush, top_k, stream, ev):
+    """Median step time with the inputs copied from pinned host memory and the
+    logits copied back inside the timed events."""
+    import vector_quantization_02_b300 as tq
+    G, N, _ = keys.shape
+    H = q.shape[1]
+    keys_h = keys.cpu().pin_memory()
+    q_h = q.cpu().pin_memory()
+    out_h = torch.empty(G, H, N, dtype=torch.float32).pin_memory()
+    keys_d = torch.empty_like(keys)
+    q_d = torch.empty_like(q)
+    e2e_t = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = ev(), ev()
+        a.record(stream)
+        keys_d.copy_(keys_h, non_blocking=True)
+        q_d.copy_(q_h, non_blocking=True)
+        tq.tq_encode(plan, keys_d, packed=packed)
+        tq.tq_score(plan, q_d, packed, N, top_k=top_k, logits=logits, workspace=ws)
+        out_h.copy_(logits, non_blocking=True)
+        b.record(stream)
+        if i >= args.warmup:
+            e2e_t.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, statistics.median(a.elapsed_time(b) for a, b in e2e_t))
+
+    return e2e_ms
+
+
+def run_ours(args, world, rank):
+    import vector_quantization_02_b300 as tq
+    w = tq_synth.WORKLOADS[args.workload]
+    bits = args.bits or w.bits[0]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    G, N, H, d = w.G, w.N, w.H, w.d
+    pk, pk_kind = peaks()
+
+    keys = tq_synth.keys(w, device=dev, seed_offset=rank)
+    q = tq_synth.queries(w, device=dev, seed_offset=rank)
+    plan = tq.Plan.from_seeds(d, bits, tq_synth.rotation_gaussian(d, w.seeds["rotation"]),
+                              tq_synth.projection(d, w.seeds["projection"]))
+    packed = torch.empty(plan.packed_bytes(G, N), dtype=torch.uint8, device=dev)
+    logits = torch.empty(G, H, N, dtype=torch.float32, device=dev)
+    top_k = w.top_k
+    ws = torch.empty(tq.score_workspace_bytes(plan, G, H, N, top_k), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tq.tq_encode(plan, keys, packed=packed)
+        tq.tq_score(plan, q, packed, N, top_k=top_k, logits=logits, workspace=ws)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, L2 flushed between steps outside the step events
+    e_start = [ev() for _ in range(args.steps)]
+    e_mid = [ev() for _ in range(args.steps)]
+    e_end = [ev() for _ in range(args.steps)]
+    clocks = Clocks(dev.index)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        e_start[i].record(stream)
+        tq.tq_encode(plan, keys, packed=packed)
+        e_mid[i].record(stream)
+        tq.tq_score(plan, q, packed, N, top_k=top_k, logits=logits, workspace=ws)
+        e_end[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    enc_ms = sum(a.elapsed_time(b) for a, b in zip(e_start, e_mid)) / args.steps
+    sc_ms = sum(a.elapsed_time(b) for a, b in zip(e_mid, e_end)) / args.steps
+    step_ms = max_over_ranks(world, enc_ms + sc_ms)
+    assert plan.status() == 0
+    keys_total = G * N * world
+    value = keys_total / (step_ms * 1e-3)
+
+    # per-kernel algorithmic bytes
+    P = plan.packed_bytes(G, N)
+    key_bytes = keys.numel() * keys.element_size()
+    logit_bytes = G * H * N * 4
+    q_bytes = q.numel() * 4
+    enc_bytes = key_bytes + P
+    sc_bytes = P + logit_bytes + q_bytes
+    hbm = pk["hbm_gbs"]
+
+    def roof(bytes_, ms, kernel, source, flops=None):
+        ach = bytes_ / (ms * 1e-3) / 1e9
+        r = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+             "traffic": kernel_traffic(kernel, source), "algorithmic_bytes": bytes_, "peak_source": pk_kind}
+        if flops is not None:
+            r["algorithmic_flops"] = flops
+            r["tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
+        return r
+
+    enc_roof = roof(enc_bytes, enc_ms, "encode", "k_encode_simt.cu", flops=4 * d * d * G * N)
+
+    # score alone on a cold L2 (a decode step reads a cache encoded earlier)
+    sc_cold = []
+    for _ in range(max(3, args.steps)):
+        flush.zero_()
+        a, b = ev(), ev()
+        a.record(stream)
+        tq.tq_score(plan, q, packed, N, top_k=top_k, logits=logits, workspace=ws)
+        b.record(stream)
+        sc_cold.append((a, b))
+    torch.cuda.synchronize()
+    sc_cold_ms = statistics.median(a.elapsed_time(b) for a, b in sc_cold)
+    sc_roof = roof(sc_bytes, sc_cold_ms, "score", "k_score_simt.cu")
+
+    # the uncompressed baseline on the same keys (fp32 copies), cold L2
+    base = None
+    if d * G * N * 4 < 40e9:
+        keys32 = keys.float()
+        base_l = torch.empty_like(logits)
+        bt = []
+        for _ in range(max(3, args.steps)):
+            flush.zero_()
+            a, b = ev(), ev()
+            a.record(stream)
+            tq.tq_score_fp32(q, keys32, logits=base_l)
+            b.record(stream)
+            bt.append((a, b))
+        torch.cuda.synchronize()
+        bms = statistics.median(a.elapsed_time(b) for a, b in bt)
+        base = {"ms": round(bms, 4), "keys_per_s": G * N / (bms * 1e-3),
+                "roofline": roof(keys32.numel() * 4 + logit_bytes + q_bytes, bms, "fp32", "k_misc.cu"),
+                "score_speedup_vs_fp32_keys": round(bms / sc_cold_ms, 3)}
+        del keys32, base_l
+
+    # end to end through the public API from pinned host memory
+    if key_bytes > 8e9:
+        e2e_ms = None
+    else:
+        e2e_ms = _e2e(args, world, plan, keys, q, packed, logits, ws, flush, top_k, stream, ev)
+    launches_per_step = 1 + 2 + (2 if top_k else 0)   # encode; query prep + score; top-k
+    line = {
+        "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "G": G, "N": N, "H": H, "d": d, "bits": bits,
+                   "key_dtype": str(w.key_dtype).replace("torch.", ""), "top_k": top_k,
+                   "l2": "flushed between steps (2x L2 memset, outside the step events)"},
+        "roofline": enc_roof,
+        "parts": {
+            "encode": {"ms": round(enc_ms, 5), "vectors_per_s": G * N / (enc_ms * 1e-3), "roofline": enc_roof},
+            "score": {"ms_in_step": round(sc_ms, 5), "ms_cold_l2": round(sc_cold_ms, 5),
+                      "keys_per_s_cold_l2": G * N / (sc_cold_ms * 1e-3),
+                      "logits_per_s_cold_l2": G * N * H / (sc_cold_ms * 1e-3), "roofline_cold_l2": sc_roof},
+            "fp32_key_baseline": base,
+        },
+        "e2e": None if e2e_ms is None else {
+            "value": keys_total / (e2e_ms * 1e-3), "unit": "keys/s", "h2d_bytes_per_step": key_bytes + q_bytes,
+            "d2h_bytes_per_step": logit_bytes, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample, cores = oracle_throughput(w, bits, args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample}
+    plan.close()
+    return line
+
+
+def run_reference(args, world, rank):
+    w = tq_synth.WORKLOADS[args.workload]
+    bits = args.bits or w.bits[0]
+    if rank != 0:
+        return None
+    vals = []
+    sample = cores = None
+    for _ in range(args.warmup + args.steps):
+        v, sample, cores = oracle_throughput(w, bits, args.cpu_budget / max(1, args.steps + args.warmup))
+        vals.append(v)
+    v = statistics.median(vals[args.warmup:]) if len(vals) > args.warmup else vals[-1]
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "G": w.G, "N": w.N, "H": w.H, "d": w.d, "bits": bits},
+        "cpu_baseline": {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen25_3b_decode", choices=sorted(tq_synth.WORKLOADS))
+    ap.add_argument("--bits", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, _ = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * tq.h -- C ABI of libtq.so: TurboQuantProd key encoding and attention-logit
+ * scoring on the compressed keys, for one B300 (sm_103a).
+ *
+ * Sources:
+ *  [PT-KR]  "turboquant-pytorch 소개" (discuss.pytorch.kr, PyTorch Korea user
+ *           group): "1단계: 랜덤 회전 + Lloyd-Max 양자화", "2단계: QJL 잔차 보정",
+ *           the usage listing ("TurboQuant 핵심 알고리즘 사용 예시"), "성능 지표".
+ *  [TAMBUR] "Google acelera LLM 8 veces" (tambur.pub): MSE-only quantisers bias
+ *           inner products; a 1-bit QJL residual pass removes the bias; 4-bit
+ *           keys speed up attention logits versus 32-bit keys.
+ *  [P5]     "알고리즘보다 커널이 성패를 가른다" (tistory27), section 3: the
+ *           bit-packed format with QJL metadata needs a dedicated kernel.
+ *
+ * Notation: d = head dimension (a multiple of 128), m = d rows of S,
+ * b = total bits per coordinate, k = b-1 Lloyd-Max bits (PROD) or k = b (MSE),
+ * L = 2^k centroids, G = groups (batch x layers x KV heads), N = tokens per
+ * group, H = query heads per group.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device pointers on the current device;
+ *    the caller owns every buffer it passes.  The library allocates device
+ *    memory only in tq_plan_create (freed by tq_plan_destroy).
+ *  - Keys, queries, logits and packed buffers must be 16-byte aligned and
+ *    contiguous in the stated layout; otherwise TQ_EALIGN.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  Argument errors are returned synchronously and
+ *    nothing is enqueued.  A failed launch returns TQ_ECUDA.  Device-side errors
+ *    (a bounded wait that ran out) are reported by tq_plan_status after the
+ *    caller synchronises.
+ *  - No entry point prints, throws, or falls back to the CPU.
+ *  - A plan is immutable after creation: calls on different streams may share
+ *    it concurrently.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_EINVAL = -1,        /* bad size, null pointer, unsupported combination */
+  TQ_EALIGN = -2,        /* a pointer is not 16-byte aligned */
+  TQ_EUNSUPPORTED = -3,  /* valid request this build does not handle */
+  TQ_ECUDA = -4,         /* a CUDA call failed (launch, copy, allocation) */
+  TQ_ETIMEOUT = -5,      /* a bounded device wait ran out (see tq_plan_status) */
+  TQ_ENOMEM = -6         /* device allocation failed in tq_plan_create */
+} tq_status;
+
+typedef enum { TQ_F32 = 0, TQ_F16 = 1, TQ_BF16 = 2 } tq_dtype;
+
+/* TQ_PROD: TurboQuantProd, (b-1)-bit Lloyd-Max codes + 1-bit QJL signs of
+ * S r + ||x|| and ||r||  ([PT-KR] 1단계 and 2단계).
+ * TQ_MSE:  TurboQuantMSE, b-bit Lloyd-Max codes + ||x|| ([PT-KR] 1단계). */
+typedef enum { TQ_PROD = 0, TQ_MSE = 1 } tq_mode;
+
+typedef struct tq_plan tq_plan;
+
+/* ---------------------------------------------------------------- plan inputs
+ * Host-side helpers that build the plan's inputs from random draws the caller
+ * makes.  They run on the CPU once per plan (they are set-up, not the path). */
+
+/* Lloyd-Max codebook for one rotated coordinate, treated as N(0, 1/d)
+ * ([PT-KR] 1단계: the optimal quantiser for the bell-shaped coordinate
+ * distribution, precomputed).  Writes `levels` ascending fp32 centroids
+ * (the N(0,1) quantiser scaled by 1/sqrt(d)) to the HOST array `out`.
+ * levels in {2,4,8,16}; d >= 1.  Errors: TQ_EINVAL. */
+tq_status tq_lloyd_max_codebook(int levels, int d, float* out);
+
+/* Random orthogonal rotation from a d x d Gaussian matrix ([PT-KR] 1단계):
+ * Pi = Q diag(sign R_ii) for the Householder QR  gaussian = Q R  (fp64),
+ * written as fp32 row-major to the HOST array `Pi_out` (y = Pi u).
+ * `gaussian` is a HOST fp64 row-major d x d array.  Errors: TQ_EINVAL
+ * (d < 1, d > 8192, null pointer, rank-deficient input). */
+tq_status tq_haar_rotation(int d, const double* gaussian, float* Pi_out);
+
+/* ---------------------------------------------------------------- plan */
+
+/* Create a plan for head dimension d and b total bits.
+ *   Pi        device fp32 d x d row-major, y = Pi u (orthogonal).
+ *   S         device fp32 d x d row-major (m = d rows); NULL for TQ_MSE.
+ *   codebook  device fp32, L ascending centroids already scaled for N(0,1/d)
+ *             (L = 2^(bits-1) for TQ_PROD, 2^bits for TQ_MSE).
+ * The plan copies Pi, S and the codebook and derives M = S Pi^T (fp64
+ * accumulation) plus the half-precision operand splits the kernels use; the
+ * caller may free its buffers once the plan exists.  Runs on `stream` and
+ * synchronises it before returning.
+ * Constraints: d % 128 == 0, 128 <= d <= 2048; TQ_PROD bits in {2,3,4};
+ * TQ_MSE bits in {1,2,3,4}.  Errors: TQ_EINVAL, TQ_ENOMEM, TQ_ECUDA. */
+tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const float* S,
+                         const float* codebook, void* stream, tq_plan** out);
+tq_status tq_plan_destroy(tq_plan* plan);
+
+/* Bytes of the packed buffer for G groups of N tokens.  Layout ([P5] §3):
+ * per group, blocks of 128 tokens; per block, for each plane p (the k code
+ * bits, LSB first, then the sign plane in TQ_PROD), for each 128-coordinate
+ * chunk c, the 128 tokens' 16-byte chunks in token order; then 128 norm pairs
+ * {float ||x||, float ||r||} (||r|| = 0 in TQ_MSE).  In a chunk, coordinate
+ * 128c + 32w + i is bit i of little-endian uint32 word w.  Tokens past N in the
+ * last block are zero.  Bytes per key: (planes*d)/8 + 8, planes = b.
+ * Returns 0 for a null plan or negative sizes. */
+size_t tq_packed_bytes(const tq_plan* plan, int64_t n_groups, int64_t n_tokens);
+
+/* ---------------------------------------------------------------- the path */
+
+/* Encode keys ([PT-KR] 1단계 + 2단계; usage listing: ``tq.compress``):
+ * for each key x: n = ||x||, u = x/n, y = Pi u, idx_j = #{i : t_i < y_j}
+ * with t_i = (c_i + c_{i+1})/2; r = x - n Pi^T c[idx]; rho = ||r||;
+ * z = [S r >= 0].  A zero key stores idx = #{t_i < 0}, z = 1, rho = 0.
+ *   keys    device [G][N][d] row-major in `dtype` (fp32, fp16 or bf16).
+ *   packed  device, tq_packed_bytes(plan, G, N) bytes, fully overwritten.
+ * G >= 0, N >= 0 (G*N == 0 is a no-op).  Errors: TQ_EINVAL, TQ_EALIGN, TQ_ECUDA. */
+tq_status tq_encode(const tq_plan* plan, const void* keys, tq_dtype dtype, int64_t n_groups,
+                    int64_t n_tokens, void* packed, void* stream);
+
+/* Bytes of scratch tq_score needs (rotated queries Pi q, projected queries
+ * S q and the top-k candidates); the caller allocates it. */
+size_t tq_score_workspace_bytes(const tq_plan* plan, int64_t n_groups, int n_heads,
+                                int64_t n_tokens, int top_k);
+
+/* Attention logits on the compressed keys ([PT-KR] usage listing:
+ * ``tq.inner_product(query, compressed)``; [TAMBUR]: the unbiased estimate):
+ *   logit = n <Pi q, c[idx]> + rho * sqrt(pi/2)/m * <S q, 2z - 1>
+ * (TQ_MSE: the first term only), which equals <q, x_mse> + the QJL term.
+ *   queries    device fp32 [G][H][d].
+ *   packed     device, as written by tq_encode for (G, N).
+ *   logits     device fp32 [G][H][N], fully overwritten.
+ *   top_k      0 for none, else 1..64: also writes, per (g, h), the top_k
+ *              logits in descending order (ties: lower token first) to
+ *              top_scores fp32 [G][H][top_k] and their token indices to
+ *              top_idx int64 [G][H][top_k]; needs top_k <= N.
+ *   workspace  device, >= tq_score_workspace_bytes(...), 256-byte aligned.
+ * 1 <= H <= 256.  Errors: TQ_EINVAL, TQ_EALIGN, TQ_ECUDA. */
+tq_status tq_score(const tq_plan* plan, const float* queries, int64_t n_groups, int n_heads,
+                   const void* packed, int64_t n_tokens, float* logits, int top_k,
+                   float* top_scores, int64_t* top_idx, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Reconstruct keys ([PT-KR] usage listing: ``tq.decompress``):
+ * x_hat = n Pi^T c[idx] + rho sqrt(pi/2)/m S^T (2z - 1)  (TQ_MSE: first term),
+ * so that <q, x_hat> equals tq_score's logit.  out: device fp32 [G][N][d]. */
+tq_status tq_decode(const tq_plan* plan, const void* packed, int64_t n_groups, int64_t n_tokens,
+                    float* out, void* stream);
+
+/* The uncompressed baseline ([TAMBUR]: "32-bit unquantized keys"):
+ * logits[g][h][t] = <queries[g][h], keys[g][t]>, all fp32.
+ *   queries device [G][H][d]; keys device [G][N][d]; logits device [G][H][N].
+ * d % 4 == 0, 1 <= d <= 4096, 1 <= H <= 256. */
+tq_status tq_score_fp32(const float* queries, const float* keys, int64_t n_groups, int n_heads,
+                        int64_t n_tokens, int d, float* logits, void* stream);
+
+/* Device-side status of the plan's last work (TQ_OK or TQ_ETIMEOUT), read
+ * with a synchronous copy; call after synchronising the streams that used it.
+ * Reading clears it. */
+tq_status tq_plan_status(tq_plan* plan);
+
+const char* tq_status_string(tq_status status);
+
+/* Version of the packed layout described above (bumped on any change). */
+int tq_format_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

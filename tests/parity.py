@@ -1,0 +1,94 @@
+"""Comparison rules between the CUDA path and the oracle (shared by the GPU tests).
+
+Tolerances (from the target the build is held to):
+* codes and sign bits are bit-identical, except coordinates within 1e-5 (unit
+  scale) of a decision boundary, or signs with |p_i| <= 1e-5 ||x||; the
+  mismatch rate over all coordinates is <= 1e-5 and no mismatch lies outside
+  those bands;
+* norms: |dn| <= 1e-6 n; |drho| <= 1e-5 n (rho is continuous across a code
+  flip at a boundary);
+* logits from identical packed input: |d logit| <= 1e-4 ||q|| n.
+The oracle decides codes and signs in fp64, the kernels in fp32 (exact fp32
+products, fp32 accumulation); the bands absorb the difference.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import tq_synth
+import vector_quantization_02_b300 as tq
+from oracle import tq_oracle as o
+
+
+class Inputs:
+    """Plan inputs for both sides from one set of seeded draws: the GPU plan is
+    built by the library's own host helpers, the oracle builds its own."""
+
+    def __init__(self, d, bits, mode, rot_seed, proj_seed):
+        self.d, self.bits, self.mode = d, bits, mode
+        self.k = bits - 1 if mode == "prod" else bits
+        self.G_rot = tq_synth.rotation_gaussian(d, rot_seed)
+        self.S = tq_synth.projection(d, proj_seed)
+        self.Pi_o = o.haar_rotation(self.G_rot.numpy()).astype(np.float32)
+        self.c_o = o.codebook_f32(1 << self.k, d)
+        self.S_o = self.S.numpy()
+
+    def plan(self):
+        return tq.Plan.from_seeds(self.d, self.bits, self.G_rot, self.S if self.mode == "prod" else None,
+                                  mode=self.mode)
+
+
+def oracle_encode(inp: Inputs, keys: torch.Tensor):
+    """Oracle encode of keys [G][N][d] (any dtype) -> (bytes, encode dict)."""
+    G, N, d = keys.shape
+    return o.encode_pack(keys.detach().cpu().double().numpy(), inp.Pi_o, inp.S_o, inp.c_o, inp.bits, inp.mode, G, N)
+
+
+def compare_encode(inp: Inputs, gpu_bytes: np.ndarray, keys: torch.Tensor, check_bytes=True) -> dict:
+    """Assert the GPU's packed bytes agree with the oracle's encode of ``keys``."""
+    G, N, d = keys.shape
+    want_bytes, e = oracle_encode(inp, keys)
+    got = o.unpack(gpu_bytes, d, inp.bits, inp.mode, G, N)
+    want = o.unpack(want_bytes, d, inp.bits, inp.mode, G, N)
+    total = G * N * d
+    code_bad = got["idx"] != want["idx"]
+    assert not np.any(code_bad & ~e["code_exempt"]), "code mismatch outside the boundary band"
+    stats = dict(code_mismatch=int(code_bad.sum()), coords=total)
+    mism = code_bad.sum()
+    n = want["n"]
+    assert np.all(np.abs(got["n"] - n) <= 1e-6 * n + 1e-30), "norm mismatch"
+    if inp.mode == "prod":
+        sign_bad = got["z"] != want["z"]
+        assert not np.any(sign_bad & ~e["sign_exempt"]), "sign mismatch outside the zero band"
+        mism += sign_bad.sum()
+        stats["sign_mismatch"] = int(sign_bad.sum())
+        assert np.all(np.abs(got["rho"] - want["rho"]) <= 1e-5 * n + 1e-30), "residual norm mismatch"
+    else:
+        assert np.all(got["rho"] == 0)
+    assert mism <= max(1e-5 * total, 0), f"mismatch rate {mism / total:.2e} above 1e-5"
+    if check_bytes and mism == 0:
+        # every code and sign bit agrees: the plane bytes, including the zero
+        # padding of the last block, are identical
+        nb = -(-N // 128)
+        bb = o.block_bytes(d, inp.bits, inp.mode)
+        plane = bb - 128 * 8
+        gb = gpu_bytes.reshape(G * nb, bb)
+        wb = want_bytes.reshape(G * nb, bb)
+        assert np.array_equal(gb[:, :plane], wb[:, :plane])
+        pad = np.arange(nb * 128) >= N
+        norms_g = gb[:, plane:].reshape(G, nb * 128, 8)
+        assert not np.any(norms_g[:, pad]), "padded tokens' norms are not zero"
+    return stats
+
+
+def qnorms(q: torch.Tensor) -> np.ndarray:
+    return torch.linalg.vector_norm(q.double(), dim=-1).cpu().numpy()          # [G][H]
+
+
+def compare_logits(got: np.ndarray, want: np.ndarray, q: torch.Tensor, n: np.ndarray, tol=1e-4) -> float:
+    """|got - want| <= tol ||q|| n elementwise; got/want [G][H][N], n [G][N]."""
+    bound = tol * qnorms(q)[:, :, None] * n[:, None, :]
+    err = np.abs(got.astype(np.float64) - want)
+    assert np.all(err <= bound + 1e-30), f"max err/bound {np.max(err / (bound + 1e-30)):.3g}"
+    return float(np.max(err / (bound + 1e-30)))

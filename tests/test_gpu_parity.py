@@ -1,0 +1,194 @@
+"""GPU parity of the CUDA path against the oracle, through the C ABI, on small
+seeded inputs that span several token blocks and a ragged tail."""
+import numpy as np
+import pytest
+import torch
+
+import tq_synth
+import vector_quantization_02_b300 as tq
+from oracle import tq_oracle as o
+
+from parity import Inputs, compare_encode, compare_logits, oracle_encode
+
+pytestmark = pytest.mark.gpu
+
+ENCODE_CASES = [
+    # d, G, N, dtype, bits, mode, outliers
+    (128, 1, 1, torch.float32, 3, "prod", False),
+    (128, 2, 127, torch.float16, 3, "prod", True),
+    (128, 1, 128, torch.bfloat16, 2, "prod", True),
+    (128, 3, 129, torch.float32, 4, "prod", False),
+    (128, 2, 300, torch.bfloat16, 3, "prod", True),
+    (128, 1, 4097, torch.float16, 4, "prod", True),
+    (256, 2, 300, torch.float32, 3, "prod", False),
+    (256, 1, 200, torch.bfloat16, 4, "prod", True),
+    (1536, 1, 130, torch.float32, 4, "prod", False),
+    (128, 2, 300, torch.float32, 1, "mse", False),
+    (128, 2, 300, torch.float16, 3, "mse", True),
+    (256, 1, 150, torch.bfloat16, 4, "mse", True),
+]
+
+
+def _case_inputs(d, G, N, dtype, bits, mode, outliers, seed=11):
+    w = tq_synth.small_case(d=d, G=G, N=N, H=4, dtype=dtype, seed=seed, outliers=outliers)
+    inp = Inputs(d, bits, mode, w.seeds["rotation"], w.seeds["projection"])
+    return w, inp
+
+
+@pytest.mark.parametrize("d,G,N,dtype,bits,mode,outliers", ENCODE_CASES)
+def test_encode_matches_oracle(cuda, d, G, N, dtype, bits, mode, outliers):
+    w, inp = _case_inputs(d, G, N, dtype, bits, mode, outliers)
+    keys = tq_synth.keys(w)
+    plan = inp.plan()
+    packed = tq.tq_encode(plan, keys.to(cuda))
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    compare_encode(inp, packed.cpu().numpy(), keys)
+
+
+def test_encode_special_keys(cuda):
+    # zero key, a huge and a tiny key, a basis vector, ties at exact zero
+    d, G, N = 128, 1, 6
+    _, inp = _case_inputs(d, G, N, torch.float32, 3, "prod", False)
+    keys = torch.zeros(G, N, d)
+    keys[0, 1] = torch.randn(d) * 1e6
+    keys[0, 2] = torch.randn(d) * 1e-6
+    keys[0, 3, 5] = 2.0
+    keys[0, 4] = torch.randn(d)
+    keys[0, 5, :] = 1.0
+    plan = inp.plan()
+    packed = tq.tq_encode(plan, keys.to(cuda))
+    torch.cuda.synchronize()
+    compare_encode(inp, packed.cpu().numpy(), keys)
+    u = o.unpack(packed.cpu().numpy(), d, 3, "prod", G, N)
+    assert u["n"][0] == 0 and u["rho"][0] == 0 and np.all(u["z"][0])
+
+
+SCORE_CASES = [
+    # d, G, N, H, bits, mode
+    (128, 1, 1, 1, 3, "prod"),
+    (128, 2, 300, 4, 2, "prod"),
+    (128, 3, 129, 8, 3, "prod"),
+    (128, 1, 4096, 16, 3, "prod"),
+    (128, 2, 257, 4, 4, "prod"),
+    (256, 2, 200, 5, 3, "prod"),
+    (1536, 1, 130, 3, 4, "prod"),
+    (128, 2, 300, 8, 3, "mse"),
+    (256, 1, 140, 4, 1, "mse"),
+]
+
+
+@pytest.mark.parametrize("d,G,N,H,bits,mode", SCORE_CASES)
+def test_score_from_oracle_packed_keys(cuda, d, G, N, H, bits, mode):
+    # identical packed input: the oracle encodes, both sides score its bytes
+    w, inp = _case_inputs(d, G, N, torch.float32, bits, mode, False, seed=23)
+    w = tq_synth.small_case(d=d, G=G, N=N, H=H, seed=23)
+    keys = tq_synth.keys(w)
+    q = tq_synth.queries(w)
+    buf, e = oracle_encode(inp, keys)
+    want = o.score_packed(q.numpy(), buf, inp.Pi_o, inp.S_o, inp.c_o, bits, mode, G, N)
+    plan = inp.plan()
+    got = tq.tq_score(plan, q.to(cuda), torch.from_numpy(buf.copy()).to(cuda), N)
+    torch.cuda.synchronize()
+    n = e["n"].astype(np.float32).astype(np.float64).reshape(G, N)
+    compare_logits(got.cpu().numpy(), want, q, n)
+
+
+@pytest.mark.parametrize("d,G,N,H,k", [(128, 2, 1000, 4, 10), (128, 1, 300, 3, 64), (256, 1, 129, 2, 1),
+                                       (128, 3, 70000, 2, 10)])
+def test_score_top_k(cuda, d, G, N, H, k):
+    w, inp = _case_inputs(d, G, N, torch.float32, 4, "prod", False, seed=31)
+    w = tq_synth.small_case(d=d, G=G, N=N, H=H, seed=31)
+    keys = tq_synth.keys(w)
+    q = tq_synth.queries(w)
+    plan = inp.plan()
+    packed = tq.tq_encode(plan, keys.to(cuda))
+    logits, ts, ti = tq.tq_score(plan, q.to(cuda), packed, N, top_k=k)
+    torch.cuda.synchronize()
+    L = logits.cpu().numpy()
+    want_s, want_i = o.topk(L, k)
+    assert np.array_equal(ti.cpu().numpy(), want_i)
+    assert np.array_equal(ts.cpu().numpy(), want_s)
+
+
+@pytest.mark.parametrize("d,G,N,bits,mode", [(128, 2, 300, 3, "prod"), (256, 1, 129, 4, "prod"),
+                                             (128, 1, 200, 2, "mse")])
+def test_decode_matches_oracle(cuda, d, G, N, bits, mode):
+    w, inp = _case_inputs(d, G, N, torch.float32, bits, mode, False, seed=41)
+    keys = tq_synth.keys(w)
+    buf, e = oracle_encode(inp, keys)
+    want = o.decode_packed(buf, inp.Pi_o, inp.S_o, inp.c_o, d, bits, mode, G, N)
+    plan = inp.plan()
+    got = tq.tq_decode(plan, torch.from_numpy(buf.copy()).to(cuda), G, N)
+    torch.cuda.synchronize()
+    n = e["n"].reshape(G, N, 1)
+    assert np.all(np.abs(got.cpu().numpy() - want) <= 1e-5 * n + 1e-30)
+
+
+def test_decode_score_consistency_on_gpu(cuda):
+    # <q, tq_decode(packed)> == tq_score(q, packed) within 1e-4 ||q|| n
+    d, G, N, H = 128, 2, 300, 4
+    w, inp = _case_inputs(d, G, N, torch.bfloat16, 3, "prod", True, seed=43)
+    w = tq_synth.small_case(d=d, G=G, N=N, H=H, dtype=torch.bfloat16, seed=43, outliers=True)
+    keys = tq_synth.keys(w).to(cuda)
+    q = tq_synth.queries(w).to(cuda)
+    plan = inp.plan()
+    packed = tq.tq_encode(plan, keys)
+    s = tq.tq_score(plan, q, packed, N)
+    x = tq.tq_decode(plan, packed, G, N)
+    torch.cuda.synchronize()
+    via_decode = torch.einsum("ghd,gnd->ghn", q.double(), x.double()).cpu().numpy()
+    n = torch.linalg.vector_norm(keys.double(), dim=-1).cpu().numpy()
+    compare_logits(s.cpu().numpy(), via_decode, q.cpu(), n)
+
+
+@pytest.mark.parametrize("G,N,H,d", [(1, 1, 1, 128), (2, 300, 4, 128), (1, 100, 256, 128), (1, 50, 3, 1536)])
+def test_fp32_baseline(cuda, G, N, H, d):
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(G, H, d, generator=g)
+    x = torch.randn(G, N, d, generator=g)
+    got = tq.tq_score_fp32(q.to(cuda), x.to(cuda))
+    torch.cuda.synchronize()
+    want = o.score_fp32(q.numpy(), x.numpy())
+    bound = 1e-5 * (torch.linalg.vector_norm(q.double(), dim=-1)[:, :, None] *
+                    torch.linalg.vector_norm(x.double(), dim=-1)[:, None, :]).numpy()
+    assert np.all(np.abs(got.cpu().numpy() - want) <= bound)
+
+
+def test_end_to_end_gpu_encode_then_score(cuda):
+    # GPU encode -> GPU score against oracle encode -> oracle score, on the keys
+    # whose codes and signs agree bit for bit (all of them, barring boundary cases)
+    d, G, N, H, bits = 128, 3, 500, 8, 3
+    w, inp = _case_inputs(d, G, N, torch.float16, bits, "prod", True, seed=47)
+    w = tq_synth.small_case(d=d, G=G, N=N, H=H, dtype=torch.float16, seed=47, outliers=True)
+    keys = tq_synth.keys(w)
+    q = tq_synth.queries(w)
+    plan = inp.plan()
+    packed = tq.tq_encode(plan, keys.to(cuda))
+    got = tq.tq_score(plan, q.to(cuda), packed, N)
+    torch.cuda.synchronize()
+    buf, e = oracle_encode(inp, keys)
+    want = o.score_packed(q.numpy(), buf, inp.Pi_o, inp.S_o, inp.c_o, bits, "prod", G, N)
+    gu = o.unpack(packed.cpu().numpy(), d, bits, "prod", G, N)
+    same = (np.all(gu["idx"] == o.unpack(buf, d, bits, "prod", G, N)["idx"], axis=1) &
+            np.all(gu["z"] == e["z"], axis=1)).reshape(G, N)
+    assert same.mean() > 0.99
+    n = e["n"].reshape(G, N)
+    gl = got.cpu().numpy()
+    gl = np.where(same[:, None, :], gl, want)
+    compare_logits(gl, want, q, n)
+
+
+def test_argument_errors_on_gpu(cuda):
+    _, inp = _case_inputs(128, 1, 10, torch.float32, 3, "prod", False)
+    plan = inp.plan()
+    keys = torch.randn(1, 10, 128, device=cuda)
+    packed = tq.tq_encode(plan, keys)
+    bad = torch.empty(plan.packed_bytes(1, 10) + 16, dtype=torch.uint8, device=cuda)[1:]
+    with pytest.raises(tq.TQError) as ei:
+        tq.tq_encode(plan, keys, packed=bad)
+    assert ei.value.status == -2
+    with pytest.raises(tq.TQError):
+        tq.tq_score(plan, torch.randn(1, 300, 128, device=cuda), packed, 10)
+    with pytest.raises(tq.TQError):
+        tq.tq_score(plan, torch.randn(1, 2, 128, device=cuda), packed, 10, top_k=11)

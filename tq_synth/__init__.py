@@ -136,18 +136,33 @@ def _group_scale_index(w: Workload, G: int) -> torch.Tensor:
     return g % (w.layers * w.kv_heads)
 
 
+KEY_CHUNK_GROUPS = 64   # keys are drawn 64 groups at a time (bounded temporaries)
+
+
 def keys(w: Workload, G: int | None = None, N: int | None = None, device="cpu",
          seed_offset: int = 0) -> torch.Tensor:
-    """Keys [G][N][d] in the workload's dtype, drawn on ``device``."""
+    """Keys [G][N][d] in the workload's dtype, drawn on ``device``.
+
+    Groups [64c, 64c + 64) are drawn with seed 1,000,003 * keys_seed + c
+    (+ seed_offset), so that no temporary exceeds 64 groups.
+    """
     G = w.G if G is None else G
     N = w.N if N is None else N
-    z = gaussian((G, N, w.d), w.seeds["keys"] + seed_offset, torch.float32, device)
-    if w.unit_keys:
-        z = z / torch.linalg.vector_norm(z, dim=-1, keepdim=True)
-    elif w.outliers:
+    out = torch.empty((G, N, w.d), dtype=w.key_dtype, device=device)
+    sc = None
+    if w.outliers and not w.unit_keys:
         sc = channel_scales(w).to(device)[_group_scale_index(w, G).to(device)]
-        z = z * sc[:, None, :]
-    return z.to(w.key_dtype)
+    for c0 in range(0, G, KEY_CHUNK_GROUPS):
+        c1 = min(G, c0 + KEY_CHUNK_GROUPS)
+        seed = 1_000_003 * w.seeds["keys"] + c0 // KEY_CHUNK_GROUPS + seed_offset
+        z = gaussian((c1 - c0, N, w.d), seed, torch.float32, device)
+        if w.unit_keys:
+            z /= torch.linalg.vector_norm(z, dim=-1, keepdim=True)
+        elif sc is not None:
+            z *= sc[c0:c1, None, :]
+        out[c0:c1] = z.to(w.key_dtype)
+        del z
+    return out
 
 
 def queries(w: Workload, G: int | None = None, H: int | None = None, device="cpu",

@@ -1,0 +1,186 @@
+// Plan derivation, decode, and the uncompressed fp32 baseline.
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace {
+
+// Out = A B^T in fp64 accumulation, rounded to fp32; A, B, Out are [d][d].
+// Also writes OutT = Out^T.  16x16 tiles.
+__global__ void abt_f64_kernel(const float* __restrict__ A, const float* __restrict__ B, int d,
+                               float* __restrict__ Out, float* __restrict__ OutT) {
+  __shared__ double sa[16][17], sb[16][17];
+  const int r = blockIdx.y * 16 + threadIdx.y;   // row of A
+  const int c = blockIdx.x * 16 + threadIdx.x;   // row of B
+  double acc = 0.0;
+  for (int k0 = 0; k0 < d; k0 += 16) {
+    sa[threadIdx.y][threadIdx.x] = A[(int64_t)(blockIdx.y * 16 + threadIdx.y) * d + k0 + threadIdx.x];
+    sb[threadIdx.y][threadIdx.x] = B[(int64_t)(blockIdx.x * 16 + threadIdx.y) * d + k0 + threadIdx.x];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc = fma(sa[threadIdx.y][k], sb[threadIdx.x][k], acc);
+    __syncthreads();
+  }
+  Out[(int64_t)r * d + c] = (float)acc;
+  OutT[(int64_t)c * d + r] = (float)acc;
+}
+
+__global__ void transpose_kernel(const float* __restrict__ A, int d, float* __restrict__ AT) {
+  __shared__ float tile[32][33];
+  const int x = blockIdx.x * 32 + threadIdx.x, y0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) tile[i][threadIdx.x] = A[(int64_t)(y0 + i) * d + x];
+  __syncthreads();
+  const int xo = blockIdx.y * 32 + threadIdx.x, yo0 = blockIdx.x * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) AT[(int64_t)(yo0 + i) * d + xo] = tile[threadIdx.x][i];
+}
+
+// Decode: out_j = n sum_i Pi[i][j] c[idx_i] + rho kappa sum_i S[i][j] (2 z_i - 1).
+// KB keys per CTA pass; thread j owns output coordinate j (Pi rows read coalesced).
+template <int KB>
+__global__ void __launch_bounds__(256)
+decode_simt_kernel(const uint8_t* __restrict__ packed, int64_t G, int64_t N, Layout lay, CodeParams cp,
+                   float kappa, const float* __restrict__ Pi, const float* __restrict__ S,
+                   float* __restrict__ out) {
+  extern __shared__ float sm[];
+  const int d = lay.d;
+  float* Yt = sm;              // [KB][d] centroid values
+  float* Sg = sm + KB * d;     // [KB][d] +-1
+  __shared__ float s_n[KB], s_r[KB];
+  const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
+  const int tiles_per_block = kTokensPerBlock / KB;
+  const int64_t n_tiles = G * nb * tiles_per_block;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t gb = tile / tiles_per_block;
+    const int64_t g = gb / nb, blk = gb % nb;
+    const int t0 = (int)(tile % tiles_per_block) * KB;
+    const uint8_t* in = packed + gb * lay.block_bytes;
+    __syncthreads();
+    for (int i = threadIdx.x; i < KB * d; i += blockDim.x) {
+      const int kk = i / d, j = i - kk * d;
+      const int c = j / kChunk, wd = (j % kChunk) / 32, b = j % 32;
+      int idx = 0;
+      for (int p = 0; p < lay.k; ++p) {
+        unsigned w = *reinterpret_cast<const unsigned*>(in + lay.plane_off(p, c, t0 + kk) + 4 * wd);
+        idx |= ((w >> b) & 1u) << p;
+      }
+      Yt[i] = cp.c[idx];
+      if (lay.prod) {
+        unsigned w = *reinterpret_cast<const unsigned*>(in + lay.plane_off(lay.k, c, t0 + kk) + 4 * wd);
+        Sg[i] = ((w >> b) & 1u) ? 1.f : -1.f;
+      }
+    }
+    if (threadIdx.x < KB) {
+      float2 nr = *reinterpret_cast<const float2*>(in + lay.norms_off + (int64_t)(t0 + threadIdx.x) * 8);
+      s_n[threadIdx.x] = nr.x;
+      s_r[threadIdx.x] = nr.y * kappa;
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < d; j += blockDim.x) {
+      float a[KB], b[KB];
+#pragma unroll
+      for (int kk = 0; kk < KB; ++kk) a[kk] = b[kk] = 0.f;
+      for (int i = 0; i < d; ++i) {
+        const float pij = __ldg(Pi + (int64_t)i * d + j);
+        const float sij = lay.prod ? __ldg(S + (int64_t)i * d + j) : 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk) {
+          a[kk] = fmaf(pij, Yt[kk * d + i], a[kk]);
+          if (lay.prod) b[kk] = fmaf(sij, Sg[kk * d + i], b[kk]);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < KB; ++kk) {
+        const int64_t tok = blk * kTokensPerBlock + t0 + kk;
+        if (tok < N) out[(g * N + tok) * d + j] = s_n[kk] * a[kk] + (lay.prod ? s_r[kk] * b[kk] : 0.f);
+      }
+    }
+  }
+}
+
+// fp32 baseline: a CTA stages KT keys of one group in shared memory (coalesced),
+// then thread (key, head) computes the dot product; the key row is read with a
+// rotated start so that a warp's 32 keys hit 32 banks.
+template <int KT>
+__global__ void __launch_bounds__(256)
+score_fp32_kernel(const float* __restrict__ q, const float* __restrict__ x, int64_t G, int H, int64_t N, int d,
+                  float* __restrict__ logits) {
+  extern __shared__ float xs[];   // [KT][d]
+  const int64_t ntile = (N + KT - 1) / KT;
+  const int64_t g = blockIdx.x / ntile, tile = blockIdx.x % ntile;
+  const int64_t tok0 = tile * KT;
+  const int kn = (int)(N - tok0 < KT ? N - tok0 : KT);
+  const float* src = x + (g * N + tok0) * d;
+  for (int i = threadIdx.x; i < kn * d; i += blockDim.x) xs[i] = src[i];
+  __syncthreads();
+  const int k = threadIdx.x % KT;
+  for (int h = threadIdx.x / KT; h < H; h += blockDim.x / KT) {
+    if (k >= kn) continue;
+    const float* qh = q + (g * H + h) * d;
+    const float* xr = xs + k * d;
+    float acc = 0.f;
+    int j = k % d;
+    for (int i = 0; i < d; ++i) {
+      acc = fmaf(__ldg(qh + j), xr[j], acc);
+      j = j + 1 == d ? 0 : j + 1;
+    }
+    logits[(g * H + h) * N + tok0 + k] = acc;
+  }
+}
+
+template <int KB>
+cudaError_t launch_decode_kb(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
+                             cudaStream_t s) {
+  const size_t smem = (size_t)2 * KB * p->d * sizeof(float);
+  auto kern = decode_simt_kernel<KB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
+  const int64_t tiles = G * nb * (kTokensPerBlock / KB);
+  int64_t grid = (int64_t)sms * 2;
+  if (grid > tiles) grid = tiles;
+  kern<<<(unsigned)grid, 256, smem, s>>>(packed, G, N, p->lay, p->cp, p->kappa, p->Pi, p->S, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s) {
+  const int d = p->d;
+  dim3 tb(32, 8), tg(d / 32, d / 32);
+  transpose_kernel<<<tg, tb, 0, s>>>(p->Pi, d, p->PiT);
+  if (p->lay.prod) {
+    transpose_kernel<<<tg, tb, 0, s>>>(p->S, d, p->ST);
+    dim3 b16(16, 16), g16(d / 16, d / 16);
+    abt_f64_kernel<<<g16, b16, 0, s>>>(p->S, p->Pi, d, p->M, p->MT);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
+                               cudaStream_t s) {
+  if (G * N == 0) return cudaSuccess;
+  if (p->d <= 128) return launch_decode_kb<16>(p, packed, G, N, out, s);
+  return launch_decode_kb<8>(p, packed, G, N, out, s);
+}
+
+template <int KT>
+static cudaError_t launch_fp32_kt(const float* q, const float* x, int64_t G, int H, int64_t N, int d,
+                                  float* logits, cudaStream_t s) {
+  const size_t smem = (size_t)KT * d * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(score_fp32_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t ntile = (N + KT - 1) / KT;
+  score_fp32_kernel<KT><<<(unsigned)(G * ntile), 256, smem, s>>>(q, x, G, H, N, d, logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, int64_t N, int d,
+                              float* logits, cudaStream_t s) {
+  if (G * N == 0 || H == 0) return cudaSuccess;
+  if (d <= 1024) return launch_fp32_kt<32>(q, x, G, H, N, d, logits, s);
+  return launch_fp32_kt<8>(q, x, G, H, N, d, logits, s);
+}
+
+}  // namespace tq

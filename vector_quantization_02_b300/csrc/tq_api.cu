@@ -1,0 +1,196 @@
+// The C ABI of libtq.so: argument checks, plan lifetime, dispatch.
+// Declarations, layouts and error behaviour are documented in include/tq.h.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "tq_internal.cuh"
+
+using namespace tq;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+tq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ECUDA; }
+
+void free_plan(tq_plan* p) {
+  if (!p) return;
+  float* bufs[] = {p->Pi, p->PiT, p->S, p->ST, p->M, p->MT};
+  for (float* b : bufs)
+    if (b) cudaFree(b);
+  if (p->err) cudaFree(p->err);
+  delete p;
+}
+
+int qs_vectors(const tq_plan* p) { return p->lay.prod ? 2 : 1; }
+
+}  // namespace
+
+extern "C" {
+
+const char* tq_status_string(tq_status s) {
+  switch (s) {
+    case TQ_OK: return "ok";
+    case TQ_EINVAL: return "invalid argument";
+    case TQ_EALIGN: return "pointer not 16-byte aligned";
+    case TQ_EUNSUPPORTED: return "unsupported";
+    case TQ_ECUDA: return "CUDA error";
+    case TQ_ETIMEOUT: return "device wait timed out";
+    case TQ_ENOMEM: return "out of device memory";
+  }
+  return "unknown status";
+}
+
+int tq_format_version(void) { return 1; }
+
+tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
+                         void* stream, tq_plan** out) {
+  if (!out) return TQ_EINVAL;
+  *out = nullptr;
+  if (d < 128 || d > kMaxD || d % 128 != 0) return TQ_EINVAL;
+  if (mode != TQ_PROD && mode != TQ_MSE) return TQ_EINVAL;
+  if (mode == TQ_PROD && (bits < 2 || bits > 4)) return TQ_EINVAL;
+  if (mode == TQ_MSE && (bits < 1 || bits > 4)) return TQ_EINVAL;
+  if (!Pi || !codebook || (mode == TQ_PROD && !S)) return TQ_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  tq_plan* p = new (std::nothrow) tq_plan();
+  if (!p) return TQ_ENOMEM;
+  std::memset(p, 0, sizeof(*p));
+  p->d = d;
+  p->bits = bits;
+  p->mode = mode;
+  cudaGetDevice(&p->device);
+  const int k = mode == TQ_PROD ? bits - 1 : bits;
+  Layout& L = p->lay;
+  L.d = d;
+  L.k = k;
+  L.prod = mode == TQ_PROD;
+  L.planes = k + L.prod;
+  L.C = d / kChunk;
+  L.norms_off = (int64_t)L.planes * L.C * kTokensPerBlock * 16;
+  L.block_bytes = L.norms_off + kTokensPerBlock * 8;
+  p->kappa = (float)(std::sqrt(M_PI / 2.0) / d);
+
+  const size_t mat = (size_t)d * d * sizeof(float);
+  bool ok = cudaMalloc(&p->Pi, mat) == cudaSuccess && cudaMalloc(&p->PiT, mat) == cudaSuccess &&
+            cudaMalloc(&p->err, sizeof(int)) == cudaSuccess;
+  if (ok && L.prod)
+    ok = cudaMalloc(&p->S, mat) == cudaSuccess && cudaMalloc(&p->ST, mat) == cudaSuccess &&
+         cudaMalloc(&p->M, mat) == cudaSuccess && cudaMalloc(&p->MT, mat) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_plan(p);
+    return TQ_ENOMEM;
+  }
+  const int levels = 1 << k;
+  float hc[kMaxLevels];
+  cudaError_t e = cudaMemcpyAsync(p->Pi, Pi, mat, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && L.prod) e = cudaMemcpyAsync(p->S, S, mat, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(hc, codebook, levels * sizeof(float), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->err, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = launch_plan_derive(p, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    free_plan(p);
+    return TQ_ECUDA;
+  }
+  CodeParams& cp = p->cp;
+  cp.L = levels;
+  for (int i = 0; i < kMaxLevels; ++i) cp.c[i] = i < levels ? hc[i] : 0.f;
+  for (int i = 0; i + 1 < kMaxLevels; ++i) cp.t[i] = i + 1 < levels ? 0.5f * (hc[i] + hc[i + 1]) : 0.f;
+  for (int i = 0; i + 1 < levels; ++i) {
+    if (!(hc[i] < hc[i + 1])) {  // must be strictly ascending and finite
+      free_plan(p);
+      return TQ_EINVAL;
+    }
+  }
+  *out = p;
+  return TQ_OK;
+}
+
+tq_status tq_plan_destroy(tq_plan* plan) {
+  if (!plan) return TQ_EINVAL;
+  free_plan(plan);
+  return TQ_OK;
+}
+
+size_t tq_packed_bytes(const tq_plan* p, int64_t G, int64_t N) {
+  if (!p || G < 0 || N < 0) return 0;
+  const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
+  return (size_t)(G * nb) * (size_t)p->lay.block_bytes;
+}
+
+tq_status tq_encode(const tq_plan* p, const void* keys, tq_dtype dtype, int64_t G, int64_t N, void* packed,
+                    void* stream) {
+  if (!p || G < 0 || N < 0) return TQ_EINVAL;
+  if (dtype != TQ_F32 && dtype != TQ_F16 && dtype != TQ_BF16) return TQ_EINVAL;
+  if (G == 0 || N == 0) return TQ_OK;
+  if (!keys || !packed) return TQ_EINVAL;
+  if (!aligned16(keys) || !aligned16(packed)) return TQ_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return from_cuda(launch_encode_simt(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
+}
+
+size_t tq_score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k) {
+  if (!p || G < 0 || H < 1 || N < 0 || top_k < 0) return 0;
+  size_t qs = align256((size_t)G * H * qs_vectors(p) * p->d * sizeof(float));
+  return qs + topk_workspace_bytes(G * H, N, top_k) + 256;
+}
+
+tq_status tq_score(const tq_plan* p, const float* queries, int64_t G, int H, const void* packed, int64_t N,
+                   float* logits, int top_k, float* top_scores, int64_t* top_idx, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (!p || G < 0 || N < 0 || H < 1 || H > 256 || top_k < 0 || top_k > 64) return TQ_EINVAL;
+  if (top_k > 0 && (top_k > N || !top_scores || !top_idx)) return TQ_EINVAL;
+  if (G == 0 || N == 0) return TQ_OK;
+  if (!queries || !packed || !logits || !workspace) return TQ_EINVAL;
+  if (workspace_bytes < tq_score_workspace_bytes(p, G, H, N, top_k)) return TQ_EINVAL;
+  if (!aligned16(queries) || !aligned16(packed) || !aligned16(logits)) return TQ_EALIGN;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_EALIGN;
+  if (top_k > 0 && (!aligned16(top_scores) || !aligned16(top_idx))) return TQ_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* qs = static_cast<float*>(workspace);
+  const size_t qs_bytes = align256((size_t)G * H * qs_vectors(p) * p->d * sizeof(float));
+  cudaError_t e = launch_query_prep(p, queries, G, H, qs, s);
+  if (e == cudaSuccess) e = launch_score_simt(p, qs, G, H, static_cast<const uint8_t*>(packed), N, logits, s);
+  if (e == cudaSuccess && top_k > 0)
+    e = launch_topk(logits, G * H, N, top_k, top_scores, top_idx, static_cast<char*>(workspace) + qs_bytes, s);
+  return from_cuda(e);
+}
+
+tq_status tq_decode(const tq_plan* p, const void* packed, int64_t G, int64_t N, float* out, void* stream) {
+  if (!p || G < 0 || N < 0) return TQ_EINVAL;
+  if (G == 0 || N == 0) return TQ_OK;
+  if (!packed || !out) return TQ_EINVAL;
+  if (!aligned16(packed) || !aligned16(out)) return TQ_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return from_cuda(launch_decode_simt(p, static_cast<const uint8_t*>(packed), G, N, out, s));
+}
+
+tq_status tq_score_fp32(const float* queries, const float* keys, int64_t G, int H, int64_t N, int d, float* logits,
+                        void* stream) {
+  if (G < 0 || N < 0 || H < 1 || H > 256 || d < 1 || d > 4096 || d % 4 != 0) return TQ_EINVAL;
+  if (G == 0 || N == 0) return TQ_OK;
+  if (!queries || !keys || !logits) return TQ_EINVAL;
+  if (!aligned16(queries) || !aligned16(keys) || !aligned16(logits)) return TQ_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return from_cuda(launch_score_fp32(queries, keys, G, H, N, d, logits, s));
+}
+
+tq_status tq_plan_status(tq_plan* p) {
+  if (!p) return TQ_EINVAL;
+  int v = 0;
+  if (cudaMemcpy(&v, p->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ECUDA;
+  if (v != 0) {
+    int zero = 0;
+    if (cudaMemcpy(p->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return TQ_ECUDA;
+    return TQ_ETIMEOUT;
+  }
+  return TQ_OK;
+}
+
+}  // extern "C"

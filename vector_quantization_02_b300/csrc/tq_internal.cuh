@@ -1,0 +1,91 @@
+// Internal declarations shared by libtq's CUDA sources (not installed).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+constexpr int kTokensPerBlock = 128;   // packed layout: tokens per block
+constexpr int kChunk = 128;            // packed layout: coordinates per 16-byte chunk
+constexpr int kMaxLevels = 16;
+constexpr int kMaxD = 2048;
+
+// Codebook and decision boundaries passed by value to kernels.
+struct CodeParams {
+  float c[kMaxLevels];      // ascending centroids (unit-norm scale)
+  float t[kMaxLevels - 1];  // t_i = (c_i + c_{i+1}) / 2, fp32
+  int L;                    // number of centroids
+};
+
+// Geometry of the packed layout for one plan.
+struct Layout {
+  int d;            // head dimension
+  int k;            // code planes
+  int planes;       // k (+1 sign plane in PROD)
+  int C;            // 128-coordinate chunks per plane
+  int prod;         // 1 for TurboQuantProd
+  int64_t block_bytes;  // bytes per 128-token block
+  int64_t norms_off;    // offset of the norm pairs inside a block
+
+  __host__ __device__ int64_t plane_off(int p, int c, int t) const {
+    return ((int64_t)(p * C + c) * kTokensPerBlock + t) * 16;
+  }
+};
+
+}  // namespace tq
+
+struct tq_plan {
+  int d, bits, mode;
+  int device;
+  tq::Layout lay;
+  tq::CodeParams cp;
+  float kappa;        // sqrt(pi/2) / m
+  float* Pi;          // [d][d] row-major, y = Pi u
+  float* PiT;         // [d][d] = Pi^T (coalesced column access in SIMT kernels)
+  float* S;           // [d][d] (PROD)
+  float* ST;          // [d][d] = S^T (PROD)
+  float* M;           // [d][d] = S Pi^T (PROD)
+  float* MT;          // [d][d] = M^T (PROD)
+  int* err;           // device error word
+};
+
+namespace tq {
+
+// ---- launchers (one per kernel family); all return cudaGetLastError()
+cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s);
+cudaError_t launch_encode_simt(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N,
+                               uint8_t* packed, cudaStream_t s);
+cudaError_t launch_query_prep(const tq_plan* p, const float* q, int64_t G, int H, float* qs,
+                              cudaStream_t s);
+cudaError_t launch_score_simt(const tq_plan* p, const float* qs, int64_t G, int H, const uint8_t* packed,
+                              int64_t N, float* logits, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int64_t rows, int64_t N, int k, float* top_scores,
+                        int64_t* top_idx, void* ws, cudaStream_t s);
+cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
+                               cudaStream_t s);
+cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, int64_t N, int d,
+                              float* logits, cudaStream_t s);
+
+size_t topk_workspace_bytes(int64_t rows, int64_t N, int k);
+
+__device__ __forceinline__ float load_key(const void* keys, int dt, int64_t i) {
+  if (dt == TQ_F32) return reinterpret_cast<const float*>(keys)[i];
+  if (dt == TQ_F16) return __half2float(reinterpret_cast<const __half*>(keys)[i]);
+  return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(keys)[i]);
+}
+
+// idx = #{i : t_i < y} (a value on a boundary takes the lower index)
+__device__ __forceinline__ int quantize_index(float y, const CodeParams& cp) {
+  int idx = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxLevels - 1; ++i)
+    if (i < cp.L - 1) idx += (y > cp.t[i]) ? 1 : 0;
+  return idx;
+}
+
+}  // namespace tq
