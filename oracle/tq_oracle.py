@@ -182,15 +182,25 @@ def encode_prod(x, Pi, S, c) -> dict:
     Also returns the exemption masks the parity checker uses: codes within
     1e-5 (unit scale) of a boundary and signs with |p_i| <= 1e-5 ||x||.
     """
+    out = encode_mse(x, Pi, c)
+    out.update(qjl_stage(x, out["idx"], out["n"], Pi, S, c))
+    return out
+
+
+def qjl_stage(x, idx, n, Pi, S, c) -> dict:
+    """The second stage for given first-stage codes ([PT-KR] "2단계"):
+    r = x - n Pi^T c[idx], rho = ||r||, p = S r, z = [p >= 0], plus the sign
+    exemption mask |p_i| <= 1e-5 n.  Also used to form the alternative
+    encoding of a key whose coordinate sits on a code boundary (either code
+    is then acceptable, and the signs follow the code taken)."""
     x = _as64(x)
     S = _as64(S)
-    out = encode_mse(x, Pi, c)
-    r = x - mse_reconstruct(out["idx"], out["n"], Pi, c)
+    n = _as64(n)
+    r = x - mse_reconstruct(idx, n, Pi, c)
     rho = np.sqrt(np.sum(r * r, axis=1))
     p = r @ S.T                                   # p = S r, one key per row
     z = p >= 0.0
-    out.update(r=r, rho=rho, p=p, z=z, sign_exempt=np.abs(p) <= 1e-5 * out["n"][:, None])
-    return out
+    return dict(r=r, rho=rho, p=p, z=z, sign_exempt=np.abs(p) <= 1e-5 * n[:, None])
 
 
 # ----------------------------------------------------------------------------

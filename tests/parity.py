@@ -46,7 +46,12 @@ def oracle_encode(inp: Inputs, keys: torch.Tensor):
 
 
 def compare_encode(inp: Inputs, gpu_bytes: np.ndarray, keys: torch.Tensor, check_bytes=True) -> dict:
-    """Assert the GPU's packed bytes agree with the oracle's encode of ``keys``."""
+    """Assert the GPU's packed bytes agree with the oracle's encode of ``keys``.
+
+    A coordinate within 1e-5 of a boundary may take either neighbouring code;
+    the key's residual, rho and signs then follow the code taken, so such a key
+    is compared against the oracle's own encoding with that boundary resolved
+    the other way (``qjl_stage`` on the alternative codes)."""
     G, N, d = keys.shape
     want_bytes, e = oracle_encode(inp, keys)
     got = o.unpack(gpu_bytes, d, inp.bits, inp.mode, G, N)
@@ -54,19 +59,35 @@ def compare_encode(inp: Inputs, gpu_bytes: np.ndarray, keys: torch.Tensor, check
     total = G * N * d
     code_bad = got["idx"] != want["idx"]
     assert not np.any(code_bad & ~e["code_exempt"]), "code mismatch outside the boundary band"
+    # a flipped code must be the neighbour across the near boundary
+    assert np.all(np.abs(got["idx"][code_bad] - want["idx"][code_bad]) == 1), "flip to a non-neighbour code"
     stats = dict(code_mismatch=int(code_bad.sum()), coords=total)
-    mism = code_bad.sum()
+    mism = int(code_bad.sum())
     n = want["n"]
     assert np.all(np.abs(got["n"] - n) <= 1e-6 * n + 1e-30), "norm mismatch"
     if inp.mode == "prod":
-        sign_bad = got["z"] != want["z"]
-        assert not np.any(sign_bad & ~e["sign_exempt"]), "sign mismatch outside the zero band"
-        mism += sign_bad.sum()
+        z_ref, rho_ref, band = e["z"].copy(), e["rho"].copy(), e["sign_exempt"].copy()
+        flipped = np.where(code_bad.any(axis=1))[0]
+        if flipped.size:
+            x = keys.detach().cpu().double().numpy().reshape(G * N, d)[flipped]
+            alt_idx = want["idx"][flipped].copy()
+            alt_idx[code_bad[flipped]] = got["idx"][flipped][code_bad[flipped]]
+            alt = o.qjl_stage(x, alt_idx, e["n"][flipped], inp.Pi_o, inp.S_o, inp.c_o)
+            z_ref[flipped], rho_ref[flipped], band[flipped] = alt["z"], alt["rho"], alt["sign_exempt"]
+        sign_bad = got["z"] != z_ref
+        bad_rows = np.where((sign_bad & ~band).any(axis=1))[0]
+        assert bad_rows.size == 0, (f"sign mismatch outside the zero band at keys {bad_rows[:8]} "
+                                    f"({int((sign_bad & ~band).sum())} signs)")
+        mism += int(sign_bad.sum())
         stats["sign_mismatch"] = int(sign_bad.sum())
-        assert np.all(np.abs(got["rho"] - want["rho"]) <= 1e-5 * n + 1e-30), "residual norm mismatch"
+        stats["boundary_flipped_keys"] = int(flipped.size)
+        assert np.all(np.abs(got["rho"] - rho_ref.astype(np.float32)) <= 1e-5 * n + 1e-30), "residual norm mismatch"
     else:
         assert np.all(got["rho"] == 0)
-    assert mism <= max(1e-5 * total, 0), f"mismatch rate {mism / total:.2e} above 1e-5"
+    # the rate can only be resolved on large samples: below 10^6 coordinates a
+    # couple of band-exempt flips are allowed, above it the rate must be <= 1e-5
+    assert mism <= max(1e-5 * total, 2 if total < 10 ** 6 else 0), \
+        f"mismatch rate {mism / total:.2e} above 1e-5 ({mism} of {total})"
     if check_bytes and mism == 0:
         # every code and sign bit agrees: the plane bytes, including the zero
         # padding of the last block, are identical
