@@ -141,6 +141,30 @@ tq_status tq_score(const tq_plan* plan, const float* queries, int64_t n_groups, 
                    float* top_scores, int64_t* top_idx, void* workspace,
                    size_t workspace_bytes, void* stream);
 
+/* The pages have no counterpart to this entry point: it is a variant of
+ * tq_score for callers that cannot allocate device memory -- for example a
+ * plugin running inside a runtime that owns all device memory through its own
+ * pool (allocating behind the host's back would break its budget), or a
+ * latency-critical caller that cannot afford cudaMalloc's device
+ * synchronisation.  It computes exactly what tq_score computes, with the same
+ * arguments minus the workspace: the scratch comes from one fixed array of
+ * TQ_SCORE_NOALLOC_MAX_BYTES in the library's device image, which every GPU
+ * that loads the library holds until the process exits.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree).
+ *  - Requests whose tq_score_workspace_bytes(...) exceeds the maximum return
+ *    TQ_EUNSUPPORTED and enqueue nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array: calls whose work overlaps on the GPU
+ *    (several streams or threads) race and must be serialised by the caller.
+ *    The array keeps the last call's contents; nothing in it needs clearing.
+ * Errors: as tq_score, plus TQ_EUNSUPPORTED. */
+#define TQ_SCORE_NOALLOC_MAX_BYTES (32u << 20)
+tq_status tq_score_noalloc(const tq_plan* plan, const float* queries, int64_t n_groups, int n_heads,
+                           const void* packed, int64_t n_tokens, float* logits, int top_k,
+                           float* top_scores, int64_t* top_idx, void* stream);
+
 /* Reconstruct keys ([PT-KR] usage listing: ``tq.decompress``):
  * x_hat = n Pi^T c[idx] + rho sqrt(pi/2)/m S^T (2z - 1)  (TQ_MSE: first term),
  * so that <q, x_hat> equals tq_score's logit.  out: device fp32 [G][N][d]. */

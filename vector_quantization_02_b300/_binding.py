@@ -24,7 +24,7 @@ _MODES = {"prod": TQ_PROD, "mse": TQ_MSE}
 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(_LIB_PATH):
-        raise ImportError(f"libtq.so not built ({_LIB_PATH}); run `python -m vector_quantization_02_b300.build`")
+        raise ImportError(f"libtq.so not built ({_LIB_PATH}); run `python vector_quantization_02_b300/build.py`")
     lib = ctypes.CDLL(_LIB_PATH)
     c_int, c_i64, c_sz, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
     sig = {
@@ -41,6 +41,7 @@ def _load() -> ctypes.CDLL:
         "tq_plan_status": (c_int, [vp]),
         "tq_status_string": (ctypes.c_char_p, [c_int]),
         "tq_format_version": (c_int, []),
+        "tq_score_noalloc": (c_int, [vp, vp, c_i64, c_int, vp, c_i64, vp, c_int, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -52,7 +53,8 @@ def _load() -> ctypes.CDLL:
 lib = _load()
 EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_plan_destroy",
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
-            "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version")
+            "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc")
+TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
 
 
 class TQError(RuntimeError):
@@ -224,3 +226,30 @@ def tq_score_fp32(queries: torch.Tensor, keys: torch.Tensor, logits: torch.Tenso
                              _dev(logits, "logits", torch.float32, (G, H, N)), ctypes.c_void_p(_stream(stream))),
            "tq_score_fp32")
     return logits
+
+
+def tq_score_noalloc(plan: Plan, queries: torch.Tensor, packed: torch.Tensor, N: int, top_k: int = 0,
+                     logits: torch.Tensor | None = None, top_scores: torch.Tensor | None = None,
+                     top_idx: torch.Tensor | None = None, stream=None):
+    """tq_score without a workspace argument, for callers that may not allocate
+    device memory: the library takes its scratch from a fixed device array
+    (TQ_SCORE_NOALLOC_MAX_BYTES).  Outputs must be passed in by such callers;
+    when they are omitted this wrapper creates them (the C entry point itself
+    never allocates)."""
+    G, H, d = queries.shape
+    dev = queries.device
+    if packed.numel() < plan.packed_bytes(G, N):
+        raise ValueError("packed buffer too small for (G, N)")
+    if logits is None:
+        logits = torch.empty(G, H, N, dtype=torch.float32, device=dev)
+    if top_k and top_scores is None:
+        top_scores = torch.empty(G, H, top_k, dtype=torch.float32, device=dev)
+    if top_k and top_idx is None:
+        top_idx = torch.empty(G, H, top_k, dtype=torch.int64, device=dev)
+    st = lib.tq_score_noalloc(plan.handle, _dev(queries, "queries", torch.float32), G, H, _dev(packed, "packed"), N,
+                              _dev(logits, "logits", torch.float32, (G, H, N)), top_k,
+                              _dev(top_scores, "top_scores", torch.float32, (G, H, top_k)) if top_k else None,
+                              _dev(top_idx, "top_idx", torch.int64, (G, H, top_k)) if top_k else None,
+                              ctypes.c_void_p(_stream(stream)))
+    _check(st, "tq_score_noalloc")
+    return (logits, top_scores, top_idx) if top_k else logits

@@ -1,6 +1,7 @@
 """Build libtq.so in-tree with nvcc for sm_103a (B300).
 
-``python -m vector_quantization_02_b300.build`` or ``build()``.  Objects go to
+``python vector_quantization_02_b300/build.py`` (by path: importing the
+package needs the library) or ``__graft_entry__.build()``.  Objects go to
 ``_build/`` at the repository root; the library lands next to this file so that
 it travels with the source tree.
 """

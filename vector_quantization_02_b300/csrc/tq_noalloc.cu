@@ -1,0 +1,82 @@
+// tq_score_noalloc: tq_score for callers that cannot allocate device memory.
+//
+// Some callers of this library are not free to call cudaMalloc.  A plugin
+// hosted inside a larger runtime (an inference server, a framework that owns
+// every byte of device memory through its own pool allocator) is usually
+// forbidden to allocate behind its host's back: doing so can exceed the
+// budget the host reserved and fragments memory it manages.  Latency-critical
+// callers avoid cudaMalloc too, because it can synchronise the device.  Such
+// callers still need the scratch that scoring uses (the rotated and projected
+// queries, and the top-k candidates).  This entry point takes that scratch
+// from one fixed array in device memory that is part of the library image, so
+// the call itself allocates nothing.
+//
+// The array is a file-scope __device__ variable: every GPU on which the
+// library is loaded holds TQ_SCORE_NOALLOC_MAX_BYTES of it until the process
+// exits.  Host code cannot use the array's name as a device address (on the
+// host it names a stand-in object), so the first call on each device looks up
+// the real address with cudaGetSymbolAddress while that device is current and
+// keeps it.  That first call should therefore come before any stream capture.
+//
+// All calls share the one array.  Calls whose work overlaps on the GPU (two
+// streams, or two threads) race on it and must be serialised by the caller.
+// The array keeps whatever the last call left in it; nothing in it needs to
+// start at zero, because every byte the kernels read in a call was written
+// earlier in the same call.
+#include <mutex>
+
+#include "tq_internal.cuh"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_score_scratch[TQ_SCORE_NOALLOC_MAX_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_score_scratch on the current device (looked up once).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_score_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" tq_status tq_score_noalloc(const tq_plan* p, const float* queries, int64_t G, int H, const void* packed,
+                                      int64_t N, float* logits, int top_k, float* top_scores, int64_t* top_idx,
+                                      void* stream) {
+  if (!p || G < 0 || N < 0 || H < 1 || H > 256 || top_k < 0 || top_k > 64) return TQ_EINVAL;
+  if (top_k > 0 && (top_k > N || !top_scores || !top_idx)) return TQ_EINVAL;
+  if (G == 0 || N == 0) return TQ_OK;
+  if (!queries || !packed || !logits) return TQ_EINVAL;
+  if (!aligned16(queries) || !aligned16(packed) || !aligned16(logits)) return TQ_EALIGN;
+  if (top_k > 0 && (!aligned16(top_scores) || !aligned16(top_idx))) return TQ_EALIGN;
+  const size_t need = tq_score_workspace_bytes(p, G, H, N, top_k);
+  if (need == 0 || need > (size_t)TQ_SCORE_NOALLOC_MAX_BYTES) return TQ_EUNSUPPORTED;
+  void* ws = nullptr;
+  if (scratch_address(&ws) != cudaSuccess) return TQ_ECUDA;
+  // same kernels and scratch layout as tq_score: [Pi q, S q][top-k candidates]
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* qs = static_cast<float*>(ws);
+  const int nv = p->lay.prod ? 2 : 1;
+  const size_t qs_bytes = ((size_t)G * H * nv * p->d * sizeof(float) + 255) & ~(size_t)255;
+  cudaError_t e = tq::launch_query_prep(p, queries, G, H, qs, s);
+  if (e == cudaSuccess) e = tq::launch_score_simt(p, qs, G, H, static_cast<const uint8_t*>(packed), N, logits, s);
+  if (e == cudaSuccess && top_k > 0)
+    e = tq::launch_topk(logits, G * H, N, top_k, top_scores, top_idx, static_cast<char*>(ws) + qs_bytes, s);
+  return e == cudaSuccess ? TQ_OK : TQ_ECUDA;
+}
