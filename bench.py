@@ -262,7 +262,10 @@ def run_ours(args, world, rank):
             r["tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
         return r
 
-    enc_roof = roof(enc_bytes, enc_ms, "encode", "k_encode_simt.cu", flops=4 * d * d * G * N)
+    tc = d == 128 and w.key_dtype in (torch.float16, torch.bfloat16)
+    enc_kernel, enc_src = ("encode_tc", "k_encode_tc.cu") if tc else ("encode_simt", "k_encode_simt.cu")
+    enc_roof = roof(enc_bytes, enc_ms, enc_kernel, enc_src, flops=4 * d * d * G * N)
+    enc_roof["kernel"] = enc_kernel
 
     # score alone on a cold L2 (a decode step reads a cache encoded earlier)
     sc_cold = []
@@ -275,7 +278,7 @@ def run_ours(args, world, rank):
         sc_cold.append((a, b))
     torch.cuda.synchronize()
     sc_cold_ms = statistics.median(a.elapsed_time(b) for a, b in sc_cold)
-    sc_roof = roof(sc_bytes, sc_cold_ms, "score", "k_score_simt.cu")
+    sc_roof = roof(sc_bytes, sc_cold_ms, "score_simt", "k_score_simt.cu")
 
     # the uncompressed baseline on the same keys (fp32 copies), cold L2
     base = None
@@ -293,7 +296,7 @@ def run_ours(args, world, rank):
         torch.cuda.synchronize()
         bms = statistics.median(a.elapsed_time(b) for a, b in bt)
         base = {"ms": round(bms, 4), "keys_per_s": G * N / (bms * 1e-3),
-                "roofline": roof(keys32.numel() * 4 + logit_bytes + q_bytes, bms, "fp32", "k_misc.cu"),
+                "roofline": roof(keys32.numel() * 4 + logit_bytes + q_bytes, bms, "score_fp32", "k_misc.cu"),
                 "score_speedup_vs_fp32_keys": round(bms / sc_cold_ms, 3)}
         del keys32, base_l
 
@@ -310,7 +313,8 @@ def run_ours(args, world, rank):
     line = {
         "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16/bf16 tensor (split operands, f32 accumulate) + f32" if tc else "f32",
+        "data": "synthetic",
         "config": {"workload": w.name, "G": G, "N": N, "H": H, "d": d, "bits": bits,
                    "key_dtype": str(w.key_dtype).replace("torch.", ""), "top_k": top_k,
                    "l2": "flushed between steps (2x L2 memset, outside the step events)"},

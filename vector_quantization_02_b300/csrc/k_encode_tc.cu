@@ -1,0 +1,455 @@
+// Encode on the 5th-generation tensor cores (tcgen05 + TMA + TMEM), d = 128,
+// fp16 or bf16 keys, TurboQuantProd.
+//
+// Same computation as the CUDA-core encode ("turboquant-pytorch 소개",
+// "1단계" then "2단계"): y = Pi x, codes idx_j = #{i : n t_i < y_j},
+// r = y - n c[idx] (rotated frame, unnormalised), rho = ||r||,
+// z = [M r >= 0] with M = S Pi^T, so that sign(M r) = sign(S (x - n Pi^T c[idx])).
+//
+// Exactness of the two contractions on fp16/bf16 tensor cores (fp32 accumulate):
+//  E2  keys are exact in their own 16-bit type; Pi is split Pi = Pi_hi + Pi_lo
+//      in that type (fp16: Pi_lo is mostly subnormal, still exact to 2^-24),
+//      so Y = X Pi_hi^T + X Pi_lo^T carries ~2^-17 relative error or better;
+//  E5  the residual and M are split in bf16: P = R_hi M_hi^T + R_hi M_lo^T +
+//      R_lo M_hi^T (the dropped R_lo M_lo^T term is ~2^-18 relative).
+//
+// Work per CTA (persistent, one CTA per SM, 128 keys = one packed block per tile):
+//  warp 0      TMA producer: key tiles (K-major, 128-byte swizzle) into a
+//              2-stage ring; once, the swizzled images of Pi_hi/lo and M_hi/lo.
+//  warp 1      TMEM owner (512 columns) and MMA issuer (one thread).  Issue
+//              order E2(i+1), E5(i) keeps the tensor pipe busy while the
+//              epilogue quantises.
+//  warps 2-9   two epilogue warpgroups; tile i goes to warpgroup i % 2, which
+//              owns TMEM columns [256 b, 256 b + 256): Y/R in the first 128
+//              (the bf16 residual split is written back over the Y columns it
+//              was computed from and is the A operand of E5), P in the last 128.
+//              Thread (warp w, lane l) owns key row 32 (w % 4) + l.
+// Every wait is bounded: on expiry the kernel raises the plan's error word,
+// drains what it issued and frees its TMEM.
+#include <cuda.h>
+
+#include "ptx_sm100.cuh"
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 320;
+constexpr int kStages = 2;
+constexpr uint32_t kOpBytes = 128 * 128 * 2;  // one 128 x 128 16-bit operand image
+constexpr uint32_t kAtomBytes = 128 * 128;    // 128 rows x 64 elements (128 B) per swizzle atom
+constexpr uint32_t kOffPiHi = 0, kOffPiLo = kOpBytes, kOffMHi = 2 * kOpBytes, kOffMLo = 3 * kOpBytes;
+constexpr uint32_t kOffX = 4 * kOpBytes;
+constexpr uint32_t kOffBar = kOffX + kStages * kOpBytes;
+enum {
+  BAR_OPS = 0,
+  BAR_XFULL = 1,
+  BAR_XEMPTY = BAR_XFULL + kStages,
+  BAR_YFULL = BAR_XEMPTY + kStages,
+  BAR_RFULL = BAR_YFULL + 2,
+  BAR_PFULL = BAR_RFULL + 2,
+  BAR_ACCEMPTY = BAR_PFULL + 2,
+  BAR_DONE = BAR_ACCEMPTY + 2,
+  BAR_COUNT = BAR_DONE + 1
+};
+constexpr uint32_t kSmemBytes = kOffBar + BAR_COUNT * 8 + 16 + 1024;  // + slot, + alignment slack
+
+struct EncTcArgs {
+  Layout lay;
+  CodeParams cp;
+  int64_t G, N, nb, n_tiles;
+  const uint8_t* pi_hi;
+  const uint8_t* pi_lo;
+  const uint8_t* m_hi;
+  const uint8_t* m_lo;
+  uint8_t* packed;
+  int* err;
+};
+
+__device__ __forceinline__ void raise(int* err, volatile int* abort) {
+  *abort = 1;
+  atomicExch(err, 1);
+}
+
+template <bool kBF16>
+__device__ __forceinline__ float2 pair_to_float2(uint32_t w) {
+  if constexpr (kBF16) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+}
+
+template <int L, bool kBF16>
+__global__ void __launch_bounds__(kThreads, 1)
+encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
+  constexpr int K = L == 2 ? 1 : L == 4 ? 2 : 3;  // code planes
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = smem_u32(smem);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  auto bar = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(BAR_OPS), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(BAR_XFULL + s), 1);
+      mbar_init(bar(BAR_XEMPTY + s), 1 + 128);  // MMA commit + the owning warpgroup's norm pass
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(BAR_YFULL + b), 1);
+      mbar_init(bar(BAR_RFULL + b), 128);
+      mbar_init(bar(BAR_PFULL + b), 1);
+      mbar_init(bar(BAR_ACCEMPTY + b), 128);
+    }
+    mbar_init(bar(BAR_DONE), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
+
+  const int64_t n_my = blockIdx.x < a.n_tiles ? (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmX);
+      mbar_arrive_expect_tx(bar(BAR_OPS), 4 * kOpBytes);
+      bulk_load(sb + kOffPiHi, a.pi_hi, kOpBytes, bar(BAR_OPS));
+      bulk_load(sb + kOffPiLo, a.pi_lo, kOpBytes, bar(BAR_OPS));
+      bulk_load(sb + kOffMHi, a.m_hi, kOpBytes, bar(BAR_OPS));
+      bulk_load(sb + kOffMLo, a.m_lo, kOpBytes, bar(BAR_OPS));
+      int64_t issued = 0;
+      for (int64_t i = 0; i < n_my; ++i) {
+        const int s = (int)(i % kStages);
+        const uint32_t use = (uint32_t)(i / kStages);
+        if (!mbar_wait(bar(BAR_XEMPTY + s), (use & 1) ^ 1, abort)) {
+          raise(a.err, abort);
+          break;
+        }
+        const int64_t tile = blockIdx.x + i * gridDim.x;
+        const int64_t g = tile / a.nb, blk = tile % a.nb;
+        const int32_t row = (int32_t)(g * a.N + blk * kTokensPerBlock);
+        mbar_arrive_expect_tx(bar(BAR_XFULL + s), kOpBytes);
+        tma_load_2d(sb + kOffX + s * kOpBytes, &tmX, 0, row, bar(BAR_XFULL + s));
+        tma_load_2d(sb + kOffX + s * kOpBytes + kAtomBytes, &tmX, 64, row, bar(BAR_XFULL + s));
+        issued = i + 1;
+      }
+      // no copy may still be landing when the CTA exits: wait for the last loads
+      int dummy = 0;
+      for (int64_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        mbar_wait(bar(BAR_XFULL + (int)(i % kStages)), (uint32_t)(i / kStages) & 1, &dummy);
+      mbar_wait(bar(BAR_OPS), 0, &dummy);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_x = idesc_f16(kBF16 ? 1u : 0u, 128, 128);
+      constexpr uint32_t idesc_r = idesc_f16(1u, 128, 128);
+      bool ok = mbar_wait(bar(BAR_OPS), 0, abort);
+      auto issue_e2 = [&](int64_t i) -> bool {
+        const int s = (int)(i % kStages), b = (int)(i & 1);
+        const uint32_t j = (uint32_t)(i >> 1);
+        if (!mbar_wait(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort)) return false;
+        if (!mbar_wait(bar(BAR_ACCEMPTY + b), (j & 1) ^ 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + 256u * b;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          const uint32_t off = (kb >> 2) * kAtomBytes + (kb & 3) * 32;
+          const uint64_t ad = sdesc_k_sw128(sb + kOffX + s * kOpBytes + off);
+          mma_f16_ss(d, ad, sdesc_k_sw128(sb + kOffPiHi + off), idesc_x, kb > 0);
+          mma_f16_ss(d, ad, sdesc_k_sw128(sb + kOffPiLo + off), idesc_x, 1);
+        }
+        mma_commit(bar(BAR_YFULL + b));
+        mma_commit(bar(BAR_XEMPTY + s));
+        return true;
+      };
+      auto issue_e5 = [&](int64_t i) -> bool {
+        const int b = (int)(i & 1);
+        const uint32_t j = (uint32_t)(i >> 1);
+        if (!mbar_wait(bar(BAR_RFULL + b), j & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t r = tmem + 256u * b, d = r + 128;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          const uint32_t off = (kb >> 2) * kAtomBytes + (kb & 3) * 32;
+          const uint32_t a_hi = r + 32 * (kb >> 1) + 8 * (kb & 1), a_lo = a_hi + 16;
+          const uint64_t mh = sdesc_k_sw128(sb + kOffMHi + off), ml = sdesc_k_sw128(sb + kOffMLo + off);
+          mma_f16_ts(d, a_hi, mh, idesc_r, kb > 0);
+          mma_f16_ts(d, a_hi, ml, idesc_r, 1);
+          mma_f16_ts(d, a_lo, mh, idesc_r, 1);
+        }
+        mma_commit(bar(BAR_PFULL + b));
+        return true;
+      };
+      if (ok && n_my > 0) ok = issue_e2(0);
+      for (int64_t i = 0; ok && i < n_my; ++i) {
+        if (i + 1 < n_my) ok = issue_e2(i + 1);
+        if (ok) ok = issue_e5(i);
+      }
+      if (!ok) raise(a.err, abort);
+      // all issued MMAs complete before TMEM is freed
+      mma_commit(bar(BAR_DONE));
+      int dummy = 0;
+      mbar_wait(bar(BAR_DONE), 0, &dummy);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + 256u * wg;
+    for (int64_t i = wg; i < n_my; i += 2) {
+      const int s = (int)(i % kStages);
+      const uint32_t j = (uint32_t)(i >> 1);
+      const int64_t tile = blockIdx.x + i * gridDim.x;
+      const int64_t blk = tile % a.nb;
+      const bool live = blk * kTokensPerBlock + row < a.N;
+
+      // E1: ||x|| from the staged key row (two 128-byte-swizzled K halves)
+      // every lane polls; the warp proceeds (or gives up) as one, because the
+      // tcgen05 loads and stores below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort))) {
+        raise(a.err, abort);
+        break;
+      }
+      float n2;
+      {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint8_t* xr = smem + kOffX + s * kOpBytes + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 q = *reinterpret_cast<const uint4*>(xr + h * kAtomBytes + ((c ^ (row & 7)) << 4));
+            const float2 f0 = pair_to_float2<kBF16>(q.x), f1 = pair_to_float2<kBF16>(q.y);
+            const float2 f2 = pair_to_float2<kBF16>(q.z), f3 = pair_to_float2<kBF16>(q.w);
+            acc[0] = fmaf(f0.x, f0.x, acc[0]);
+            acc[1] = fmaf(f0.y, f0.y, acc[1]);
+            acc[2] = fmaf(f1.x, f1.x, acc[2]);
+            acc[3] = fmaf(f1.y, f1.y, acc[3]);
+            acc[4] = fmaf(f2.x, f2.x, acc[4]);
+            acc[5] = fmaf(f2.y, f2.y, acc[5]);
+            acc[6] = fmaf(f3.x, f3.x, acc[6]);
+            acc[7] = fmaf(f3.y, f3.y, acc[7]);
+          }
+        }
+        n2 = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      }
+      mbar_arrive(bar(BAR_XEMPTY + s));
+      const float n = sqrtf(n2);
+      // thresholds scaled by n (a zero key compares 0 with the unscaled
+      // boundaries: idx = #{t_i < 0}); centroids scaled by n
+      const float sc = n > 0.f ? n : 1.f;
+      float nt[L - 1], nc[L];
+#pragma unroll
+      for (int q = 0; q < L - 1; ++q) nt[q] = sc * a.cp.t[q];
+#pragma unroll
+      for (int q = 0; q < L; ++q) nc[q] = n * a.cp.c[q];
+
+      // E2 result -> E3 codes, E4 residual; the residual's bf16 split goes back
+      // into the same TMEM columns as the A operand of E5
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_YFULL + wg), j & 1, abort))) {
+        raise(a.err, abort);
+        break;
+      }
+      tc_fence_after();
+      // plane words of the four 32-coordinate chunks shift through pl[p][0..3]
+      // (the chunk loop is not unrolled: the unrolled body overflows the
+      // instruction cache)
+      uint32_t pl[K][4];
+#pragma unroll
+      for (int p = 0; p < K; ++p) pl[p][0] = pl[p][1] = pl[p][2] = pl[p][3] = 0;
+      float rr = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(t_lane + 32 * cc, v);
+        tmem_ld_wait();
+        uint32_t w[K];
+#pragma unroll
+        for (int p = 0; p < K; ++p) w[p] = 0;
+        uint32_t hi[16], lo[16];
+        // coordinates from 31 down to 0: each funnel shift appends one bit, so
+        // coordinate e ends at bit e
+#pragma unroll
+        for (int e = 30; e >= 0; e -= 2) {
+          float r2[2];
+#pragma unroll
+          for (int u = 1; u >= 0; --u) {
+            const float y = __uint_as_float(v[e + u]);
+            // sb[q] = n t_q - y: its sign bit is [y > n t_q] (a tie gives +0)
+            uint32_t sb[L - 1];
+            float cv = nc[0];
+#pragma unroll
+            for (int q = 0; q < L - 1; ++q) {
+              sb[q] = __float_as_uint(nt[q] - y);
+              cv = (int)sb[q] < 0 ? nc[q + 1] : cv;
+            }
+            // bit p of idx = #{q : y > n t_q} is the XOR of the sign bits of
+            // the thresholds q with (q + 1) % 2^p == 0 (the count is monotone)
+#pragma unroll
+            for (int p = 0; p < K; ++p) {
+              uint32_t x = 0;
+#pragma unroll
+              for (int q = 0; q < L - 1; ++q)
+                if (((q + 1) & ((1 << p) - 1)) == 0) x ^= sb[q];
+              w[p] = __funnelshift_l(x, w[p], 1);
+            }
+            const float r = y - cv;
+            rr = fmaf(r, r, rr);
+            r2[u] = r;
+          }
+          const __nv_bfloat162 h = __floats2bfloat162_rn(r2[0], r2[1]);
+          const float2 hf = __bfloat1622float2(h);
+          const __nv_bfloat162 l = __floats2bfloat162_rn(r2[0] - hf.x, r2[1] - hf.y);
+          hi[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+          lo[e >> 1] = *reinterpret_cast<const uint32_t*>(&l);
+        }
+        tmem_st16(t_lane + 32 * cc, hi);
+        tmem_st16(t_lane + 32 * cc + 16, lo);
+#pragma unroll
+        for (int p = 0; p < K; ++p) {
+          pl[p][0] = pl[p][1];
+          pl[p][1] = pl[p][2];
+          pl[p][2] = pl[p][3];
+          pl[p][3] = w[p];
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(BAR_RFULL + wg));
+      const float rho = sqrtf(rr);
+
+      // E5 result -> sign plane
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PFULL + wg), j & 1, abort))) {
+        raise(a.err, abort);
+        break;
+      }
+      tc_fence_after();
+      uint32_t zs[4] = {0, 0, 0, 0};
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(t_lane + 128 + 32 * cc, v);
+        tmem_ld_wait();
+        // shift in the sign bits (coordinate e at bit e), then invert: z = [p >= 0]
+        uint32_t z = 0;
+#pragma unroll
+        for (int e = 31; e >= 0; --e) z = __funnelshift_l(v[e], z, 1);
+        zs[0] = zs[1];
+        zs[1] = zs[2];
+        zs[2] = zs[3];
+        zs[3] = n > 0.f ? ~z : 0xFFFFFFFFu;
+      }
+      tc_fence_before();
+      mbar_arrive(bar(BAR_ACCEMPTY + wg));
+
+      // E6: this key's 16-byte chunks and norms (consecutive rows -> consecutive 16 B)
+      uint8_t* out = a.packed + tile * a.lay.block_bytes;
+#pragma unroll
+      for (int p = 0; p < K; ++p) {
+        const uint4 val = live ? make_uint4(pl[p][0], pl[p][1], pl[p][2], pl[p][3])
+                               : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(out + ((int64_t)p * kTokensPerBlock + row) * 16) = val;
+      }
+      *reinterpret_cast<uint4*>(out + ((int64_t)K * kTokensPerBlock + row) * 16) =
+          live ? make_uint4(zs[0], zs[1], zs[2], zs[3]) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, rho) : make_float2(0.f, 0.f);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+using EncodeTmapFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTmapFn tmap_encoder() {
+  static EncodeTmapFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTmapFn>(p);
+  }
+  return fn;
+}
+
+template <int L, bool kBF16>
+cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, uint8_t* packed, cudaStream_t s) {
+  EncodeTmapFn enc = tmap_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)(G * N)};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&tm, kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   const_cast<void*>(keys), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  EncTcArgs a;
+  a.lay = p->lay;
+  a.cp = p->cp;
+  a.G = G;
+  a.N = N;
+  a.nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
+  a.n_tiles = G * a.nb;
+  const uint8_t* ops = p->tc_ops;
+  a.pi_hi = ops + (kBF16 ? 2 : 0) * kOpBytes;
+  a.pi_lo = ops + (kBF16 ? 3 : 1) * kOpBytes;
+  a.m_hi = ops + 4 * kOpBytes;
+  a.m_lo = ops + 5 * kOpBytes;
+  a.packed = packed;
+  a.err = p->err;
+  auto kern = encode_tc_kernel<L, kBF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t grid = a.n_tiles < sms ? a.n_tiles : sms;
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tm, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool encode_tc_supported(const tq_plan* p, tq_dtype dt) {
+  return p->tc_ops != nullptr && p->d == 128 && p->lay.prod && (dt == TQ_F16 || dt == TQ_BF16) &&
+         p->cp.L >= 2 && p->cp.L <= 8;
+}
+
+cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N, uint8_t* packed,
+                             cudaStream_t s) {
+  const bool bf = dt == TQ_BF16;
+  switch (p->cp.L) {
+    case 2: return bf ? launch_tc<2, true>(p, keys, G, N, packed, s) : launch_tc<2, false>(p, keys, G, N, packed, s);
+    case 4: return bf ? launch_tc<4, true>(p, keys, G, N, packed, s) : launch_tc<4, false>(p, keys, G, N, packed, s);
+    case 8: return bf ? launch_tc<8, true>(p, keys, G, N, packed, s) : launch_tc<8, false>(p, keys, G, N, packed, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tq

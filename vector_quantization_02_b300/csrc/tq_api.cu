@@ -4,6 +4,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <type_traits>
+#include <vector>
 
 #include "tq_internal.cuh"
 
@@ -22,10 +24,59 @@ void free_plan(tq_plan* p) {
   for (float* b : bufs)
     if (b) cudaFree(b);
   if (p->err) cudaFree(p->err);
+  if (p->tc_ops) cudaFree(p->tc_ops);
   delete p;
 }
 
 int qs_vectors(const tq_plan* p) { return p->lay.prod ? 2 : 1; }
+
+// Byte offset of element (n, k) of a 128 x 128 16-bit matrix stored as the
+// tensor cores read a K-major operand with the 128-byte swizzle: two 64-wide
+// K halves of 16 KB; in each, row n at (n / 8) * 1024 + (n % 8) * 128 and its
+// 16-byte chunk c at position c ^ (n % 8).
+size_t sw128_offset(int n, int k) {
+  return (size_t)(k / 64) * 16384 + (size_t)(n / 8) * 1024 + (n % 8) * 128 + ((((k % 64) / 8) ^ (n % 8)) * 16) +
+         (k % 8) * 2;
+}
+
+// Splits a row-major 128 x 128 fp32 matrix into hi + lo in a 16-bit type and
+// writes both swizzled images.
+template <typename T>
+void split_images(const float* A, uint8_t* hi, uint8_t* lo) {
+  for (int n = 0; n < 128; ++n)
+    for (int k = 0; k < 128; ++k) {
+      const float v = A[n * 128 + k];
+      T h, l;
+      float hf;
+      if constexpr (sizeof(T) == 2 && std::is_same<T, __half>::value) {
+        h = __float2half_rn(v);
+        hf = __half2float(h);
+        l = __float2half_rn(v - hf);
+      } else {
+        h = __float2bfloat16_rn(v);
+        hf = __bfloat162float(h);
+        l = __float2bfloat16_rn(v - hf);
+      }
+      std::memcpy(hi + sw128_offset(n, k), &h, 2);
+      std::memcpy(lo + sw128_offset(n, k), &l, 2);
+    }
+}
+
+// Operand images for the tensor-core encode (d = 128, PROD).
+cudaError_t build_tc_ops(tq_plan* p) {
+  constexpr size_t img = 128 * 128 * 2;
+  std::vector<float> Pi(128 * 128), M(128 * 128);
+  std::vector<uint8_t> host(6 * img);
+  cudaError_t e = cudaMemcpy(Pi.data(), p->Pi, Pi.size() * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(M.data(), p->M, M.size() * 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  split_images<__half>(Pi.data(), host.data(), host.data() + img);
+  split_images<__nv_bfloat16>(Pi.data(), host.data() + 2 * img, host.data() + 3 * img);
+  split_images<__nv_bfloat16>(M.data(), host.data() + 4 * img, host.data() + 5 * img);
+  e = cudaMalloc(&p->tc_ops, host.size());
+  if (e == cudaSuccess) e = cudaMemcpy(p->tc_ops, host.data(), host.size(), cudaMemcpyHostToDevice);
+  return e;
+}
 
 }  // namespace
 
@@ -108,6 +159,12 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
       return TQ_EINVAL;
     }
   }
+  if (L.prod && d == 128) {
+    if (build_tc_ops(p) != cudaSuccess) {
+      free_plan(p);
+      return TQ_ECUDA;
+    }
+  }
   *out = p;
   return TQ_OK;
 }
@@ -132,6 +189,8 @@ tq_status tq_encode(const tq_plan* p, const void* keys, tq_dtype dtype, int64_t 
   if (!keys || !packed) return TQ_EINVAL;
   if (!aligned16(keys) || !aligned16(packed)) return TQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (encode_tc_supported(p, dtype))
+    return from_cuda(launch_encode_tc(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
   return from_cuda(launch_encode_simt(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
 }
 

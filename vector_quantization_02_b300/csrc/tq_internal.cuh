@@ -51,6 +51,8 @@ struct tq_plan {
   float* ST;          // [d][d] = S^T (PROD)
   float* M;           // [d][d] = S Pi^T (PROD)
   float* MT;          // [d][d] = M^T (PROD)
+  uint8_t* tc_ops;    // tensor-core operand images (d = 128, PROD): Pi hi/lo fp16,
+                      // Pi hi/lo bf16, M hi/lo bf16; 32 KB each, K-major 128-byte swizzle
   int* err;           // device error word
 };
 
@@ -60,6 +62,9 @@ namespace tq {
 cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s);
 cudaError_t launch_encode_simt(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N,
                                uint8_t* packed, cudaStream_t s);
+bool encode_tc_supported(const tq_plan* p, tq_dtype dt);
+cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N, uint8_t* packed,
+                             cudaStream_t s);
 cudaError_t launch_query_prep(const tq_plan* p, const float* q, int64_t G, int H, float* qs,
                               cudaStream_t s);
 cudaError_t launch_score_simt(const tq_plan* p, const float* qs, int64_t G, int H, const uint8_t* packed,
