@@ -63,27 +63,48 @@ def kernel_traffic(kernel: str, source: str):
 
 
 class Clocks:
-    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region.
+    A reader thread collects the rows; start() returns once the first sample
+    has arrived, so that the region is covered from its beginning."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device: int):
+        import threading
         self.proc = None
+        self.rows = []
+        # nvidia-smi index of this CUDA device (CUDA_VISIBLE_DEVICES maps CUDA indices)
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        self.index = ids[device] if device < len(ids) and ids[device].isdigit() else str(device)
         try:
-            uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, AttributeError, RuntimeError):
+                ["nvidia-smi", f"--query-gpu=index,{self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
             self.proc = None
+            return
+        self.first = threading.Event()
+
+        def read():
+            for line in self.proc.stdout:
+                if line.count(",") >= 8:
+                    self.rows.append(line.strip().split(","))
+                    self.first.set()
+        self.thread = threading.Thread(target=read, daemon=True)
+        self.thread.start()
+        self.first.wait(timeout=15)
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
-        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 7]
+        self.thread.join(timeout=10)
+        rows = list(self.rows)
+        if len({r[0].strip() for r in rows}) > 1:
+            rows = [r for r in rows if r[0].strip() == self.index]
+        rows = [r[1:] for r in rows]
         sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
         mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -278,7 +299,9 @@ def run_ours(args, world, rank):
         sc_cold.append((a, b))
     torch.cuda.synchronize()
     sc_cold_ms = statistics.median(a.elapsed_time(b) for a, b in sc_cold)
-    sc_roof = roof(sc_bytes, sc_cold_ms, "score_simt", "k_score_simt.cu")
+    sc_tc = d == 128 and H <= 16 and bits <= 4
+    sc_roof = roof(sc_bytes, sc_cold_ms, *(("score_tc", "k_score_tc.cu") if sc_tc else ("score_simt", "k_score_simt.cu")))
+    sc_roof["kernel"] = "score_tc" if sc_tc else "score_simt"
 
     # the uncompressed baseline on the same keys (fp32 copies), cold L2
     base = None

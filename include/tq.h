@@ -72,6 +72,19 @@ typedef struct tq_plan tq_plan;
  * levels in {2,4,8,16}; d >= 1.  Errors: TQ_EINVAL. */
 tq_status tq_lloyd_max_codebook(int levels, int d, float* out);
 
+/* Parity (Walsh) expansion of a codebook of `levels` entries (HOST array,
+ * ascending, levels in {2,4,8,16}) over the bits of its index:
+ *   codebook[idx] = c0 + sum_t coefs[t] * parity(idx & masks[t]),
+ * parity(x) = popcount(x) mod 2.  This is how the tensor-core scorer writes
+ * the MSE term <Pi q, c[idx]> ([PT-KR] usage listing, ``inner_product``) as
+ * dot products with XOR planes of the packed code bits.  Only terms with a
+ * non-zero coefficient are returned, in increasing mask order (an exactly
+ * odd-symmetric codebook has none on even-weight masks).  Writes *n_terms
+ * (<= levels - 1) and that many HOST masks/coefs, and *c0 = codebook[0].
+ * Errors: TQ_EINVAL. */
+tq_status tq_codebook_parity_expansion(int levels, const float* codebook, int* n_terms, unsigned* masks,
+                                       double* coefs, double* c0);
+
 /* Random orthogonal rotation from a d x d Gaussian matrix ([PT-KR] 1단계):
  * Pi = Q diag(sign R_ii) for the Householder QR  gaussian = Q R  (fp64),
  * written as fp32 row-major to the HOST array `Pi_out` (y = Pi u).

@@ -90,3 +90,36 @@ def test_library_rotation_rejects_rank_deficient():
     g = torch.zeros(8, 8, dtype=torch.float64)
     with pytest.raises(tq.TQError):
         tq.tq_haar_rotation(g)
+
+
+def _reconstruct(levels, masks, coefs, c0):
+    return np.array([c0 + sum(cf * (bin(i & m).count("1") & 1) for m, cf in zip(masks, coefs))
+                     for i in range(levels)])
+
+
+@pytest.mark.parametrize("levels", [2, 4, 8, 16])
+def test_parity_expansion_of_the_lloyd_max_codebook(levels):
+    # the odd-symmetric codebook has weight only on odd-weight masks: k planes
+    # for k <= 2, k + 1 for k = 3 (the triple product), 8 for k = 4
+    c = tq.tq_lloyd_max_codebook(levels, 128)
+    masks, coefs, c0 = tq.tq_codebook_parity_expansion(c)
+    assert all(bin(m).count("1") % 2 == 1 for m in masks)
+    assert len(masks) == {2: 1, 4: 2, 8: 4, 16: 8}[levels]
+    assert np.max(np.abs(_reconstruct(levels, masks, coefs, c0) - c.numpy().astype(np.float64))) <= 1e-15
+    # k = 1 (two levels, -a and a): one plane with weight 2a
+    if levels == 2:
+        assert masks == [1] and coefs[0] == 2 * float(c[1]) and c0 == float(c[0])
+
+
+def test_parity_expansion_of_an_asymmetric_codebook():
+    # a codebook with no symmetry needs every mask; the expansion is still exact
+    c = torch.tensor([-1.5, -0.25, 0.125, 2.0, 2.5, 3.0, 7.0, 7.5])
+    masks, coefs, c0 = tq.tq_codebook_parity_expansion(c)
+    assert masks == list(range(1, 8))
+    assert np.array_equal(_reconstruct(8, masks, coefs, c0), c.numpy().astype(np.float64))
+    # a uniform (affine) codebook is linear in the bits: only the single-bit masks
+    u = torch.tensor([0.0, 1.0, 2.0, 3.0]) * 0.5 - 0.75
+    masks, coefs, c0 = tq.tq_codebook_parity_expansion(u)
+    assert masks == [1, 2] and coefs == [0.5, 1.0] and c0 == -0.75
+    with pytest.raises(tq.TQError):
+        tq.tq_codebook_parity_expansion(torch.zeros(3))

@@ -75,6 +75,14 @@ SCORE_CASES = [
     (1536, 1, 130, 3, 4, "prod"),
     (128, 2, 300, 8, 3, "mse"),
     (256, 1, 140, 4, 1, "mse"),
+    # tensor-core path: many groups per CTA (query images change mid-range),
+    # padded heads, ragged tails, MSE with one and three code bits
+    (128, 300, 200, 4, 3, "prod"),
+    (128, 5, 1000, 12, 3, "prod"),
+    (128, 3, 129, 16, 2, "prod"),
+    (128, 4, 700, 2, 4, "prod"),
+    (128, 2, 260, 7, 1, "mse"),
+    (128, 1, 385, 16, 4, "mse"),
 ]
 
 

@@ -42,6 +42,7 @@ def _load() -> ctypes.CDLL:
         "tq_status_string": (ctypes.c_char_p, [c_int]),
         "tq_format_version": (c_int, []),
         "tq_score_noalloc": (c_int, [vp, vp, c_i64, c_int, vp, c_i64, vp, c_int, vp, vp, vp]),
+        "tq_codebook_parity_expansion": (c_int, [c_int, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -53,7 +54,8 @@ def _load() -> ctypes.CDLL:
 lib = _load()
 EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_plan_destroy",
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
-            "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc")
+            "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
+            "tq_codebook_parity_expansion")
 TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
 
 
@@ -104,6 +106,20 @@ def tq_haar_rotation(gaussian: torch.Tensor) -> torch.Tensor:
     _check(lib.tq_haar_rotation(d, ctypes.c_void_p(g.data_ptr()), ctypes.c_void_p(out.data_ptr())),
            "tq_haar_rotation")
     return out
+
+
+def tq_codebook_parity_expansion(codebook: torch.Tensor):
+    """Parity expansion of a host codebook: (masks, coefs, c0) with
+    codebook[idx] = c0 + sum_t coefs[t] * parity(idx & masks[t])."""
+    c = codebook.detach().to("cpu", torch.float32).contiguous()
+    L = c.numel()
+    n = ctypes.c_int(0)
+    masks = (ctypes.c_uint * max(1, L - 1))()
+    coefs = (ctypes.c_double * max(1, L - 1))()
+    c0 = ctypes.c_double(0.0)
+    _check(lib.tq_codebook_parity_expansion(L, ctypes.c_void_p(c.data_ptr()), ctypes.byref(n), masks, coefs,
+                                            ctypes.byref(c0)), "tq_codebook_parity_expansion")
+    return [int(masks[i]) for i in range(n.value)], [float(coefs[i]) for i in range(n.value)], c0.value
 
 
 # ---------------------------------------------------------------- plan

@@ -1,0 +1,760 @@
+// Score on the 5th-generation tensor cores (tcgen05, fp8 operands, A operand in
+// TMEM), d = 128, up to 16 query heads per group.
+//
+// Computes the same estimate as the CUDA-core score ("turboquant-pytorch 소개",
+// usage listing ``tq.inner_product(query, compressed)`` and "2단계"):
+//     logit = n <Pi q, c[idx]> + rho sqrt(pi/2)/m <S q, 2z - 1>.
+//
+// Bit-plane form.  The codebook is written in its parity (Walsh) expansion over
+// the k code bits, c[idx] = c0 + sum_T gamma_T x_T(idx), where x_T(idx) is the
+// XOR of the bits of idx selected by the mask T.  For an odd-symmetric codebook
+// (the Lloyd-Max codebook of a symmetric density) only odd-weight masks carry
+// weight: {1} for k = 1, {1, 2} for k = 2, {1, 2, 4, 7} for k = 3.  Hence
+//     <Pi q, c[idx]> = c0 sum(Pi q) + sum_T <gamma_T Pi q, x_T>,
+//     <S q, 2z - 1>  = <2 S q, z> - sum(S q),
+// i.e. per key a sum of dot products between 0/1 bit planes and real query
+// vectors: a dense contraction [128 keys x 128 K] . [128 K x N] per plane.
+//
+// Exactness.  Each key bit becomes an e4m3 value that is an exact power of two:
+// a 32-coordinate plane word W yields eight 32-bit TMEM words (four e4m3 each)
+// with two shifts and eight ANDs; every byte of output word o holds one source
+// bit at bit position 3 + o % 4 of the byte, i.e. the e4m3 value 2^-6, 2^-5,
+// 2^-3 or 2.  The query side carries the reciprocal power of two and a
+// per-(head, term) power-of-two normalisation, and is split into four e4m3
+// slices q = s0 + s1/16 + s2/256 + s3/4096 (about 2^-16 relative), one group
+// of N = 4 Hp columns each.  Every product is exact; the accumulation is fp32.
+//
+// Work per CTA (persistent, contiguous range of 128-token blocks), four roles
+// that only meet at mbarriers, so expansion never waits for an epilogue:
+//  warps 0-3    MMA issuers, tile i to warp i % 4 (one elected lane each: a
+//               single thread issues one tcgen05.mma about every 50 cycles, and
+//               every mbarrier operation costs it ~150 cycles, so a tile is one
+//               job: two waits, all its MMAs - the MMA-term planes into one
+//               accumulator, the sign plane into another - and two commits).
+//               The issuers take their barrier waits strictly in tile order (a
+//               turn counter in shared memory): a parity wait cannot tell phase
+//               k from phase k + 2, so a ring entry's uses must be waited for by
+//               one sequence of waits.  Their MMA issue still overlaps.
+//               Warp 0 owns the TMEM allocation (512 columns).
+//  warps 4-11   two expansion warpgroups; tile i goes to warpgroup i % 2.
+//               Thread (warp w, lane l) owns key row 32 (w % 4) + l: it reads its
+//               16-byte plane chunks from the staged block and writes all the
+//               tile's expanded planes into one group of 32-column TMEM slots
+//               (a ring of SG groups, SG even so that every group is always
+//               filled by the same warpgroup), then arrives once.
+//  warps 12-19  two epilogue warpgroups; tile i goes to warpgroup i % 2.  They
+//               read the accumulators of a tile (a ring of DS stages, DS even), combine
+//               slices and terms with the key's norms, and store H logits (one
+//               coalesced store per head).
+//  warp 20      producer: bulk copies of packed blocks (8-stage ring) and of the
+//               per-group query operand images (double-buffered).
+// Every wait is bounded: on expiry the kernel raises the plan's error word,
+// drains what it issued and frees its TMEM.
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "ptx_sm100.cuh"
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace {
+
+using namespace ptx;
+
+constexpr int kIssuers = 4;
+constexpr int kExpWarps = 8;        // two expansion warpgroups
+constexpr int kEpiWarps = 8;        // two epilogue warpgroups
+constexpr int kThreads = 32 * (kIssuers + kExpWarps + kEpiWarps + 1);
+constexpr int kExpWarp0 = kIssuers, kEpiWarp0 = kIssuers + kExpWarps, kProducerWarp = kEpiWarp0 + kEpiWarps;
+constexpr int kStages = 8;          // packed-block ring (power of two)
+constexpr int kMaxGroups = 4;       // TMEM plane-slot groups (one tile each)
+constexpr int kMaxDStages = 4;      // accumulator stages
+constexpr int kSlices = 4;          // e4m3 slices of the query operand
+constexpr int kPlaneCols = 32;      // TMEM columns of one expanded plane (128 e4m3)
+
+enum {
+  BAR_FULL = 0,
+  BAR_EMPTY = BAR_FULL + kStages,
+  BAR_BFULL = BAR_EMPTY + kStages,
+  BAR_BEMPTY = BAR_BFULL + 2,
+  BAR_PFULL = BAR_BEMPTY + 2,
+  BAR_PEMPTY = BAR_PFULL + kMaxGroups,
+  BAR_DFULL = BAR_PEMPTY + kMaxGroups,
+  BAR_DEMPTY = BAR_DFULL + kMaxDStages,
+  BAR_DONE = BAR_DEMPTY + kMaxDStages,
+  BAR_COUNT = BAR_DONE + kIssuers
+};
+
+// reciprocal of the e4m3 value of bit 3 + i of a byte (2^-6, 2^-5, 2^-3, 2)
+__constant__ float c_comp[4] = {64.f, 32.f, 8.f, 0.5f};
+// source bit (within each byte of the plane word) of expanded word o
+__constant__ int c_src[8] = {3, 4, 5, 6, 0, 1, 2, 7};
+
+// MMA-term planes of an odd-symmetric codebook with k code bits.
+__host__ __device__ constexpr int planes_of(int k) { return k == 3 ? 4 : k; }
+
+struct ScoreTcArgs {
+  Layout lay;
+  int H, Hp;                  // heads, padded heads (4, 8 or 16)
+  int SG, DS;                 // TMEM plane-slot groups, accumulator stages
+  uint32_t slot0;             // first slot column (groups of NP x 32 columns)
+  uint32_t img_bytes;         // per group: planes x (4 Hp rows x 128 B)
+  int64_t N, nb, n_tiles;
+  const uint8_t* packed;
+  const uint8_t* images;      // [G][img_bytes]
+  const float4* consts;       // [G][Hp] {1/sigma_A, c0 sum(Pi q), 1/sigma_B, -sum(S q)}
+  float kappa;
+  float* logits;
+  int* err;
+};
+
+__device__ __forceinline__ void raise(int* err, volatile int* abort) {
+  *abort = 1;
+  atomicExch(err, 1);
+}
+
+// Eight TMEM words (32 e4m3 values) from one 32-coordinate plane word.
+__device__ __forceinline__ void expand_word(uint32_t W, uint32_t* o) {
+  const uint32_t b = W << 3, c = W >> 1;
+  o[0] = W & 0x08080808u;
+  o[1] = W & 0x10101010u;
+  o[2] = W & 0x20202020u;
+  o[3] = W & 0x40404040u;
+  o[4] = b & 0x08080808u;
+  o[5] = b & 0x10101010u;
+  o[6] = b & 0x20202020u;
+  o[7] = c & 0x40404040u;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate)
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::f8f6f4: e4m3 A and B, fp32 accumulate, K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Position in a ring of n entries: index and the parity of the pass over it.
+struct Ring {
+  uint32_t idx = 0, phase = 0;
+  __device__ __forceinline__ void advance(uint32_t by, uint32_t n) {
+    idx += by;
+    while (idx >= n) {
+      idx -= n;
+      phase ^= 1u;
+    }
+  }
+};
+
+// (group, block) of a tile, advanced without divisions.
+struct TilePos {
+  uint32_t g = 0, blk = 0;
+  __device__ __forceinline__ void init(int64_t tile, int64_t nb) {
+    g = (uint32_t)(tile / nb);
+    blk = (uint32_t)(tile - (int64_t)g * nb);
+  }
+  __device__ __forceinline__ void advance(uint32_t by, uint32_t nb) {
+    blk += by;
+    while (blk >= nb) {
+      blk -= nb;
+      ++g;
+    }
+  }
+};
+
+// Tokens' accumulators of one term: sum over slices of D[slice * HP + h] / 16^slice.
+template <int HP>
+__device__ __forceinline__ void load_term(uint32_t taddr, float (&acc)[HP]) {
+  constexpr int N = kSlices * HP;
+#pragma unroll
+  for (int h = 0; h < HP; ++h) acc[h] = 0.f;
+#pragma unroll
+  for (int c0 = 0; c0 < N; c0 += 16) {
+    uint32_t v[16];
+    tmem_ld16(taddr + c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int col = c0 + e, sl = col / HP, h = col % HP;
+      const float w = sl == 0 ? 1.f : sl == 1 ? 0.0625f : sl == 2 ? 0.00390625f : 0.000244140625f;
+      acc[h] = fmaf(__uint_as_float(v[e]), w, acc[h]);
+    }
+  }
+}
+
+template <int HP, int K, int PROD>
+__global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs a) {
+  constexpr int N = kSlices * HP;               // MMA N: slice-major rows of the query image
+  constexpr int NA = planes_of(K);              // MMA-term planes
+  constexpr int NP = NA + PROD;                 // planes per tile
+  constexpr int NJ = 1 + PROD;                  // MMA jobs per tile
+  constexpr uint32_t kStageMask = kStages - 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t off_ring = 2 * a.img_bytes;
+  const uint32_t blk_bytes = (uint32_t)a.lay.block_bytes;
+  const uint32_t off_bar = (off_ring + kStages * blk_bytes + 7) & ~7u;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ uint32_t s_turn;              // tile whose issuer may take its waits
+  __shared__ float4 s_cst[kEpiWarps][HP];  // constants of each epilogue warp's current tile
+  auto bar = [&](int i) { return sb + off_bar + 8u * (uint32_t)i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t SG = (uint32_t)a.SG, DS = (uint32_t)a.DS, nb = (uint32_t)a.nb;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    s_turn = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(BAR_FULL + s), 1);
+      mbar_init(bar(BAR_EMPTY + s), 256);  // one expansion and one epilogue warpgroup
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(BAR_BFULL + b), 1);
+      mbar_init(bar(BAR_BEMPTY + b), kIssuers);
+    }
+    for (int s = 0; s < kMaxGroups; ++s) {
+      mbar_init(bar(BAR_PFULL + s), 128);
+      mbar_init(bar(BAR_PEMPTY + s), 1);
+    }
+    for (int d = 0; d < kMaxDStages; ++d) {
+      mbar_init(bar(BAR_DFULL + d), 1);
+      mbar_init(bar(BAR_DEMPTY + d), 128);
+    }
+    for (int w = 0; w < kIssuers; ++w) mbar_init(bar(BAR_DONE + w), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
+
+  const int64_t t_begin = blockIdx.x * a.n_tiles / gridDim.x;
+  const uint32_t n_my = (uint32_t)((blockIdx.x + 1) * a.n_tiles / gridDim.x - t_begin);
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      TilePos pos;
+      pos.init(t_begin, a.nb);
+      uint32_t epoch = 0, issued = 0;
+      bool ok = true, have_img = false;
+      const uint8_t* src = a.packed + t_begin * a.lay.block_bytes;
+      for (uint32_t i = 0; i < n_my; ++i, src += blk_bytes) {
+        if (i > 0) {
+          const uint32_t g0 = pos.g;
+          pos.advance(1, nb);
+          if (pos.g != g0) ++epoch;
+        }
+        if (i == 0 || pos.blk == 0) {  // a new group: its query operand image
+          const uint32_t b = epoch & 1u;
+          if (!mbar_wait_suspend(bar(BAR_BEMPTY + b), ((epoch >> 1) & 1u) ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(BAR_BFULL + b), a.img_bytes);
+          bulk_load(sb + b * a.img_bytes, a.images + (int64_t)pos.g * a.img_bytes, a.img_bytes, bar(BAR_BFULL + b));
+          have_img = true;
+        }
+        const uint32_t s = i & kStageMask;
+        if (!mbar_wait_suspend(bar(BAR_EMPTY + s), ((i / kStages) & 1u) ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(BAR_FULL + s), blk_bytes);
+        bulk_load(sb + off_ring + s * blk_bytes, src, blk_bytes, bar(BAR_FULL + s));
+        issued = i + 1;
+      }
+      if (!ok) raise(a.err, abort);
+      // no copy may still be landing when the CTA exits
+      int dummy = 0;
+      for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        mbar_wait(bar(BAR_FULL + (i & kStageMask)), (i / kStages) & 1u, &dummy);
+      if (have_img) {
+        for (uint32_t e = epoch > 0 ? epoch - 1 : 0; e <= epoch; ++e)
+          mbar_wait(bar(BAR_BFULL + (e & 1u)), (e >> 1) & 1u, &dummy);
+      }
+    }
+  } else if (warp < kIssuers) {
+    // ------------------------------------------------------------ MMA issuers
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3(128, N);
+      TilePos pos;
+      pos.init(t_begin, a.nb);
+      uint32_t epoch = 0;
+      Ring group, stage;  // plane-slot group and accumulator stage of tile i
+      bool need_b = true, ok = true;
+      for (uint32_t i = 0; ok && i < n_my; ++i, group.advance(1, SG), stage.advance(1, DS)) {
+        if (i > 0) {
+          const uint32_t g0 = pos.g;
+          pos.advance(1, nb);
+          if (pos.g != g0) {
+            // this warp's MMAs on the previous group's image are all issued
+            mma_commit(bar(BAR_BEMPTY + (epoch & 1u)));
+            ++epoch;
+            need_b = true;
+          }
+        }
+        if ((i & (kIssuers - 1)) != (uint32_t)warp) continue;
+        // wait for this tile's turn (the previous tile's issuer has passed its waits)
+        {
+          const volatile uint32_t* turn = &s_turn;
+          uint32_t it = 0;
+          while (*turn != i && it < kWaitLimit) {
+            if ((++it & 63) == 0 && *abort) it = kWaitLimit;
+          }
+          if (*turn != i) {
+            ok = false;
+            break;
+          }
+        }
+        if (need_b) {
+          if (!mbar_wait_suspend(bar(BAR_BFULL + (epoch & 1u)), (epoch >> 1) & 1u, abort)) {
+            ok = false;
+            break;
+          }
+          need_b = false;
+        }
+        if (!mbar_wait_suspend(bar(BAR_PFULL + group.idx), group.phase, abort) ||
+            !mbar_wait_suspend(bar(BAR_DEMPTY + stage.idx), stage.phase ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        *static_cast<volatile uint32_t*>(&s_turn) = i + 1;
+        tc_fence_after();
+        const uint32_t img = sb + (epoch & 1u) * a.img_bytes;
+        const uint32_t d = tmem + stage.idx * (uint32_t)(NJ * N);
+        const uint32_t at = tmem + a.slot0 + group.idx * (uint32_t)(NP * kPlaneCols);
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          // plane p of the image: N rows x 128 B (one swizzle atom column);
+          // K step kb starts 32 bytes further (2 in descriptor units)
+          const uint64_t b0 = sdesc_k_sw128(img + (uint32_t)p * (uint32_t)N * 128u);
+          const uint32_t dp = p < NA ? d : d + N;
+#pragma unroll
+          for (uint32_t kb = 0; kb < 4; ++kb)
+            mma_f8_ts(dp, at + (uint32_t)(p * kPlaneCols) + 8u * kb, b0 + 2u * kb, idesc,
+                      ((p > 0 && p < NA) || kb > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(BAR_PEMPTY + group.idx));
+        mma_commit(bar(BAR_DFULL + stage.idx));
+      }
+      if (!ok) raise(a.err, abort);
+      mma_commit(bar(BAR_DONE + warp));
+      int dummy = 0;
+      mbar_wait(bar(BAR_DONE + warp), 0, &dummy);
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ expansion
+    const uint32_t wg = (uint32_t)(warp - kExpWarp0) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + a.slot0;
+    Ring group;
+    group.advance(wg, SG);
+    for (uint32_t i = wg; i < n_my; i += 2, group.advance(2, SG)) {
+      const uint32_t s = i & kStageMask;
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_FULL + s), (i / kStages) & 1u, abort))) {
+        raise(a.err, abort);
+        break;
+      }
+      const uint8_t* blkp = smem + off_ring + s * blk_bytes;
+      uint4 w[NP];
+#pragma unroll
+      for (int q = 0; q < K; ++q) w[q] = *reinterpret_cast<const uint4*>(blkp + ((q * kTokensPerBlock) + row) * 16);
+      if constexpr (K == 3) {  // the triple-product plane x0 ^ x1 ^ x2
+        w[3] = make_uint4(w[0].x ^ w[1].x ^ w[2].x, w[0].y ^ w[1].y ^ w[2].y, w[0].z ^ w[1].z ^ w[2].z,
+                          w[0].w ^ w[1].w ^ w[2].w);
+      }
+      if constexpr (PROD) w[NA] = *reinterpret_cast<const uint4*>(blkp + ((K * kTokensPerBlock) + row) * 16);
+      mbar_arrive(bar(BAR_EMPTY + s));
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_PEMPTY + group.idx), group.phase ^ 1u, abort))) {
+        raise(a.err, abort);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = lane_base + group.idx * (uint32_t)(NP * kPlaneCols);
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        uint32_t o[32];
+        expand_word(w[p].x, o);
+        expand_word(w[p].y, o + 8);
+        expand_word(w[p].z, o + 16);
+        expand_word(w[p].w, o + 24);
+        tmem_st32(taddr + (uint32_t)(p * kPlaneCols), o);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(BAR_PFULL + group.idx));
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t eg = (uint32_t)(warp - kEpiWarp0) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    float4* wcst = s_cst[warp - kEpiWarp0];
+    TilePos pos;
+    pos.init(t_begin + eg, a.nb);
+    Ring stage;
+    stage.advance(eg, DS);
+    for (uint32_t i = eg; i < n_my; i += 2, stage.advance(2, DS)) {
+      if (i != eg) pos.advance(2, nb);
+      const int64_t tok = (int64_t)pos.blk * kTokensPerBlock + row;
+      // this tile's per-head constants (each warp keeps its own copy) and norms
+      const float4 my_cst = lane < HP ? __ldg(a.consts + (int64_t)pos.g * a.Hp + lane) : make_float4(0, 0, 0, 0);
+      const uint32_t s = i & kStageMask;
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_FULL + s), (i / kStages) & 1u, abort))) {
+        raise(a.err, abort);
+        break;
+      }
+      const float2 nr = *reinterpret_cast<const float2*>(smem + off_ring + s * blk_bytes + a.lay.norms_off + row * 8);
+      mbar_arrive(bar(BAR_EMPTY + s));
+      if (lane < HP) wcst[lane] = my_cst;
+      __syncwarp();
+
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_DFULL + stage.idx), stage.phase, abort))) {
+        raise(a.err, abort);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = lane_base + stage.idx * (uint32_t)(NJ * N);
+      float accA[HP], accB[HP];
+      load_term<HP>(d, accA);
+      if constexpr (PROD) load_term<HP>(d + N, accB);
+      tc_fence_before();
+      mbar_arrive(bar(BAR_DEMPTY + stage.idx));
+      if (tok < a.N) {
+        const float rk = nr.y * a.kappa;
+        float* out = a.logits + ((int64_t)pos.g * a.H) * a.N + tok;
+#pragma unroll
+        for (int h = 0; h < HP; ++h) {
+          if (h < a.H) {
+            const float4 c = wcst[h];
+            float v = nr.x * fmaf(accA[h], c.x, c.y);
+            if constexpr (PROD) v = fmaf(rk, fmaf(accB[h], c.z, c.w), v);
+            out[(int64_t)h * a.N] = v;
+          }
+        }
+      }
+      __syncwarp();  // every lane has read wcst before the next tile overwrites it
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- query operand images
+// Byte offset of element (row n, K index k) of an image of rows x 128 e4m3
+// (one 128-byte swizzle atom column), as the tensor cores read a K-major operand.
+__device__ __forceinline__ uint32_t img_offset(int n, int k) {
+  return (uint32_t)(n >> 3) * 1024u + (uint32_t)(n & 7) * 128u + (uint32_t)(((k >> 4) ^ (n & 7)) << 4) +
+         (uint32_t)(k & 15);
+}
+
+__device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t x) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw(x, __NV_E4M3)));
+}
+
+constexpr int kPrepHeads = 4;      // heads per prep CTA
+constexpr int kPrepThreads = 256;  // two threads per output coordinate (halves of the sum)
+
+// One CTA per (group, up to 4 heads).  Pi^T and S^T are staged in shared memory
+// (one round trip), Pi q and S q are formed in fp32, then every plane's image
+// rows (4 slices x head) and the heads' constants are written.
+__global__ void __launch_bounds__(kPrepThreads)
+score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int prod, ParityExpansion px,
+                     const float* __restrict__ PiT, const float* __restrict__ ST, uint32_t img_bytes,
+                     uint8_t* __restrict__ images, float4* __restrict__ consts, int* err) {
+  constexpr int d = 128;
+  extern __shared__ float prep_sm[];
+  float* sPi = prep_sm;                 // [d][d] Pi^T
+  float* sS = prep_sm + d * d;          // [d][d] S^T
+  __shared__ float s_q[kPrepHeads][d], s_part[2][2][kPrepHeads][d];
+  __shared__ float red[4 * kPrepHeads][4];
+  __shared__ float s_coef[kMaxTerms];
+  const int quads = (H + kPrepHeads - 1) / kPrepHeads;
+  const int64_t g = blockIdx.x / quads;
+  const int h0 = (blockIdx.x % quads) * kPrepHeads;
+  const int nh = min(kPrepHeads, H - h0);
+  const int t = threadIdx.x, j = t & (d - 1), half = t >> 7;
+  const int N = kSlices * Hp;
+  __shared__ __align__(8) uint64_t s_bar;
+  const uint32_t bar = smem_u32(&s_bar);
+  if (t == 0) {  // Pi^T and S^T (64 KB each) in one round trip
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = d * d * sizeof(float);
+    mbar_arrive_expect_tx(bar, prod ? 2 * bytes : bytes);
+    bulk_load(smem_u32(sPi), PiT, bytes, bar);
+    if (prod) bulk_load(smem_u32(sS), ST, bytes, bar);
+  }
+  if (t < d)
+#pragma unroll
+    for (int hh = 0; hh < kPrepHeads; ++hh) s_q[hh][t] = hh < nh ? q[(g * H + h0 + hh) * d + t] : 0.f;
+  if (t < kMaxTerms) s_coef[t] = t < px.n ? px.coef[t] : 0.f;
+  __syncthreads();
+  {
+    int no_abort = 0;
+    if (!mbar_wait(bar, 0, &no_abort) && t == 0) atomicExch(err, 1);
+  }
+  // partial sums over i in [64 half, 64 half + 64) for output coordinate j
+  float qr[kPrepHeads], sq[kPrepHeads];
+#pragma unroll
+  for (int hh = 0; hh < kPrepHeads; ++hh) qr[hh] = sq[hh] = 0.f;
+#pragma unroll 8
+  for (int i = 64 * half; i < 64 * half + 64; ++i) {
+    const float pv = sPi[i * d + j];
+    const float sv = prod ? sS[i * d + j] : 0.f;
+#pragma unroll
+    for (int hh = 0; hh < kPrepHeads; ++hh) {
+      qr[hh] = fmaf(pv, s_q[hh][i], qr[hh]);
+      sq[hh] = fmaf(sv, s_q[hh][i], sq[hh]);
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < kPrepHeads; ++hh) {
+    s_part[half][0][hh][j] = qr[hh];
+    s_part[half][1][hh][j] = sq[hh];
+  }
+  __syncthreads();
+  // full values; per head sum and max |.| (warp shuffles in the first 4 warps)
+  float v[4 * kPrepHeads];
+#pragma unroll
+  for (int hh = 0; hh < kPrepHeads; ++hh) {
+    qr[hh] = s_part[0][0][hh][j] + s_part[1][0][hh][j];
+    sq[hh] = s_part[0][1][hh][j] + s_part[1][1][hh][j];
+    v[4 * hh + 0] = qr[hh];
+    v[4 * hh + 1] = sq[hh];
+    v[4 * hh + 2] = fabsf(qr[hh]);
+    v[4 * hh + 3] = fabsf(sq[hh]);
+  }
+  __syncthreads();
+  if (half == 0) {
+#pragma unroll
+    for (int hh = 0; hh < kPrepHeads; ++hh) {
+      s_part[0][0][hh][j] = qr[hh];
+      s_part[0][1][hh][j] = sq[hh];
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+#pragma unroll
+    for (int r = 0; r < 4 * kPrepHeads; ++r) {
+      const float x = __shfl_xor_sync(0xffffffffu, v[r], o);
+      v[r] = (r & 2) ? fmaxf(v[r], x) : v[r] + x;
+    }
+  }
+  if (half == 0 && (t & 31) == 0)
+#pragma unroll
+    for (int r = 0; r < 4 * kPrepHeads; ++r) red[r][t >> 5] = v[r];
+  __syncthreads();
+  float gmax = 0.f;
+  for (int p = 0; p < nA; ++p) gmax = fmaxf(gmax, fabsf(s_coef[p]));
+  const int nP = nA + prod;
+  uint8_t* img = images + g * img_bytes;
+  // K index kk of a plane: TMEM column c = kk / 4 = 8 w + o, byte b = kk % 4,
+  // coordinate 32 w + 8 b + src(o)
+  const int kk = j, col = kk >> 2, bte = kk & 3;
+  const int jc = 32 * (col >> 3) + 8 * bte + c_src[col & 7];
+  const float comp = c_comp[col & 3];
+  for (int hh = 0; hh < nh; ++hh) {
+    const int h = h0 + hh;
+    const float sum_qr = (red[4 * hh][0] + red[4 * hh][1]) + (red[4 * hh][2] + red[4 * hh][3]);
+    const float sum_sq = (red[4 * hh + 1][0] + red[4 * hh + 1][1]) + (red[4 * hh + 1][2] + red[4 * hh + 1][3]);
+    const float max_qr = fmaxf(fmaxf(red[4 * hh + 2][0], red[4 * hh + 2][1]), fmaxf(red[4 * hh + 2][2], red[4 * hh + 2][3]));
+    const float max_sq = fmaxf(fmaxf(red[4 * hh + 3][0], red[4 * hh + 3][1]), fmaxf(red[4 * hh + 3][2], red[4 * hh + 3][3]));
+    // sigma = 2^(2 - e) with max |value| < 2^e: normalised values below 4, so
+    // with the compensation (at most 64) every slice stays below 256
+    int eA = 0, eB = 0;
+    const float mA = gmax * max_qr, mB = 2.f * max_sq;
+    if (mA > 0.f) frexpf(mA, &eA);
+    if (mB > 0.f) frexpf(mB, &eB);
+    const float sA = ldexpf(1.f, 2 - eA), sB = ldexpf(1.f, 2 - eB);
+    // the two thread halves split the planes
+    for (int p = half; p < nP; p += 2) {
+      float val = p < nA ? s_coef[p] * s_part[0][0][hh][jc] * comp * sA : 2.f * s_part[0][1][hh][jc] * comp * sB;
+      uint8_t* base = img + (uint32_t)p * (uint32_t)N * 128u;
+      float scale = 1.f;
+#pragma unroll
+      for (int sl = 0; sl < kSlices; ++sl) {
+        const __nv_fp8_storage_t x = __nv_cvt_float_to_fp8(val * scale, __NV_SATFINITE, __NV_E4M3);
+        base[img_offset(sl * Hp + h, kk)] = x;
+        val -= e4m3_value(x) / scale;
+        scale *= 16.f;
+      }
+    }
+    if (t == 0) consts[g * Hp + h] = make_float4(1.f / sA, px.c0 * sum_qr, 1.f / sB, -sum_sq);
+  }
+  if (h0 == 0) {  // zero rows of the padding heads
+    for (int p = half; p < nP; p += 2) {
+      uint8_t* base = img + (uint32_t)p * (uint32_t)N * 128u;
+      for (int hz = H; hz < Hp; ++hz)
+        for (int sl = 0; sl < kSlices; ++sl) base[img_offset(sl * Hp + hz, kk)] = 0;
+    }
+  }
+}
+
+int hp_of(int H) { return H <= 4 ? 4 : H <= 8 ? 8 : 16; }
+
+// The masks the kernels expand for k code bits (odd-symmetric codebook).
+bool standard_masks(const ParityExpansion& px, int k) {
+  static const uint32_t want[3][4] = {{1u}, {1u, 2u}, {1u, 2u, 4u, 7u}};
+  if (k < 1 || k > 3 || px.n != planes_of(k)) return false;
+  for (int i = 0; i < px.n; ++i)
+    if (px.mask[i] != want[k - 1][i]) return false;
+  return true;
+}
+
+struct TcGeom {
+  int Hp, N, nA, nP, SG, DS;
+  uint32_t slot0, img, smem;
+};
+
+bool tc_geom(const tq_plan* p, int H, TcGeom* gm) {
+  if (p->d != 128 || H < 1 || H > 16) return false;
+  const int k = p->lay.k;
+  if (!standard_masks(p->px, k)) return false;
+  gm->Hp = hp_of(H);
+  gm->N = kSlices * gm->Hp;
+  gm->nA = planes_of(k);
+  gm->nP = gm->nA + p->lay.prod;
+  const int dcols = (1 + p->lay.prod) * gm->N;  // accumulator columns of one tile
+  const int gcols = gm->nP * kPlaneCols;        // plane columns of one tile
+  // even ring sizes (see the kernel's comment); prefer four slot groups
+  const int cand[3][2] = {{4, 2}, {2, 4}, {2, 2}};
+  gm->SG = gm->DS = 0;
+  for (const auto& c : cand) {
+    if (c[0] * gcols + c[1] * dcols <= 512) {
+      gm->SG = c[0];
+      gm->DS = c[1];
+      break;
+    }
+  }
+  if (gm->SG < 2 || gm->DS < 2) return false;
+  gm->slot0 = (uint32_t)(gm->DS * dcols);
+  gm->img = ((uint32_t)gm->nP * (uint32_t)gm->N * 128u + 1023u) & ~1023u;
+  const uint32_t ring = kStages * (uint32_t)p->lay.block_bytes;
+  gm->smem = 2 * gm->img + ring + BAR_COUNT * 8 + 16 + 1024;
+  return gm->smem <= 200 * 1024;
+}
+
+template <int HP, int K, int PROD>
+cudaError_t launch_kernel(const ScoreTcArgs& a, const TcGeom& gm, int64_t grid, cudaStream_t s) {
+  auto kern = score_tc_kernel<HP, K, PROD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gm.smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)grid, kThreads, gm.smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int HP>
+cudaError_t launch_hp(const ScoreTcArgs& a, const TcGeom& gm, int64_t grid, int k, int prod, cudaStream_t s) {
+  switch (k * 2 + prod) {
+    case 2: return launch_kernel<HP, 1, 0>(a, gm, grid, s);
+    case 3: return launch_kernel<HP, 1, 1>(a, gm, grid, s);
+    case 4: return launch_kernel<HP, 2, 0>(a, gm, grid, s);
+    case 5: return launch_kernel<HP, 2, 1>(a, gm, grid, s);
+    case 6: return launch_kernel<HP, 3, 0>(a, gm, grid, s);
+    case 7: return launch_kernel<HP, 3, 1>(a, gm, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool score_tc_supported(const tq_plan* p, int H) {
+  TcGeom gm;
+  return tc_geom(p, H, &gm);
+}
+
+size_t score_tc_workspace_bytes(const tq_plan* p, int64_t G, int H) {
+  TcGeom gm;
+  if (!tc_geom(p, H, &gm)) return 0;
+  const size_t imgs = (size_t)G * gm.img;
+  return ((imgs + 255) & ~(size_t)255) + (size_t)G * gm.Hp * sizeof(float4);
+}
+
+cudaError_t launch_score_tc(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed,
+                            int64_t N, float* logits, void* ws, cudaStream_t s) {
+  TcGeom gm;
+  if (!tc_geom(p, H, &gm)) return cudaErrorInvalidValue;
+  if (G * N == 0) return cudaSuccess;
+  uint8_t* images = static_cast<uint8_t*>(ws);
+  float4* consts = reinterpret_cast<float4*>(images + (((size_t)G * gm.img + 255) & ~(size_t)255));
+  const size_t prep_smem = 2 * 128 * 128 * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(score_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)prep_smem);
+  if (e != cudaSuccess) return e;
+  const int64_t prep_blocks = G * ((H + kPrepHeads - 1) / kPrepHeads);
+  score_tc_prep_kernel<<<(unsigned)prep_blocks, kPrepThreads, prep_smem, s>>>(
+      queries, H, gm.Hp, gm.nA, p->lay.prod, p->px, p->PiT, p->lay.prod ? p->ST : p->PiT, gm.img, images, consts,
+      p->err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  ScoreTcArgs a;
+  a.lay = p->lay;
+  a.H = H;
+  a.Hp = gm.Hp;
+  a.SG = gm.SG;
+  a.DS = gm.DS;
+  a.slot0 = gm.slot0;
+  a.img_bytes = gm.img;
+  a.N = N;
+  a.nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
+  a.n_tiles = G * a.nb;
+  a.packed = packed;
+  a.images = images;
+  a.consts = consts;
+  a.kappa = p->kappa;
+  a.logits = logits;
+  a.err = p->err;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t grid = a.n_tiles < sms ? a.n_tiles : sms;
+  const int k = p->lay.k, prod = p->lay.prod;
+  if (gm.Hp == 4) return launch_hp<4>(a, gm, grid, k, prod, s);
+  if (gm.Hp == 8) return launch_hp<8>(a, gm, grid, k, prod, s);
+  return launch_hp<16>(a, gm, grid, k, prod, s);
+}
+
+}  // namespace tq

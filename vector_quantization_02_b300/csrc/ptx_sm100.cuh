@@ -54,6 +54,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
   return false;
 }
 
+// As mbar_wait, but each poll lets the hardware suspend the thread for up to
+// kSuspendNs nanoseconds while the phase is incomplete, so a waiting warp
+// issues few instructions and notices the completion within about that time.
+// At most kSuspendPolls polls (about a second).
+constexpr uint32_t kSuspendNs = 128;
+constexpr uint32_t kSuspendPolls = 1u << 23;
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, const volatile int* abort) {
+  for (uint32_t it = 0; it < kSuspendPolls; ++it) {
+    if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
+    if ((it & 63) == 63 && *abort) return false;
+  }
+  return false;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
                                             uint32_t bar) {

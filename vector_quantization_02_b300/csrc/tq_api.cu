@@ -80,6 +80,36 @@ cudaError_t build_tc_ops(tq_plan* p) {
 
 }  // namespace
 
+namespace tq {
+
+// Workspace: [tensor-core query images and constants | Pi q, S q] [top-k candidates]
+size_t score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k) {
+  const size_t prep = score_tc_supported(p, H)
+                          ? score_tc_workspace_bytes(p, G, H)
+                          : (size_t)G * H * qs_vectors(p) * p->d * sizeof(float);
+  return align256(prep) + topk_workspace_bytes(G * H, N, top_k) + 256;
+}
+
+cudaError_t score_run(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed, int64_t N,
+                      float* logits, int top_k, float* top_scores, int64_t* top_idx, void* ws, cudaStream_t s) {
+  cudaError_t e;
+  size_t prep;
+  if (score_tc_supported(p, H)) {
+    prep = score_tc_workspace_bytes(p, G, H);
+    e = launch_score_tc(p, queries, G, H, packed, N, logits, ws, s);
+  } else {
+    prep = (size_t)G * H * qs_vectors(p) * p->d * sizeof(float);
+    float* qs = static_cast<float*>(ws);
+    e = launch_query_prep(p, queries, G, H, qs, s);
+    if (e == cudaSuccess) e = launch_score_simt(p, qs, G, H, packed, N, logits, s);
+  }
+  if (e == cudaSuccess && top_k > 0)
+    e = launch_topk(logits, G * H, N, top_k, top_scores, top_idx, static_cast<char*>(ws) + align256(prep), s);
+  return e;
+}
+
+}  // namespace tq
+
 extern "C" {
 
 const char* tq_status_string(tq_status s) {
@@ -159,6 +189,21 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
       return TQ_EINVAL;
     }
   }
+  {
+    unsigned masks[kMaxTerms];
+    double coefs[kMaxTerms], c0 = 0.0;
+    int n = 0;
+    if (tq_codebook_parity_expansion(levels, hc, &n, masks, coefs, &c0) != TQ_OK) {
+      free_plan(p);
+      return TQ_EINVAL;
+    }
+    p->px.n = n;
+    for (int i = 0; i < kMaxTerms; ++i) {
+      p->px.mask[i] = i < n ? masks[i] : 0u;
+      p->px.coef[i] = i < n ? (float)coefs[i] : 0.f;
+    }
+    p->px.c0 = (float)c0;
+  }
   if (L.prod && d == 128) {
     if (build_tc_ops(p) != cudaSuccess) {
       free_plan(p);
@@ -196,8 +241,7 @@ tq_status tq_encode(const tq_plan* p, const void* keys, tq_dtype dtype, int64_t 
 
 size_t tq_score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k) {
   if (!p || G < 0 || H < 1 || N < 0 || top_k < 0) return 0;
-  size_t qs = align256((size_t)G * H * qs_vectors(p) * p->d * sizeof(float));
-  return qs + topk_workspace_bytes(G * H, N, top_k) + 256;
+  return score_workspace_bytes(p, G, H, N, top_k);
 }
 
 tq_status tq_score(const tq_plan* p, const float* queries, int64_t G, int H, const void* packed, int64_t N,
@@ -212,13 +256,8 @@ tq_status tq_score(const tq_plan* p, const float* queries, int64_t G, int H, con
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_EALIGN;
   if (top_k > 0 && (!aligned16(top_scores) || !aligned16(top_idx))) return TQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* qs = static_cast<float*>(workspace);
-  const size_t qs_bytes = align256((size_t)G * H * qs_vectors(p) * p->d * sizeof(float));
-  cudaError_t e = launch_query_prep(p, queries, G, H, qs, s);
-  if (e == cudaSuccess) e = launch_score_simt(p, qs, G, H, static_cast<const uint8_t*>(packed), N, logits, s);
-  if (e == cudaSuccess && top_k > 0)
-    e = launch_topk(logits, G * H, N, top_k, top_scores, top_idx, static_cast<char*>(workspace) + qs_bytes, s);
-  return from_cuda(e);
+  return from_cuda(score_run(p, queries, G, H, static_cast<const uint8_t*>(packed), N, logits, top_k, top_scores,
+                             top_idx, workspace, s));
 }
 
 tq_status tq_decode(const tq_plan* p, const void* packed, int64_t G, int64_t N, float* out, void* stream) {

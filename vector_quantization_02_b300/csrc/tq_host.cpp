@@ -72,6 +72,36 @@ extern "C" tq_status tq_lloyd_max_codebook(int levels, int d, float* out) {
   return TQ_OK;
 }
 
+// Parity (Walsh) expansion of a codebook indexed by k = log2(levels) bits:
+// with chi_T(idx) = (-1)^popcount(idx & T), the Walsh coefficients are
+// w_T = 2^-k sum_idx c[idx] chi_T(idx), and since chi_T = 1 - 2 parity(idx & T),
+//   c[idx] = c[0] + sum_{T != 0} (-2 w_T) parity(idx & T).
+// Sums of at most 16 fp32 values scaled by a power of two are exact in fp64,
+// so a codebook that is exactly odd-symmetric (c[L-1-i] = -c[i]) gets exactly
+// zero weight on every even-weight mask and those terms are dropped.
+extern "C" tq_status tq_codebook_parity_expansion(int levels, const float* codebook, int* n_terms,
+                                                  unsigned* masks, double* coefs, double* c0) {
+  if (!codebook || !n_terms || !masks || !coefs || !c0) return TQ_EINVAL;
+  if (!(levels == 2 || levels == 4 || levels == 8 || levels == 16)) return TQ_EINVAL;
+  int n = 0;
+  for (int T = 1; T < levels; ++T) {
+    double w = 0.0;
+    for (int idx = 0; idx < levels; ++idx) {
+      const double c = (double)codebook[idx];
+      w += (__builtin_popcount((unsigned)(idx & T)) & 1) ? -c : c;
+    }
+    w /= (double)levels;
+    if (w != 0.0) {
+      masks[n] = (unsigned)T;
+      coefs[n] = -2.0 * w;
+      ++n;
+    }
+  }
+  *n_terms = n;
+  *c0 = (double)codebook[0];
+  return TQ_OK;
+}
+
 extern "C" tq_status tq_haar_rotation(int d, const double* gaussian, float* Pi_out) {
   if (!gaussian || !Pi_out || d < 1 || d > 8192) return TQ_EINVAL;
   const size_t n = (size_t)d;

@@ -22,6 +22,18 @@ struct CodeParams {
   int L;                    // number of centroids
 };
 
+// Parity (Walsh) expansion of a codebook over its k index bits:
+//   c[idx] = c0 + sum_t coef[t] * parity(idx & mask[t]),
+// with only the terms whose coefficient is not zero.  Scoring contracts the
+// XOR planes of the code bits against coef[t] Pi q.
+constexpr int kMaxTerms = kMaxLevels - 1;
+struct ParityExpansion {
+  int n;
+  uint32_t mask[kMaxTerms];
+  float coef[kMaxTerms];
+  float c0;
+};
+
 // Geometry of the packed layout for one plan.
 struct Layout {
   int d;            // head dimension
@@ -44,6 +56,7 @@ struct tq_plan {
   int device;
   tq::Layout lay;
   tq::CodeParams cp;
+  tq::ParityExpansion px;  // codebook in parity form (tensor-core score)
   float kappa;        // sqrt(pi/2) / m
   float* Pi;          // [d][d] row-major, y = Pi u
   float* PiT;         // [d][d] = Pi^T (coalesced column access in SIMT kernels)
@@ -77,6 +90,17 @@ cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, 
                               float* logits, cudaStream_t s);
 
 size_t topk_workspace_bytes(int64_t rows, int64_t N, int k);
+
+bool score_tc_supported(const tq_plan* p, int H);
+size_t score_tc_workspace_bytes(const tq_plan* p, int64_t G, int H);
+cudaError_t launch_score_tc(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed,
+                            int64_t N, float* logits, void* ws, cudaStream_t s);
+
+// Scoring as tq_score performs it (query preparation, score kernel, optional
+// top-k) on a caller-provided workspace of at least score_workspace_bytes().
+size_t score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k);
+cudaError_t score_run(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed, int64_t N,
+                      float* logits, int top_k, float* top_scores, int64_t* top_idx, void* ws, cudaStream_t s);
 
 __device__ __forceinline__ float load_key(const void* keys, int dt, int64_t i) {
   if (dt == TQ_F32) return reinterpret_cast<const float*>(keys)[i];

@@ -69,14 +69,9 @@ extern "C" tq_status tq_score_noalloc(const tq_plan* p, const float* queries, in
   if (need == 0 || need > (size_t)TQ_SCORE_NOALLOC_MAX_BYTES) return TQ_EUNSUPPORTED;
   void* ws = nullptr;
   if (scratch_address(&ws) != cudaSuccess) return TQ_ECUDA;
-  // same kernels and scratch layout as tq_score: [Pi q, S q][top-k candidates]
+  // the same kernels and scratch layout as tq_score
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* qs = static_cast<float*>(ws);
-  const int nv = p->lay.prod ? 2 : 1;
-  const size_t qs_bytes = ((size_t)G * H * nv * p->d * sizeof(float) + 255) & ~(size_t)255;
-  cudaError_t e = tq::launch_query_prep(p, queries, G, H, qs, s);
-  if (e == cudaSuccess) e = tq::launch_score_simt(p, qs, G, H, static_cast<const uint8_t*>(packed), N, logits, s);
-  if (e == cudaSuccess && top_k > 0)
-    e = tq::launch_topk(logits, G * H, N, top_k, top_scores, top_idx, static_cast<char*>(ws) + qs_bytes, s);
+  cudaError_t e = tq::score_run(p, queries, G, H, static_cast<const uint8_t*>(packed), N, logits, top_k, top_scores,
+                                top_idx, ws, s);
   return e == cudaSuccess ? TQ_OK : TQ_ECUDA;
 }
