@@ -16,9 +16,10 @@
 // Work per CTA (persistent, one CTA per SM, 128 keys = one packed block per tile):
 //  warp 0      TMA producer: key tiles (K-major, 128-byte swizzle) into a
 //              2-stage ring; once, the swizzled images of Pi_hi/lo and M_hi/lo.
-//  warp 1      TMEM owner (512 columns) and MMA issuer (one thread).  Issue
-//              order E2(i+1), E5(i) keeps the tensor pipe busy while the
-//              epilogue quantises.
+//  warp 1      TMEM owner (512 columns) and E2 issuer (one thread);
+//  warp 10     E5 issuer (one thread).  Two issuers, because a single thread
+//              issues one tcgen05.mma only every ~50-80 cycles and E5 of tile i
+//              must not wait behind E2 of tile i + 1.
 //  warps 2-9   two epilogue warpgroups; tile i goes to warpgroup i % 2, which
 //              owns TMEM columns [256 b, 256 b + 256): Y/R in the first 128
 //              (the bf16 residual split is written back over the Y columns it
@@ -36,7 +37,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kE5Warp = 10;
 constexpr int kStages = 2;
 constexpr uint32_t kOpBytes = 128 * 128 * 2;  // one 128 x 128 16-bit operand image
 constexpr uint32_t kAtomBytes = 128 * 128;    // 128 rows x 64 elements (128 B) per swizzle atom
@@ -48,11 +50,12 @@ enum {
   BAR_XFULL = 1,
   BAR_XEMPTY = BAR_XFULL + kStages,
   BAR_YFULL = BAR_XEMPTY + kStages,
-  BAR_RFULL = BAR_YFULL + 2,
-  BAR_PFULL = BAR_RFULL + 2,
+  BAR_RFULL = BAR_YFULL + 2,       // [stage][half]: residual of coordinates 64 h .. 64 h + 63 written
+  BAR_PFULL = BAR_RFULL + 4,
   BAR_ACCEMPTY = BAR_PFULL + 2,
   BAR_DONE = BAR_ACCEMPTY + 2,
-  BAR_COUNT = BAR_DONE + 1
+  BAR_DONE5 = BAR_DONE + 1,
+  BAR_COUNT = BAR_DONE5 + 1
 };
 constexpr uint32_t kSmemBytes = kOffBar + BAR_COUNT * 8 + 16 + 1024;  // + slot, + alignment slack
 
@@ -103,11 +106,13 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(BAR_YFULL + b), 1);
-      mbar_init(bar(BAR_RFULL + b), 128);
+      mbar_init(bar(BAR_RFULL + 2 * b), 128);
+      mbar_init(bar(BAR_RFULL + 2 * b + 1), 128);
       mbar_init(bar(BAR_PFULL + b), 1);
       mbar_init(bar(BAR_ACCEMPTY + b), 128);
     }
     mbar_init(bar(BAR_DONE), 1);
+    mbar_init(bar(BAR_DONE5), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -153,58 +158,66 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
         mbar_wait(bar(BAR_XFULL + (int)(i % kStages)), (uint32_t)(i / kStages) & 1, &dummy);
       mbar_wait(bar(BAR_OPS), 0, &dummy);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kE5Warp) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       constexpr uint32_t idesc_x = idesc_f16(kBF16 ? 1u : 0u, 128, 128);
       constexpr uint32_t idesc_r = idesc_f16(1u, 128, 128);
+      const bool e2 = warp == 1;
       bool ok = mbar_wait(bar(BAR_OPS), 0, abort);
-      auto issue_e2 = [&](int64_t i) -> bool {
-        const int s = (int)(i % kStages), b = (int)(i & 1);
-        const uint32_t j = (uint32_t)(i >> 1);
-        if (!mbar_wait(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort)) return false;
-        if (!mbar_wait(bar(BAR_ACCEMPTY + b), (j & 1) ^ 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + 256u * b;
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const uint32_t off = (kb >> 2) * kAtomBytes + (kb & 3) * 32;
-          const uint64_t ad = sdesc_k_sw128(sb + kOffX + s * kOpBytes + off);
-          mma_f16_ss(d, ad, sdesc_k_sw128(sb + kOffPiHi + off), idesc_x, kb > 0);
-          mma_f16_ss(d, ad, sdesc_k_sw128(sb + kOffPiLo + off), idesc_x, 1);
-        }
-        mma_commit(bar(BAR_YFULL + b));
-        mma_commit(bar(BAR_XEMPTY + s));
-        return true;
-      };
-      auto issue_e5 = [&](int64_t i) -> bool {
+      for (int64_t i = 0; ok && i < n_my; ++i) {
         const int b = (int)(i & 1);
         const uint32_t j = (uint32_t)(i >> 1);
-        if (!mbar_wait(bar(BAR_RFULL + b), j & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t r = tmem + 256u * b, d = r + 128;
+        if (e2) {
+          // E2: Y = X Pi^T, Pi split hi + lo
+          const int s = (int)(i % kStages);
+          if (!mbar_wait(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort) ||
+              !mbar_wait(bar(BAR_ACCEMPTY + b), (j & 1) ^ 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + 256u * b;
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const uint32_t off = (kb >> 2) * kAtomBytes + (kb & 3) * 32;
-          const uint32_t a_hi = r + 32 * (kb >> 1) + 8 * (kb & 1), a_lo = a_hi + 16;
-          const uint64_t mh = sdesc_k_sw128(sb + kOffMHi + off), ml = sdesc_k_sw128(sb + kOffMLo + off);
-          mma_f16_ts(d, a_hi, mh, idesc_r, kb > 0);
-          mma_f16_ts(d, a_hi, ml, idesc_r, 1);
-          mma_f16_ts(d, a_lo, mh, idesc_r, 1);
+          for (int kb = 0; kb < 8; ++kb) {
+            const uint32_t off = (kb >> 2) * kAtomBytes + (kb & 3) * 32;
+            const uint64_t ad = sdesc_k_sw128(sb + kOffX + s * kOpBytes + off);
+            mma_f16_ss(d, ad, sdesc_k_sw128(sb + kOffPiHi + off), idesc_x, kb > 0);
+            mma_f16_ss(d, ad, sdesc_k_sw128(sb + kOffPiLo + off), idesc_x, 1);
+          }
+          mma_commit(bar(BAR_YFULL + b));
+          mma_commit(bar(BAR_XEMPTY + s));
+        } else {
+          // E5: P = R' M^T with R' = R_hi + R_lo and M = M_hi + M_lo (bf16), R_lo M_lo dropped;
+          // the first 64 coordinates' MMAs start while the epilogue still
+          // quantises the last 64
+          const uint32_t r = tmem + 256u * b, d = r + 128;
+#pragma unroll
+          for (int kb = 0; kb < 8; ++kb) {
+            if ((kb & 3) == 0) {
+              if (!mbar_wait(bar(BAR_RFULL + 2 * b + (kb >> 2)), j & 1, abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t off = (kb >> 2) * kAtomBytes + (kb & 3) * 32;
+            const uint32_t a_hi = r + 32 * (kb >> 1) + 8 * (kb & 1), a_lo = a_hi + 16;
+            const uint64_t mh = sdesc_k_sw128(sb + kOffMHi + off), ml = sdesc_k_sw128(sb + kOffMLo + off);
+            mma_f16_ts(d, a_hi, mh, idesc_r, kb > 0);
+            mma_f16_ts(d, a_hi, ml, idesc_r, 1);
+            mma_f16_ts(d, a_lo, mh, idesc_r, 1);
+          }
+          if (!ok) break;
+          mma_commit(bar(BAR_PFULL + b));
         }
-        mma_commit(bar(BAR_PFULL + b));
-        return true;
-      };
-      if (ok && n_my > 0) ok = issue_e2(0);
-      for (int64_t i = 0; ok && i < n_my; ++i) {
-        if (i + 1 < n_my) ok = issue_e2(i + 1);
-        if (ok) ok = issue_e5(i);
       }
       if (!ok) raise(a.err, abort);
       // all issued MMAs complete before TMEM is freed
-      mma_commit(bar(BAR_DONE));
+      const int done = e2 ? BAR_DONE : BAR_DONE5;
+      mma_commit(bar(done));
       int dummy = 0;
-      mbar_wait(bar(BAR_DONE), 0, &dummy);
+      mbar_wait(bar(done), 0, &dummy);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -274,11 +287,9 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
 #pragma unroll
       for (int p = 0; p < K; ++p) pl[p][0] = pl[p][1] = pl[p][2] = pl[p][3] = 0;
       float rr = 0.f;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(t_lane + 32 * cc, v);
-        tmem_ld_wait();
+      // one 32-coordinate chunk: codes into pl (shifted in), residual split
+      // written back over the chunk's own Y columns
+      auto chunk = [&](const uint32_t (&v)[32], int cc) {
         uint32_t w[K];
 #pragma unroll
         for (int p = 0; p < K; ++p) w[p] = 0;
@@ -292,12 +303,12 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
           for (int u = 1; u >= 0; --u) {
             const float y = __uint_as_float(v[e + u]);
             // sb[q] = n t_q - y: its sign bit is [y > n t_q] (a tie gives +0)
-            uint32_t sb[L - 1];
+            uint32_t sbit[L - 1];
             float cv = nc[0];
 #pragma unroll
             for (int q = 0; q < L - 1; ++q) {
-              sb[q] = __float_as_uint(nt[q] - y);
-              cv = (int)sb[q] < 0 ? nc[q + 1] : cv;
+              sbit[q] = __float_as_uint(nt[q] - y);
+              cv = (int)sbit[q] < 0 ? nc[q + 1] : cv;
             }
             // bit p of idx = #{q : y > n t_q} is the XOR of the sign bits of
             // the thresholds q with (q + 1) % 2^p == 0 (the count is monotone)
@@ -306,12 +317,12 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
               uint32_t x = 0;
 #pragma unroll
               for (int q = 0; q < L - 1; ++q)
-                if (((q + 1) & ((1 << p) - 1)) == 0) x ^= sb[q];
+                if (((q + 1) & ((1 << p) - 1)) == 0) x ^= sbit[q];
               w[p] = __funnelshift_l(x, w[p], 1);
             }
-            const float r = y - cv;
-            rr = fmaf(r, r, rr);
-            r2[u] = r;
+            const float rv = y - cv;
+            rr = fmaf(rv, rv, rr);
+            r2[u] = rv;
           }
           const __nv_bfloat162 h = __floats2bfloat162_rn(r2[0], r2[1]);
           const float2 hf = __bfloat1622float2(h);
@@ -328,10 +339,24 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
           pl[p][2] = pl[p][3];
           pl[p][3] = w[p];
         }
+      };
+      // the next chunk's TMEM load is in flight while a chunk is processed
+      uint32_t va[32], vb[32];
+      tmem_ld32(t_lane, va);
+      tmem_ld_wait();
+#pragma unroll 1
+      for (int cc = 0; cc < 4; cc += 2) {
+        tmem_ld32(t_lane + 32 * (cc + 1), vb);
+        chunk(va, cc);
+        tmem_ld_wait();
+        if (cc + 2 < 4) tmem_ld32(t_lane + 32 * (cc + 2), va);
+        chunk(vb, cc + 1);
+        // this half of the residual is in TMEM: E5 may start on it
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_RFULL + 2 * wg + (cc >> 1)));
+        if (cc + 2 < 4) tmem_ld_wait();
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(BAR_RFULL + wg));
       const float rho = sqrtf(rr);
 
       // E5 result -> sign plane
@@ -340,20 +365,22 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
         break;
       }
       tc_fence_after();
-      uint32_t zs[4] = {0, 0, 0, 0};
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(t_lane + 128 + 32 * cc, v);
+      uint32_t zs[4];
+      {
+        uint32_t v[4][32];
+        tmem_ld32(t_lane + 128, v[0]);
+        tmem_ld32(t_lane + 160, v[1]);
+        tmem_ld32(t_lane + 192, v[2]);
+        tmem_ld32(t_lane + 224, v[3]);
         tmem_ld_wait();
         // shift in the sign bits (coordinate e at bit e), then invert: z = [p >= 0]
-        uint32_t z = 0;
 #pragma unroll
-        for (int e = 31; e >= 0; --e) z = __funnelshift_l(v[e], z, 1);
-        zs[0] = zs[1];
-        zs[1] = zs[2];
-        zs[2] = zs[3];
-        zs[3] = n > 0.f ? ~z : 0xFFFFFFFFu;
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t z = 0;
+#pragma unroll
+          for (int e = 31; e >= 0; --e) z = __funnelshift_l(v[cc][e], z, 1);
+          zs[cc] = n > 0.f ? ~z : 0xFFFFFFFFu;
+        }
       }
       tc_fence_before();
       mbar_arrive(bar(BAR_ACCEMPTY + wg));
