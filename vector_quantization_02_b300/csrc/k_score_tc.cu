@@ -26,28 +26,30 @@
 //
 // Work per CTA (persistent, contiguous range of 128-token blocks), four roles
 // that only meet at mbarriers, so expansion never waits for an epilogue:
-//  warps 0-3    MMA issuers, tile i to warp i % 4 (one elected lane each: a
-//               single thread issues one tcgen05.mma about every 50 cycles, and
-//               every mbarrier operation costs it ~150 cycles, so a tile is one
-//               job: two waits, all its MMAs - the MMA-term planes into one
-//               accumulator, the sign plane into another - and two commits).
-//               The issuers take their barrier waits strictly in tile order (a
-//               turn counter in shared memory): a parity wait cannot tell phase
-//               k from phase k + 2, so a ring entry's uses must be waited for by
-//               one sequence of waits.  Their MMA issue still overlaps.
+//  warps 0-3    MMA issuers (one elected lane each: a single thread issues one
+//               tcgen05.mma about every 50 cycles, and every mbarrier operation
+//               costs it ~150 cycles).  A tile has one job per term - the
+//               MMA-term planes into one accumulator, the sign plane into
+//               another; tile i's jobs go to warps 2 (i % 2) and 2 (i % 2) + 1.
 //               Warp 0 owns the TMEM allocation (512 columns).
 //  warps 4-11   two expansion warpgroups; tile i goes to warpgroup i % 2.
 //               Thread (warp w, lane l) owns key row 32 (w % 4) + l: it reads its
 //               16-byte plane chunks from the staged block and writes all the
 //               tile's expanded planes into one group of 32-column TMEM slots
-//               (a ring of SG groups, SG even so that every group is always
-//               filled by the same warpgroup), then arrives once.
+//               (a ring of SG groups), then arrives once.
 //  warps 12-19  two epilogue warpgroups; tile i goes to warpgroup i % 2.  They
-//               read the accumulators of a tile (a ring of DS stages, DS even), combine
+//               read the accumulators of a tile (a ring of DS stages), combine
 //               slices and terms with the key's norms, and store H logits (one
 //               coalesced store per head).
 //  warp 20      producer: bulk copies of packed blocks (8-stage ring) and of the
 //               per-group query operand images (double-buffered).
+// Ordering.  A parity wait cannot tell phase k of an mbarrier from phase k + 2,
+// so every ring entry has exactly one consumer, which waits for its uses in
+// sequence: with the ring sizes even, tile i's packed block, plane-slot group
+// and accumulator stage are only ever waited for by the expansion warpgroup,
+// the issuer pair and the epilogue warpgroup of parity i % 2.  (Barrier waits
+// cost ~150 cycles even when the phase is complete, so serialising the waits
+// of different consumers through counters would cap the tile rate.)
 // Every wait is bounded: on expiry the kernel raises the plan's error word,
 // drains what it issued and frees its TMEM.
 #include <cuda_fp8.h>
@@ -190,6 +192,31 @@ struct TilePos {
   }
 };
 
+__device__ __forceinline__ float slice_weight(int sl) {
+  return sl == 0 ? 1.f : sl == 1 ? 0.0625f : sl == 2 ? 0.00390625f : 0.000244140625f;
+}
+
+// Both terms' accumulators of a tile (NJ x N <= 64 columns): every TMEM load is
+// issued before a single wait.
+template <int HP, int NJ>
+__device__ __forceinline__ void load_terms(uint32_t taddr, float (&accA)[HP], float (&accB)[HP]) {
+  constexpr int N = kSlices * HP;
+  uint32_t v[NJ * N / 16][16];
+#pragma unroll
+  for (int c = 0; c < NJ * N / 16; ++c) tmem_ld16(taddr + 16 * c, v[c]);
+  tmem_ld_wait();
+#pragma unroll
+  for (int h = 0; h < HP; ++h) accA[h] = accB[h] = 0.f;
+#pragma unroll
+  for (int c = 0; c < NJ * N / 16; ++c)
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int col = 16 * c + e, term = col / N, sl = (col % N) / HP, h = col % HP;
+      if (term == 0) accA[h] = fmaf(__uint_as_float(v[c][e]), slice_weight(sl), accA[h]);
+      else accB[h] = fmaf(__uint_as_float(v[c][e]), slice_weight(sl), accB[h]);
+    }
+}
+
 // Tokens' accumulators of one term: sum over slices of D[slice * HP + h] / 16^slice.
 template <int HP>
 __device__ __forceinline__ void load_term(uint32_t taddr, float (&acc)[HP]) {
@@ -225,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
   const uint32_t off_bar = (off_ring + kStages * blk_bytes + 7) & ~7u;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ uint32_t s_turn;              // tile whose issuer may take its waits
   __shared__ float4 s_cst[kEpiWarps][HP];  // constants of each epilogue warp's current tile
   auto bar = [&](int i) { return sb + off_bar + 8u * (uint32_t)i; };
 
@@ -233,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
   const uint32_t SG = (uint32_t)a.SG, DS = (uint32_t)a.DS, nb = (uint32_t)a.nb;
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    s_turn = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
       mbar_init(bar(BAR_EMPTY + s), 256);  // one expansion and one epilogue warpgroup
@@ -244,10 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
     }
     for (int s = 0; s < kMaxGroups; ++s) {
       mbar_init(bar(BAR_PFULL + s), 128);
-      mbar_init(bar(BAR_PEMPTY + s), 1);
+      mbar_init(bar(BAR_PEMPTY + s), NJ);
     }
     for (int d = 0; d < kMaxDStages; ++d) {
-      mbar_init(bar(BAR_DFULL + d), 1);
+      mbar_init(bar(BAR_DFULL + d), NJ);
       mbar_init(bar(BAR_DEMPTY + d), 128);
     }
     for (int w = 0; w < kIssuers; ++w) mbar_init(bar(BAR_DONE + w), 1);
@@ -329,49 +354,40 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
             need_b = true;
           }
         }
-        if ((i & (kIssuers - 1)) != (uint32_t)warp) continue;
-        // wait for this tile's turn (the previous tile's issuer has passed its waits)
-        {
-          const volatile uint32_t* turn = &s_turn;
-          uint32_t it = 0;
-          while (*turn != i && it < kWaitLimit) {
-            if ((++it & 63) == 0 && *abort) it = kWaitLimit;
+        for (int job = 0; job < NJ; ++job) {
+          // tile i's term jobs: warps 2 (i % 2) + job (the only waiters on its ring entries)
+          if ((uint32_t)(2 * (i & 1) + job) != (uint32_t)warp) continue;
+          if (need_b) {
+            if (!mbar_wait_suspend(bar(BAR_BFULL + (epoch & 1u)), (epoch >> 1) & 1u, abort)) {
+              ok = false;
+              break;
+            }
+            need_b = false;
           }
-          if (*turn != i) {
+          if (!mbar_wait_suspend(bar(BAR_PFULL + group.idx), group.phase, abort) ||
+              !mbar_wait_suspend(bar(BAR_DEMPTY + stage.idx), stage.phase ^ 1u, abort)) {
             ok = false;
             break;
           }
-        }
-        if (need_b) {
-          if (!mbar_wait_suspend(bar(BAR_BFULL + (epoch & 1u)), (epoch >> 1) & 1u, abort)) {
-            ok = false;
-            break;
+          tc_fence_after();
+          const uint32_t img = sb + (epoch & 1u) * a.img_bytes;
+          const uint32_t d = tmem + stage.idx * (uint32_t)(NJ * N) + (uint32_t)(job * N);
+          const uint32_t at = tmem + a.slot0 + group.idx * (uint32_t)(NP * kPlaneCols);
+          const int p0 = job == 0 ? 0 : NA, p1 = job == 0 ? NA : NP;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            if (p < p0 || p >= p1) continue;
+            // plane p of the image: N rows x 128 B (one swizzle atom column);
+            // K step kb starts 32 bytes further (2 in descriptor units)
+            const uint64_t b0 = sdesc_k_sw128(img + (uint32_t)p * (uint32_t)N * 128u);
+#pragma unroll
+            for (uint32_t kb = 0; kb < 4; ++kb)
+              mma_f8_ts(d, at + (uint32_t)(p * kPlaneCols) + 8u * kb, b0 + 2u * kb, idesc,
+                        (p > p0 || kb > 0) ? 1u : 0u);
           }
-          need_b = false;
+          mma_commit(bar(BAR_PEMPTY + group.idx));
+          mma_commit(bar(BAR_DFULL + stage.idx));
         }
-        if (!mbar_wait_suspend(bar(BAR_PFULL + group.idx), group.phase, abort) ||
-            !mbar_wait_suspend(bar(BAR_DEMPTY + stage.idx), stage.phase ^ 1u, abort)) {
-          ok = false;
-          break;
-        }
-        *static_cast<volatile uint32_t*>(&s_turn) = i + 1;
-        tc_fence_after();
-        const uint32_t img = sb + (epoch & 1u) * a.img_bytes;
-        const uint32_t d = tmem + stage.idx * (uint32_t)(NJ * N);
-        const uint32_t at = tmem + a.slot0 + group.idx * (uint32_t)(NP * kPlaneCols);
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-          // plane p of the image: N rows x 128 B (one swizzle atom column);
-          // K step kb starts 32 bytes further (2 in descriptor units)
-          const uint64_t b0 = sdesc_k_sw128(img + (uint32_t)p * (uint32_t)N * 128u);
-          const uint32_t dp = p < NA ? d : d + N;
-#pragma unroll
-          for (uint32_t kb = 0; kb < 4; ++kb)
-            mma_f8_ts(dp, at + (uint32_t)(p * kPlaneCols) + 8u * kb, b0 + 2u * kb, idesc,
-                      ((p > 0 && p < NA) || kb > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(BAR_PEMPTY + group.idx));
-        mma_commit(bar(BAR_DFULL + stage.idx));
       }
       if (!ok) raise(a.err, abort);
       mma_commit(bar(BAR_DONE + warp));
@@ -454,8 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
       tc_fence_after();
       const uint32_t d = lane_base + stage.idx * (uint32_t)(NJ * N);
       float accA[HP], accB[HP];
-      load_term<HP>(d, accA);
-      if constexpr (PROD) load_term<HP>(d + N, accB);
+      if constexpr (NJ * N <= 64) {
+        load_terms<HP, NJ>(d, accA, accB);
+      } else {
+        load_term<HP>(d, accA);
+        if constexpr (PROD) load_term<HP>(d + N, accB);
+      }
       tc_fence_before();
       mbar_arrive(bar(BAR_DEMPTY + stage.idx));
       if (tok < a.N) {
@@ -658,7 +678,7 @@ bool tc_geom(const tq_plan* p, int H, TcGeom* gm) {
   gm->nP = gm->nA + p->lay.prod;
   const int dcols = (1 + p->lay.prod) * gm->N;  // accumulator columns of one tile
   const int gcols = gm->nP * kPlaneCols;        // plane columns of one tile
-  // even ring sizes (see the kernel's comment); prefer four slot groups
+  // even ring sizes (see the kernel's comment), the deepest that fit
   const int cand[3][2] = {{4, 2}, {2, 4}, {2, 2}};
   gm->SG = gm->DS = 0;
   for (const auto& c : cand) {
