@@ -45,34 +45,30 @@ def oracle_encode(inp: Inputs, keys: torch.Tensor):
     return o.encode_pack(keys.detach().cpu().double().numpy(), inp.Pi_o, inp.S_o, inp.c_o, inp.bits, inp.mode, G, N)
 
 
-def compare_encode(inp: Inputs, gpu_bytes: np.ndarray, keys: torch.Tensor, check_bytes=True) -> dict:
-    """Assert the GPU's packed bytes agree with the oracle's encode of ``keys``.
+def compare_fields(inp: Inputs, got: dict, e: dict, x: np.ndarray) -> dict:
+    """Assert the GPU's per-key fields (idx, z, n, rho of keys ``x`` [n][d],
+    fp64) agree with the oracle's encoding ``e`` of the same keys.
 
     A coordinate within 1e-5 of a boundary may take either neighbouring code;
     the key's residual, rho and signs then follow the code taken, so such a key
     is compared against the oracle's own encoding with that boundary resolved
     the other way (``qjl_stage`` on the alternative codes)."""
-    G, N, d = keys.shape
-    want_bytes, e = oracle_encode(inp, keys)
-    got = o.unpack(gpu_bytes, d, inp.bits, inp.mode, G, N)
-    want = o.unpack(want_bytes, d, inp.bits, inp.mode, G, N)
-    total = G * N * d
-    code_bad = got["idx"] != want["idx"]
+    total = x.size
+    code_bad = got["idx"] != e["idx"]
     assert not np.any(code_bad & ~e["code_exempt"]), "code mismatch outside the boundary band"
     # a flipped code must be the neighbour across the near boundary
-    assert np.all(np.abs(got["idx"][code_bad] - want["idx"][code_bad]) == 1), "flip to a non-neighbour code"
+    assert np.all(np.abs(got["idx"][code_bad] - e["idx"][code_bad]) == 1), "flip to a non-neighbour code"
     stats = dict(code_mismatch=int(code_bad.sum()), coords=total)
     mism = int(code_bad.sum())
-    n = want["n"]
+    n = e["n"]
     assert np.all(np.abs(got["n"] - n) <= 1e-6 * n + 1e-30), "norm mismatch"
     if inp.mode == "prod":
         z_ref, rho_ref, band = e["z"].copy(), e["rho"].copy(), e["sign_exempt"].copy()
         flipped = np.where(code_bad.any(axis=1))[0]
         if flipped.size:
-            x = keys.detach().cpu().double().numpy().reshape(G * N, d)[flipped]
-            alt_idx = want["idx"][flipped].copy()
+            alt_idx = e["idx"][flipped].copy()
             alt_idx[code_bad[flipped]] = got["idx"][flipped][code_bad[flipped]]
-            alt = o.qjl_stage(x, alt_idx, e["n"][flipped], inp.Pi_o, inp.S_o, inp.c_o)
+            alt = o.qjl_stage(x[flipped], alt_idx, n[flipped], inp.Pi_o, inp.S_o, inp.c_o)
             z_ref[flipped], rho_ref[flipped], band[flipped] = alt["z"], alt["rho"], alt["sign_exempt"]
         sign_bad = got["z"] != z_ref
         bad_rows = np.where((sign_bad & ~band).any(axis=1))[0]
@@ -88,7 +84,19 @@ def compare_encode(inp: Inputs, gpu_bytes: np.ndarray, keys: torch.Tensor, check
     # couple of band-exempt flips are allowed, above it the rate must be <= 1e-5
     assert mism <= max(1e-5 * total, 2 if total < 10 ** 6 else 0), \
         f"mismatch rate {mism / total:.2e} above 1e-5 ({mism} of {total})"
-    if check_bytes and mism == 0:
+    stats["mismatches"] = mism
+    return stats
+
+
+def compare_encode(inp: Inputs, gpu_bytes: np.ndarray, keys: torch.Tensor, check_bytes=True) -> dict:
+    """Assert the GPU's packed bytes agree with the oracle's encode of ``keys``
+    (all keys; see compare_fields for the rules)."""
+    G, N, d = keys.shape
+    want_bytes, e = oracle_encode(inp, keys)
+    got = o.unpack(gpu_bytes, d, inp.bits, inp.mode, G, N)
+    x = keys.detach().cpu().double().numpy().reshape(G * N, d)
+    stats = compare_fields(inp, got, e, x)
+    if check_bytes and stats["mismatches"] == 0:
         # every code and sign bit agrees: the plane bytes, including the zero
         # padding of the last block, are identical
         nb = -(-N // 128)
