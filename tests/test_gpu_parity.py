@@ -150,7 +150,9 @@ def test_decode_score_consistency_on_gpu(cuda):
     compare_logits(s.cpu().numpy(), via_decode, q.cpu(), n)
 
 
-@pytest.mark.parametrize("G,N,H,d", [(1, 1, 1, 128), (2, 300, 4, 128), (1, 100, 256, 128), (1, 50, 3, 1536)])
+@pytest.mark.parametrize("G,N,H,d", [(1, 1, 1, 128), (2, 300, 4, 128), (1, 100, 256, 128), (1, 50, 3, 1536),
+                                     (3, 1000, 12, 128), (2, 129, 9, 64), (1, 257, 16, 132), (2, 5, 2, 8),
+                                     (1, 515, 17, 128), (4, 33, 1, 128)])
 def test_fp32_baseline(cuda, G, N, H, d):
     g = torch.Generator().manual_seed(5)
     q = torch.randn(G, H, d, generator=g)
@@ -161,6 +163,14 @@ def test_fp32_baseline(cuda, G, N, H, d):
     bound = 1e-5 * (torch.linalg.vector_norm(q.double(), dim=-1)[:, :, None] *
                     torch.linalg.vector_norm(x.double(), dim=-1)[:, None, :]).numpy()
     assert np.all(np.abs(got.cpu().numpy() - want) <= bound)
+
+
+def test_fp32_baseline_rejects_ragged_rows(cuda):
+    """Rows must be a whole number of 16-byte chunks (d % 4 == 0)."""
+    q = torch.zeros(1, 2, 6, device=cuda)
+    x = torch.zeros(1, 5, 6, device=cuda)
+    with pytest.raises(tq.TQError):
+        tq.tq_score_fp32(q, x)
 
 
 def test_end_to_end_gpu_encode_then_score(cuda):

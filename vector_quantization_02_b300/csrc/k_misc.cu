@@ -144,6 +144,153 @@ cudaError_t launch_decode_kb(const tq_plan* p, const uint8_t* packed, int64_t G,
   return cudaGetLastError();
 }
 
+// Streaming form for d % 4 == 0, d <= 1024: thread t of a block owns key t of
+// its 128-key tile and reads it with 16-byte loads; the group's queries sit in
+// shared memory and are read as broadcasts, eight heads per pass over the key.
+// Logit stores are coalesced (consecutive threads, consecutive tokens).
+constexpr int kF32Tile = 128;
+constexpr int kF32Heads = 8;
+
+__global__ void __launch_bounds__(kF32Tile)
+score_fp32_stream_kernel(const float* __restrict__ q, const float* __restrict__ x, int64_t G, int H, int64_t N,
+                         int d, int64_t n_tiles, float* __restrict__ logits) {
+  extern __shared__ float4 qs4[];  // [H][d / 4]
+  const int d4 = d >> 2;
+  const int64_t tiles_per_group = (N + kF32Tile - 1) / kF32Tile;
+  int64_t cur_g = -1;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t g = tile / tiles_per_group;
+    const int64_t tok = (tile - g * tiles_per_group) * kF32Tile + threadIdx.x;
+    if (g != cur_g) {
+      __syncthreads();
+      const float4* qg = reinterpret_cast<const float4*>(q + g * H * d);
+      for (int i = threadIdx.x; i < H * d4; i += kF32Tile) qs4[i] = __ldg(qg + i);
+      __syncthreads();
+      cur_g = g;
+    }
+    if (tok >= N) continue;
+    const float4* xr = reinterpret_cast<const float4*>(x + (g * N + tok) * d);
+    float* out = logits + (g * H) * N + tok;
+    for (int h0 = 0; h0 < H; h0 += kF32Heads) {
+      float acc[kF32Heads];
+#pragma unroll
+      for (int h = 0; h < kF32Heads; ++h) acc[h] = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < d4; ++j) {
+        const float4 xv = __ldg(xr + j);
+#pragma unroll
+        for (int h = 0; h < kF32Heads; ++h) {
+          if (h0 + h < H) {
+            const float4 qv = qs4[(h0 + h) * d4 + j];
+            acc[h] = fmaf(qv.x, xv.x, fmaf(qv.y, xv.y, fmaf(qv.z, xv.z, fmaf(qv.w, xv.w, acc[h]))));
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kF32Heads; ++h)
+        if (h0 + h < H) out[(int64_t)(h0 + h) * N] = acc[h];
+    }
+  }
+}
+
+// d = 128: eight lanes share a key, lane c reading its 16-byte chunks c, c+8,
+// c+16, c+24, so one load instruction covers four whole 128-byte key rows. Each
+// lane forms partial dot products for eight heads (queries from shared memory,
+// the eight lanes of a key reading eight distinct chunks), and a reduce-scatter
+// across the eight lanes leaves lane c with head c's logit for its key. A warp
+// takes sixteen keys (four loads of four rows in flight per chunk), a block
+// 128 consecutive keys of one group, so the tiles spread evenly over a grid
+// of resident blocks.
+constexpr int kD128Sub = 4;  // groups of four keys per warp
+constexpr int kD128Tile = 8 * 4 * kD128Sub;
+
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
+}
+
+// Eight partial sums per lane -> lane (c) of each 8-lane group holds the group's
+// total for value index c. Round with offset s keeps the half whose index bit
+// matches the lane's bit s and sends the other half to the partner lane.
+__device__ __forceinline__ float reduce_scatter8(float (&v)[8], int c) {
+  const bool u4 = c & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = u4 ? v[i] : v[i + 4];
+    const float keep = u4 ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  const bool u2 = c & 2;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = u2 ? v[i] : v[i + 2];
+    const float keep = u2 ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  const bool u1 = c & 1;
+  const float send = u1 ? v[0] : v[1];
+  const float keep = u1 ? v[1] : v[0];
+  return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+}
+
+__global__ void __launch_bounds__(256, 2)
+score_fp32_d128_kernel(const float* __restrict__ q, const float* __restrict__ x, int64_t G, int H, int64_t N,
+                       int64_t n_tiles, float* __restrict__ logits) {
+  extern __shared__ float4 qs4[];  // [H][32]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = lane & 7, tg = lane >> 3;
+  const int64_t tiles_per_group = (N + kD128Tile - 1) / kD128Tile;
+  int64_t cur_g = -1;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t g = tile / tiles_per_group;
+    const int64_t tile_tok = (tile - g * tiles_per_group) * kD128Tile;
+    if (g != cur_g) {
+      __syncthreads();
+      const float4* qg = reinterpret_cast<const float4*>(q + g * H * 128);
+      for (int i = threadIdx.x; i < H * 32; i += blockDim.x) qs4[i] = __ldg(qg + i);
+      __syncthreads();
+      cur_g = g;
+    }
+    const float4* xg = reinterpret_cast<const float4*>(x + g * N * 128);
+    float* lg = logits + g * H * N;
+    {
+      const int64_t base = tile_tok + warp * 4 * kD128Sub;
+      if (base >= N) continue;
+      int64_t tok[kD128Sub];
+      float4 xv[kD128Sub][4];
+#pragma unroll
+      for (int s2 = 0; s2 < kD128Sub; ++s2) {
+        tok[s2] = base + s2 * 4 + tg;
+        const bool ok = tok[s2] < N;
+        const float4* row = xg + (ok ? tok[s2] : 0) * 32 + c;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xv[s2][j] = ok ? __ldg(row + 8 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int h0 = 0; h0 < H; h0 += 8) {
+        float acc[kD128Sub][8];
+#pragma unroll
+        for (int s2 = 0; s2 < kD128Sub; ++s2)
+#pragma unroll
+          for (int h = 0; h < 8; ++h) acc[s2][h] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const int hh = h0 + h < H ? h0 + h : H - 1;  // padded heads repeat a real one, stored nowhere
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 qv = qs4[hh * 32 + c + 8 * j];
+#pragma unroll
+            for (int s2 = 0; s2 < kD128Sub; ++s2) acc[s2][h] = dot4(qv, xv[s2][j], acc[s2][h]);
+          }
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < kD128Sub; ++s2) {
+          const float r = reduce_scatter8(acc[s2], c);
+          if (tok[s2] < N && h0 + c < H) lg[(int64_t)(h0 + c) * N + tok[s2]] = r;
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s) {
@@ -179,6 +326,31 @@ static cudaError_t launch_fp32_kt(const float* q, const float* x, int64_t G, int
 cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, int64_t N, int d,
                               float* logits, cudaStream_t s) {
   if (G * N == 0 || H == 0) return cudaSuccess;
+  const size_t qbytes = (size_t)H * d * sizeof(float);
+  if (d == 128 && qbytes <= 96 * 1024) {
+    const int64_t n_tiles = G * ((N + kD128Tile - 1) / kD128Tile);
+    cudaError_t e = cudaFuncSetAttribute(score_fp32_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)qbytes);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t grid = n_tiles < (int64_t)sms * 2 ? n_tiles : (int64_t)sms * 2;
+    score_fp32_d128_kernel<<<(unsigned)grid, 256, qbytes, s>>>(q, x, G, H, N, n_tiles, logits);
+    return cudaGetLastError();
+  }
+  if (d % 4 == 0 && d <= 1024 && qbytes <= 96 * 1024) {
+    const int64_t n_tiles = G * ((N + kF32Tile - 1) / kF32Tile);
+    cudaError_t e = cudaFuncSetAttribute(score_fp32_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)qbytes);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t grid = n_tiles < (int64_t)sms * 16 ? n_tiles : (int64_t)sms * 16;
+    score_fp32_stream_kernel<<<(unsigned)grid, kF32Tile, qbytes, s>>>(q, x, G, H, N, d, n_tiles, logits);
+    return cudaGetLastError();
+  }
   if (d <= 1024) return launch_fp32_kt<32>(q, x, G, H, N, d, logits, s);
   return launch_fp32_kt<8>(q, x, G, H, N, d, logits, s);
 }
