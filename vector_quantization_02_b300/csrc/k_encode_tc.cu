@@ -62,6 +62,7 @@ constexpr uint32_t kSmemBytes = kOffBar + BAR_COUNT * 8 + 16 + 1024;  // + slot,
 struct EncTcArgs {
   Layout lay;
   CodeParams cp;
+  ParityExpansion px;
   int64_t G, N, nb, n_tiles;
   const uint8_t* pi_hi;
   const uint8_t* pi_lo;
@@ -85,7 +86,11 @@ __device__ __forceinline__ float2 pair_to_float2(uint32_t w) {
   }
 }
 
-template <int L, bool kBF16>
+// PX: the codebook's parity expansion has the odd-weight masks of a symmetric
+// codebook ({1}, {1, 2} or {1, 2, 4, 7}); the centroid n c[idx] is then summed
+// from the code bits' sign words (one LOP3 and one FADD per term) instead of
+// selected threshold by threshold.
+template <int L, bool kBF16, bool PX>
 __global__ void __launch_bounds__(kThreads, 1)
 encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
   constexpr int K = L == 2 ? 1 : L == 4 ? 2 : 3;  // code planes
@@ -272,6 +277,13 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       for (int q = 0; q < L - 1; ++q) nt[q] = sc * a.cp.t[q];
 #pragma unroll
       for (int q = 0; q < L; ++q) nc[q] = n * a.cp.c[q];
+      // signed-form terms: -n half[t] as bits (the sign flips where the term's
+      // parity is 1), and n mid
+      constexpr int NT = K == 1 ? 1 : K == 2 ? 2 : 4;
+      uint32_t nhalf[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) nhalf[t] = __float_as_uint(-(n * a.px.half[t]));
+      const float nmid = n * a.px.mid;
 
       // E2 result -> E3 codes, E4 residual; the residual's bf16 split goes back
       // into the same TMEM columns as the A operand of E5
@@ -308,17 +320,30 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
 #pragma unroll
             for (int q = 0; q < L - 1; ++q) {
               sbit[q] = __float_as_uint(nt[q] - y);
-              cv = (int)sbit[q] < 0 ? nc[q + 1] : cv;
+              if constexpr (!PX) cv = (int)sbit[q] < 0 ? nc[q + 1] : cv;
             }
             // bit p of idx = #{q : y > n t_q} is the XOR of the sign bits of
             // the thresholds q with (q + 1) % 2^p == 0 (the count is monotone)
+            uint32_t xb[K];
 #pragma unroll
             for (int p = 0; p < K; ++p) {
               uint32_t x = 0;
 #pragma unroll
               for (int q = 0; q < L - 1; ++q)
                 if (((q + 1) & ((1 << p) - 1)) == 0) x ^= sbit[q];
+              xb[p] = x;
               w[p] = __funnelshift_l(x, w[p], 1);
+            }
+            if constexpr (PX) {
+              // term t contributes +n half[t] where its parity (bit 31 of the
+              // XOR of its bits' sign words) is 1, else -n half[t]
+              constexpr uint32_t kS = 0x80000000u;
+              cv = nmid + __uint_as_float(nhalf[0] ^ (xb[0] & kS));
+              if constexpr (K >= 2) cv += __uint_as_float(nhalf[1] ^ (xb[1] & kS));
+              if constexpr (K == 3) {
+                cv += __uint_as_float(nhalf[2] ^ (xb[2] & kS));
+                cv += __uint_as_float(nhalf[3] ^ ((xb[0] ^ xb[1] ^ xb[2]) & kS));
+              }
             }
             const float rv = y - cv;
             rr = fmaf(rv, rv, rr);
@@ -422,7 +447,17 @@ EncodeTmapFn tmap_encoder() {
   return fn;
 }
 
-template <int L, bool kBF16>
+// The expansion's masks are those of a symmetric codebook with k code bits.
+bool odd_masks(const ParityExpansion& px, int k) {
+  static const uint32_t want[3][4] = {{1u}, {1u, 2u}, {1u, 2u, 4u, 7u}};
+  const int n = k == 3 ? 4 : k;
+  if (k < 1 || k > 3 || px.n != n) return false;
+  for (int i = 0; i < n; ++i)
+    if (px.mask[i] != want[k - 1][i]) return false;
+  return true;
+}
+
+template <int L, bool kBF16, bool PX>
 cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, uint8_t* packed, cudaStream_t s) {
   EncodeTmapFn enc = tmap_encoder();
   if (!enc) return cudaErrorNotSupported;
@@ -439,6 +474,7 @@ cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, 
   EncTcArgs a;
   a.lay = p->lay;
   a.cp = p->cp;
+  a.px = p->px;
   a.G = G;
   a.N = N;
   a.nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
@@ -450,7 +486,7 @@ cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, 
   a.m_lo = ops + 5 * kOpBytes;
   a.packed = packed;
   a.err = p->err;
-  auto kern = encode_tc_kernel<L, kBF16>;
+  auto kern = encode_tc_kernel<L, kBF16, PX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
@@ -471,11 +507,19 @@ bool encode_tc_supported(const tq_plan* p, tq_dtype dt) {
 cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N, uint8_t* packed,
                              cudaStream_t s) {
   const bool bf = dt == TQ_BF16;
+  const int k = p->cp.L == 2 ? 1 : p->cp.L == 4 ? 2 : 3;
+  const bool px = odd_masks(p->px, k);
+#define TQ_ENC_CASE(LV)                                                                                        \
+  case LV:                                                                                                     \
+    if (px) return bf ? launch_tc<LV, true, true>(p, keys, G, N, packed, s)                                    \
+                      : launch_tc<LV, false, true>(p, keys, G, N, packed, s);                                  \
+    return bf ? launch_tc<LV, true, false>(p, keys, G, N, packed, s) : launch_tc<LV, false, false>(p, keys, G, N, packed, s);
   switch (p->cp.L) {
-    case 2: return bf ? launch_tc<2, true>(p, keys, G, N, packed, s) : launch_tc<2, false>(p, keys, G, N, packed, s);
-    case 4: return bf ? launch_tc<4, true>(p, keys, G, N, packed, s) : launch_tc<4, false>(p, keys, G, N, packed, s);
-    case 8: return bf ? launch_tc<8, true>(p, keys, G, N, packed, s) : launch_tc<8, false>(p, keys, G, N, packed, s);
+    TQ_ENC_CASE(2)
+    TQ_ENC_CASE(4)
+    TQ_ENC_CASE(8)
   }
+#undef TQ_ENC_CASE
   return cudaErrorInvalidValue;
 }
 

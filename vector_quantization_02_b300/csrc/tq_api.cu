@@ -198,11 +198,15 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
       return TQ_EINVAL;
     }
     p->px.n = n;
+    double mid = c0;
     for (int i = 0; i < kMaxTerms; ++i) {
       p->px.mask[i] = i < n ? masks[i] : 0u;
       p->px.coef[i] = i < n ? (float)coefs[i] : 0.f;
+      p->px.half[i] = i < n ? (float)(0.5 * coefs[i]) : 0.f;
+      if (i < n) mid += 0.5 * coefs[i];
     }
     p->px.c0 = (float)c0;
+    p->px.mid = (float)mid;
   }
   if (L.prod && d == 128) {
     if (build_tc_ops(p) != cudaSuccess) {

@@ -32,6 +32,11 @@ struct ParityExpansion {
   uint32_t mask[kMaxTerms];
   float coef[kMaxTerms];
   float c0;
+  // the same expansion in signed form, for arithmetic on sign bits:
+  //   c[idx] = mid + sum_t (parity ? half[t] : -half[t]),
+  // half[t] = coef[t] / 2 and mid = c0 + sum_t coef[t] / 2 (rounded from fp64)
+  float half[kMaxTerms];
+  float mid;
 };
 
 // Geometry of the packed layout for one plan.
