@@ -48,15 +48,15 @@ def peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
-def kernel_traffic(kernel: str, source: str):
+def kernel_traffic(kernel: str, source: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel; else None."""
+    this workload and the current source of the kernel; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f).get(kernel)
         with open(os.path.join(ROOT, "vector_quantization_02_b300", "csrc", source), "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
-        if t and t.get("source_sha") == sha:
+        if t and t.get("source_sha") == sha and t.get("workload") == workload:
             return t["dram_bytes_per_launch"]
     except (OSError, ValueError, KeyError):
         pass
@@ -295,19 +295,32 @@ def run_ours(args, world, rank):
     sc_bytes = P + logit_bytes + q_bytes
     hbm = pk["hbm_gbs"]
 
+    tflops_peak = pk.get("bf16_tflops", FALLBACK_PEAKS.get("bf16_tflops"))
+
     def roof(bytes_, ms, kernel, source, flops=None):
+        """HBM roofline, or the bf16 tensor roofline where the algorithmic flops
+        at that peak take longer than the bytes at HBM speed."""
         ach = bytes_ / (ms * 1e-3) / 1e9
-        r = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
-             "traffic": kernel_traffic(kernel, source), "algorithmic_bytes": bytes_, "peak_source": pk_kind}
+        tensor = flops is not None and flops / (tflops_peak * 1e12) > bytes_ / (hbm * 1e9)
+        if tensor:
+            tf = flops / (ms * 1e-3) / 1e12
+            r = {"bound": "tensor", "achieved": round(tf, 2), "peak": tflops_peak, "unit": "TFLOP/s",
+                 "frac": round(tf / tflops_peak, 4)}
+        else:
+            r = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4)}
+        r.update({"traffic": kernel_traffic(kernel, source, w.name), "algorithmic_bytes": bytes_,
+                  "peak_source": pk_kind, "kernel": kernel})
         if flops is not None:
             r["algorithmic_flops"] = flops
             r["tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
+            r["gbs"] = round(ach, 1)
         return r
 
-    tc = d == 128 and w.key_dtype in (torch.float16, torch.bfloat16)
-    enc_kernel, enc_src = ("encode_tc", "k_encode_tc.cu") if tc else ("encode_simt", "k_encode_simt.cu")
+    kernels = {"tensor_d128": ("{}_tc", "k_{}_tc.cu"), "tensor_wide": ("{}_wide", "k_{}_wide.cu"),
+               "cuda_core": ("{}_simt", "k_{}_simt.cu")}
+    ek, es = kernels[plan.encode_path(w.key_dtype)]
+    enc_kernel, enc_src = ek.format("encode"), es.format("encode")
     enc_roof = roof(enc_bytes, enc_ms, enc_kernel, enc_src, flops=4 * d * d * G * N)
-    enc_roof["kernel"] = enc_kernel
 
     # score alone on a cold L2 (a decode step reads a cache encoded earlier)
     sc_cold = []
@@ -321,9 +334,14 @@ def run_ours(args, world, rank):
         sc_cold.append((a, b))
     torch.cuda.synchronize()
     sc_cold_ms = statistics.median(a.elapsed_time(b) for a, b in sc_cold)
-    sc_tc = d == 128 and H <= 16 and bits <= 4
-    sc_roof = roof(sc_bytes, sc_cold_ms, *(("score_tc", "k_score_tc.cu") if sc_tc else ("score_simt", "k_score_simt.cu")))
-    sc_roof["kernel"] = "score_tc" if sc_tc else "score_simt"
+    sk, ss = kernels[plan.score_path(H)]
+    arith = {"encode_tc": "f16/bf16 split operands on tensor cores", "encode_simt": "f32",
+             "score_tc": "e4m3 bit planes and query slices on tensor cores", "score_wide":
+             "bf16 split operands on tensor cores", "score_simt": "f32"}
+    dtype_desc = (f"encode: {arith[enc_kernel]}; score: {arith[sk.format('score')]}; f32 accumulate")
+    # algorithmic flops of the estimate: two length-d dot products per (key, head)
+    sc_roof = roof(sc_bytes, sc_cold_ms, sk.format("score"), ss.format("score"),
+                   flops=(2 if plan.mode == "prod" else 1) * 2 * d * H * G * N)
 
     # the uncompressed baseline on the same keys (fp32 copies), cold L2
     base = None
@@ -342,7 +360,8 @@ def run_ours(args, world, rank):
         torch.cuda.synchronize()
         bms = statistics.median(a.elapsed_time(b) for a, b in bt)
         base = {"ms": round(bms, 4), "keys_per_s": G * N / (bms * 1e-3),
-                "roofline": roof(keys32.numel() * 4 + logit_bytes + q_bytes, bms, "score_fp32", "k_misc.cu"),
+                "roofline": roof(keys32.numel() * 4 + logit_bytes + q_bytes, bms, "score_fp32", "k_misc.cu",
+                                 flops=2 * d * H * G * N),
                 "score_speedup_vs_fp32_keys": round(bms / sc_cold_ms, 3)}
         del keys32, base_l
 
@@ -356,7 +375,7 @@ def run_ours(args, world, rank):
     line = {
         "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16/bf16 tensor (split operands, f32 accumulate) + f32" if tc else "f32",
+        "vs_baseline": None, "dtype": dtype_desc,
         "data": "synthetic",
         "config": {"workload": w.name, "G": G, "N": N, "H": H, "d": d, "bits": bits,
                    "key_dtype": str(w.key_dtype).replace("torch.", ""), "top_k": top_k,

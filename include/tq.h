@@ -201,6 +201,16 @@ const char* tq_status_string(tq_status status);
 /* Version of the packed layout described above (bumped on any change). */
 int tq_format_version(void);
 
+/* Which kernel family a call takes, for reports and tests (no GPU work):
+ *   TQ_PATH_TENSOR_D128  tcgen05 kernels specialised for d = 128 (encode: fp16/bf16
+ *                        keys, Prod; score: H <= 16, odd-symmetric codebook, k <= 3);
+ *   TQ_PATH_TENSOR_WIDE  tcgen05 score for any d (multiple of 128), H <= 256;
+ *   TQ_PATH_CUDA_CORE    CUDA-core kernels (every other shape).
+ * Returns the path, or TQ_EINVAL for a null plan or an out-of-range argument. */
+typedef enum { TQ_PATH_TENSOR_D128 = 0, TQ_PATH_TENSOR_WIDE = 1, TQ_PATH_CUDA_CORE = 2 } tq_path;
+int tq_score_path(const tq_plan* plan, int n_heads);
+int tq_encode_path(const tq_plan* plan, tq_dtype dtype);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,6 +66,13 @@ def test_encode_special_keys(cuda):
 
 SCORE_CASES = [
     # d, G, N, H, bits, mode
+    # wide tensor-core path (d != 128 or H > 16): heads padded to 16, all 256
+    # heads, d = 384, MSE with 16 levels, d = 1536 over a ragged tail
+    (128, 2, 300, 40, 3, "prod"),
+    (128, 1, 257, 256, 4, "prod"),
+    (384, 2, 129, 17, 2, "prod"),
+    (256, 1, 300, 20, 4, "mse"),
+    (1536, 1, 385, 64, 4, "prod"),
     (128, 1, 1, 1, 3, "prod"),
     (128, 2, 300, 4, 2, "prod"),
     (128, 3, 129, 8, 3, "prod"),
@@ -98,6 +105,7 @@ def test_score_from_oracle_packed_keys(cuda, d, G, N, H, bits, mode):
     plan = inp.plan()
     got = tq.tq_score(plan, q.to(cuda), torch.from_numpy(buf.copy()).to(cuda), N)
     torch.cuda.synchronize()
+    assert plan.status() == 0
     n = e["n"].astype(np.float32).astype(np.float64).reshape(G, N)
     compare_logits(got.cpu().numpy(), want, q, n)
 
@@ -210,3 +218,19 @@ def test_argument_errors_on_gpu(cuda):
         tq.tq_score(plan, torch.randn(1, 300, 128, device=cuda), packed, 10)
     with pytest.raises(tq.TQError):
         tq.tq_score(plan, torch.randn(1, 2, 128, device=cuda), packed, 10, top_k=11)
+
+
+@pytest.mark.parametrize("d,bits,mode,H,dtype,score_path,encode_path", [
+    (128, 3, "prod", 8, torch.float16, "tensor_d128", "tensor_d128"),     # decode cache
+    (128, 4, "prod", 4, torch.bfloat16, "tensor_d128", "tensor_d128"),    # long context
+    (128, 3, "prod", 16, torch.float32, "tensor_d128", "cuda_core"),      # single head, fp32 keys
+    (1536, 4, "prod", 256, torch.float32, "tensor_wide", "cuda_core"),    # vector search
+    (128, 3, "prod", 40, torch.float16, "tensor_wide", "tensor_d128"),
+    (256, 4, "mse", 20, torch.bfloat16, "tensor_wide", "cuda_core"),
+])
+def test_dispatch_paths(cuda, d, bits, mode, H, dtype, score_path, encode_path):
+    """The kernel family each workload's shape takes (so bench labels and
+    rooflines name the kernel that ran)."""
+    plan = Inputs(d, bits, mode, 11, 12).plan()
+    assert plan.score_path(H) == score_path
+    assert plan.encode_path(dtype) == encode_path

@@ -43,6 +43,8 @@ def _load() -> ctypes.CDLL:
         "tq_format_version": (c_int, []),
         "tq_score_noalloc": (c_int, [vp, vp, c_i64, c_int, vp, c_i64, vp, c_int, vp, vp, vp]),
         "tq_codebook_parity_expansion": (c_int, [c_int, vp, vp, vp, vp, vp]),
+        "tq_score_path": (c_int, [vp, c_int]),
+        "tq_encode_path": (c_int, [vp, c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -55,7 +57,8 @@ lib = _load()
 EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_plan_destroy",
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
             "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
-            "tq_codebook_parity_expansion")
+            "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path")
+PATHS = {0: "tensor_d128", 1: "tensor_wide", 2: "cuda_core"}
 TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
 
 
@@ -170,6 +173,18 @@ class Plan:
 
     def status(self) -> int:
         return int(lib.tq_plan_status(self.handle))
+
+    def score_path(self, H: int) -> str:
+        """Kernel family tq_score takes for H heads: tensor_d128, tensor_wide or cuda_core."""
+        r = int(lib.tq_score_path(self.handle, H))
+        _check(min(r, 0), "tq_score_path")
+        return PATHS[r]
+
+    def encode_path(self, dtype: torch.dtype) -> str:
+        """Kernel family tq_encode takes for keys of this dtype."""
+        r = int(lib.tq_encode_path(self.handle, _DTYPES[dtype]))
+        _check(min(r, 0), "tq_encode_path")
+        return PATHS[r]
 
 
 # ---------------------------------------------------------------- the path

@@ -430,23 +430,6 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-using EncodeTmapFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTmapFn tmap_encoder() {
-  static EncodeTmapFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTmapFn>(p);
-  }
-  return fn;
-}
-
 // The expansion's masks are those of a symmetric codebook with k code bits.
 bool odd_masks(const ParityExpansion& px, int k) {
   static const uint32_t want[3][4] = {{1u}, {1u, 2u}, {1u, 2u, 4u, 7u}};
@@ -459,18 +442,10 @@ bool odd_masks(const ParityExpansion& px, int k) {
 
 template <int L, bool kBF16, bool PX>
 cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, uint8_t* packed, cudaStream_t s) {
-  EncodeTmapFn enc = tmap_encoder();
-  if (!enc) return cudaErrorNotSupported;
   CUtensorMap tm;
-  const cuuint64_t dims[2] = {128, (cuuint64_t)(G * N)};
-  const cuuint64_t strides[1] = {256};
-  const cuuint32_t box[2] = {64, 128};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&tm, kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                   const_cast<void*>(keys), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const cudaError_t te = make_tmap_2d(&tm, kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                      keys, 128, (uint64_t)(G * N), 256, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (te != cudaSuccess) return te;
   EncTcArgs a;
   a.lay = p->lay;
   a.cp = p->cp;
@@ -521,6 +496,37 @@ cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, in
   }
 #undef TQ_ENC_CASE
   return cudaErrorInvalidValue;
+}
+
+
+using EncodeTmapFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTmapFn tmap_encoder() {
+  static EncodeTmapFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTmapFn>(p);
+  }
+  return fn;
+}
+
+cudaError_t make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                         uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTmapFn enc = tmap_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace tq

@@ -291,6 +291,86 @@ score_fp32_d128_kernel(const float* __restrict__ q, const float* __restrict__ x,
   }
 }
 
+// Many heads or long rows (e.g. 256 queries of d = 1536): a register-tiled
+// fp32 product per group, logits[h][t] = sum_j q[h][j] x[t][j].  A block owns 64
+// heads x 128 keys and walks d in steps of 16 through k-major shared tiles;
+// thread (ty, tx) accumulates heads 4 ty .. 4 ty + 3 against keys 8 tx .. 8 tx + 7.
+// Blocks of the same key tile are adjacent in the grid (head tile fastest), so
+// a key row is fetched from HBM once and re-read from L2.
+constexpr int kGH = 64, kGT = 128, kGK = 16;
+
+__global__ void __launch_bounds__(256)
+score_fp32_gemm_kernel(const float* __restrict__ q, const float* __restrict__ x, int H, int64_t N, int d,
+                       int h_tiles, int64_t t_tiles, float* __restrict__ logits) {
+  __shared__ __align__(16) float qs[kGK][kGH];
+  __shared__ __align__(16) float xs[kGK][kGT];
+  const int64_t bid = blockIdx.x;
+  const int ht = (int)(bid % h_tiles);
+  const int64_t rest = bid / h_tiles;
+  const int64_t tt = rest % t_tiles, g = rest / t_tiles;
+  const int h0 = ht * kGH;
+  const int64_t t0 = tt * kGT;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const float* qg = q + (g * H) * (int64_t)d;
+  const float* xg = x + (g * N) * (int64_t)d;
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < d; k0 += kGK) {
+    // q tile: 64 heads x 16 coordinates (one float4 per thread)
+    {
+      const int r = tid >> 2, c = (tid & 3) * 4;
+      const float4 v = h0 + r < H ? __ldg(reinterpret_cast<const float4*>(qg + (int64_t)(h0 + r) * d + k0 + c))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      qs[c + 0][r] = v.x;
+      qs[c + 1][r] = v.y;
+      qs[c + 2][r] = v.z;
+      qs[c + 3][r] = v.w;
+    }
+    // key tile: 128 keys x 16 coordinates (two float4 per thread)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = tid + u * 256, r = i >> 2, c = (i & 3) * 4;
+      const float4 v = t0 + r < N ? __ldg(reinterpret_cast<const float4*>(xg + (t0 + r) * d + k0 + c))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      xs[c + 0][r] = v.x;
+      xs[c + 1][r] = v.y;
+      xs[c + 2][r] = v.z;
+      xs[c + 3][r] = v.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kGK; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&qs[k][ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&xs[k][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&xs[k][tx * 8 + 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int h = h0 + ty * 4 + i;
+    if (h >= H) continue;
+    float* out = logits + (g * H + h) * N + t0 + tx * 8;
+    if (t0 + tx * 8 + 8 <= N && (N & 3) == 0) {
+      reinterpret_cast<float4*>(out)[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      reinterpret_cast<float4*>(out)[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (t0 + tx * 8 + j < N) out[j] = acc[i][j];
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s) {
@@ -327,6 +407,13 @@ cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, 
                               float* logits, cudaStream_t s) {
   if (G * N == 0 || H == 0) return cudaSuccess;
   const size_t qbytes = (size_t)H * d * sizeof(float);
+  if (d % kGK == 0 && (H > 16 || d > 1024)) {
+    const int h_tiles = (H + kGH - 1) / kGH;
+    const int64_t t_tiles = (N + kGT - 1) / kGT;
+    const int64_t blocks = G * t_tiles * h_tiles;
+    score_fp32_gemm_kernel<<<(unsigned)blocks, 256, 0, s>>>(q, x, H, N, d, h_tiles, t_tiles, logits);
+    return cudaGetLastError();
+  }
   if (d == 128 && qbytes <= 96 * 1024) {
     const int64_t n_tiles = G * ((N + kD128Tile - 1) / kD128Tile);
     cudaError_t e = cudaFuncSetAttribute(score_fp32_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

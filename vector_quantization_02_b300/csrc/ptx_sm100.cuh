@@ -177,4 +177,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_type, uint32_t M, u
 }
 
 }  // namespace ptx
+
+// Host: a 2-D tiled tensor map (rows of `cols` elements, `row_bytes` apart) whose
+// box is box_cols x box_rows elements.
+cudaError_t make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                         uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+
 }  // namespace tq

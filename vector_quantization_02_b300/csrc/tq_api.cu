@@ -84,9 +84,9 @@ namespace tq {
 
 // Workspace: [tensor-core query images and constants | Pi q, S q] [top-k candidates]
 size_t score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k) {
-  const size_t prep = score_tc_supported(p, H)
-                          ? score_tc_workspace_bytes(p, G, H)
-                          : (size_t)G * H * qs_vectors(p) * p->d * sizeof(float);
+  const size_t prep = score_tc_supported(p, H)     ? score_tc_workspace_bytes(p, G, H)
+                      : score_wide_supported(p, H) ? score_wide_workspace_bytes(p, G, H)
+                                                   : (size_t)G * H * qs_vectors(p) * p->d * sizeof(float);
   return align256(prep) + topk_workspace_bytes(G * H, N, top_k) + 256;
 }
 
@@ -97,6 +97,9 @@ cudaError_t score_run(const tq_plan* p, const float* queries, int64_t G, int H, 
   if (score_tc_supported(p, H)) {
     prep = score_tc_workspace_bytes(p, G, H);
     e = launch_score_tc(p, queries, G, H, packed, N, logits, ws, s);
+  } else if (score_wide_supported(p, H)) {
+    prep = score_wide_workspace_bytes(p, G, H);
+    e = launch_score_wide(p, queries, G, H, packed, N, logits, ws, s);
   } else {
     prep = (size_t)G * H * qs_vectors(p) * p->d * sizeof(float);
     float* qs = static_cast<float*>(ws);
@@ -126,6 +129,18 @@ const char* tq_status_string(tq_status s) {
 }
 
 int tq_format_version(void) { return 1; }
+
+int tq_score_path(const tq_plan* p, int H) {
+  if (!p || H < 1 || H > 256) return TQ_EINVAL;
+  if (tq::score_tc_supported(p, H)) return TQ_PATH_TENSOR_D128;
+  if (tq::score_wide_supported(p, H)) return TQ_PATH_TENSOR_WIDE;
+  return TQ_PATH_CUDA_CORE;
+}
+
+int tq_encode_path(const tq_plan* p, tq_dtype dt) {
+  if (!p || (dt != TQ_F32 && dt != TQ_F16 && dt != TQ_BF16)) return TQ_EINVAL;
+  return tq::encode_tc_supported(p, dt) ? TQ_PATH_TENSOR_D128 : TQ_PATH_CUDA_CORE;
+}
 
 tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
                          void* stream, tq_plan** out) {

@@ -101,6 +101,11 @@ size_t score_tc_workspace_bytes(const tq_plan* p, int64_t G, int H);
 cudaError_t launch_score_tc(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed,
                             int64_t N, float* logits, void* ws, cudaStream_t s);
 
+bool score_wide_supported(const tq_plan* p, int H);
+size_t score_wide_workspace_bytes(const tq_plan* p, int64_t G, int H);
+cudaError_t launch_score_wide(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed,
+                              int64_t N, float* logits, void* ws, cudaStream_t s);
+
 // Scoring as tq_score performs it (query preparation, score kernel, optional
 // top-k) on a caller-provided workspace of at least score_workspace_bytes().
 size_t score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k);
