@@ -336,6 +336,7 @@ def run_ours(args, world, rank):
     sc_cold_ms = statistics.median(a.elapsed_time(b) for a, b in sc_cold)
     sk, ss = kernels[plan.score_path(H)]
     arith = {"encode_tc": "f16/bf16 split operands on tensor cores", "encode_simt": "f32",
+             "encode_wide": "f16 split operands on tensor cores",
              "score_tc": "e4m3 bit planes and query slices on tensor cores", "score_wide":
              "bf16 split operands on tensor cores", "score_simt": "f32"}
     dtype_desc = (f"encode: {arith[enc_kernel]}; score: {arith[sk.format('score')]}; f32 accumulate")

@@ -26,6 +26,12 @@ ENCODE_CASES = [
     (128, 2, 300, torch.float32, 1, "mse", False),
     (128, 2, 300, torch.float16, 3, "mse", True),
     (256, 1, 150, torch.bfloat16, 4, "mse", True),
+    # wide tensor-core encode: fp16 keys at d = 256, three 128-column jobs per
+    # phase at d = 384, 2-bit bf16 at d = 512, fp32 d = 1536 over a ragged tail
+    (256, 2, 200, torch.float16, 3, "prod", True),
+    (384, 1, 300, torch.float32, 3, "prod", True),
+    (512, 1, 129, torch.bfloat16, 2, "prod", False),
+    (1536, 1, 300, torch.float32, 4, "prod", False),
 ]
 
 
@@ -223,8 +229,8 @@ def test_argument_errors_on_gpu(cuda):
 @pytest.mark.parametrize("d,bits,mode,H,dtype,score_path,encode_path", [
     (128, 3, "prod", 8, torch.float16, "tensor_d128", "tensor_d128"),     # decode cache
     (128, 4, "prod", 4, torch.bfloat16, "tensor_d128", "tensor_d128"),    # long context
-    (128, 3, "prod", 16, torch.float32, "tensor_d128", "cuda_core"),      # single head, fp32 keys
-    (1536, 4, "prod", 256, torch.float32, "tensor_wide", "cuda_core"),    # vector search
+    (128, 3, "prod", 16, torch.float32, "tensor_d128", "tensor_wide"),    # single head, fp32 keys
+    (1536, 4, "prod", 256, torch.float32, "tensor_wide", "tensor_wide"),  # vector search
     (128, 3, "prod", 40, torch.float16, "tensor_wide", "tensor_d128"),
     (256, 4, "mse", 20, torch.bfloat16, "tensor_wide", "cuda_core"),
 ])

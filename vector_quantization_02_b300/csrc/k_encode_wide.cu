@@ -1,0 +1,690 @@
+// Encode on the tensor cores for any head dimension d (a multiple of 128) and
+// any key dtype, TurboQuantProd: the shape of a vector-search index (10^6
+// fp32 keys of d = 1536), where the two d x d projections are long dense
+// contractions.
+//
+// Same computation as the other encode kernels ("turboquant-pytorch 소개",
+// "1단계" then "2단계"): y = Pi x, codes idx_j = #{i : n t_i < y_j},
+// r = y - n c[idx] (rotated frame, unnormalised), rho = ||r||,
+// z = [M r >= 0] with M = S Pi^T.
+//
+// Exactness on fp16 tensor cores (fp32 accumulate): every operand is split
+// into an fp16 pair v = hi + lo (22 significant bits) and each product is
+// issued three times (hi hi, hi lo, lo hi; lo lo is ~2^-22 of a term).  At
+// d = 1536 the error of y reaches p = M r amplified by the norm of M's rows
+// (~d^1/2), so the operands carry powers of two that keep every lo part in
+// fp16's normal range: the key enters as u = 2^8 x / ||x|| (the loaders sum
+// ||x||^2 over the row first), Pi as 2^8 Pi, so Y = 2^16 Pi u, compared with
+// 2^16 t; the residual enters E5 as 2^10 r'.  Signs do not see the scales.
+//
+// A tile is 128 keys (one packed block).  Its work is a sequence of jobs,
+// each one fp32 accumulator of 128 keys x NC coordinates (NC = 256, or 128
+// when d is not a multiple of 256) over K = d in stages of 32 coordinates:
+//   d / NC E2 jobs  Y[:, chunk] = X Pi[chunk]^T, then quantised: code bits
+//                   into the packed block, the residual's split into a
+//                   per-SM scratch row (rows of this SM's CTA only),
+//   d / NC E5 jobs  P[:, chunk] = R M[chunk]^T, then the sign bits.
+// The scratch belongs to the SM: this kernel needs a whole SM (all 512 TMEM
+// columns, more than half of the shared memory), so no two of its CTAs, from
+// any launch, share one at a time.
+//  warp 0       producer: TMA loads of the B operand (hi and lo rows of Pi or
+//               M for the job's chunk, 64-byte swizzle) into a 4-stage ring.
+//  warp 1       TMEM owner (accumulator in [0, NC), key-operand ring in
+//               [256, 512)) and MMA issuer (one thread).
+//  warps 2-5    A operand: thread (warp w, lane l) owns key row 32 (w % 4) + l;
+//               per tile it first sums ||x||^2 over the row (compensated), then
+//               writes its 32 coordinates per stage into TMEM (8-stage ring):
+//               the scaled unit key for E2, the residual for E5.
+//  warps 6-13   epilogue: two warpgroups, each taking half of a job's columns.
+// Every wait is bounded: on expiry the kernel raises the plan's error word,
+// drains what it issued and frees its TMEM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx_sm100.cuh"
+#include "tq_internal.cuh"
+
+namespace tq {
+namespace {
+
+using namespace ptx;
+
+constexpr int kEThreads = 448;
+constexpr int kEpiWarp0 = 6;       // warps 2-5 load the A operand
+constexpr int kBStages = 4;
+constexpr int kAStages = 8;
+constexpr int kStageK = 32;        // coordinates per stage
+constexpr int kARing = 256;        // first TMEM column of the A ring
+constexpr int kAPartCols = 16;     // TMEM columns of one A part per stage (32 16-bit values)
+constexpr int kSliceCols = 128;    // output columns of a job (two partial accumulators of 128 columns)
+constexpr int kSliceStages = 4;    // stages (128 coordinates of K) per partial accumulator
+
+enum {
+  BAR_BFULL = 0,
+  BAR_BEMPTY = BAR_BFULL + kBStages,
+  BAR_AFULL = BAR_BEMPTY + kBStages,
+  BAR_AEMPTY = BAR_AFULL + kAStages,
+  BAR_DFULL = BAR_AEMPTY + kAStages,   // [2] partial accumulators
+  BAR_DEMPTY = BAR_DFULL + 2,
+  BAR_NREADY = BAR_DEMPTY + 2,
+  BAR_RREADY = BAR_NREADY + 1,
+  BAR_RHO = BAR_RREADY + 1,
+  BAR_DONE = BAR_RHO + 1,
+  BAR_COUNT = BAR_DONE + 1
+};
+
+struct EncWideArgs {
+  Layout lay;
+  CodeParams cp;
+  ParityExpansion px;
+  int NC, J, S;               // chunk columns, jobs per phase, stages per job
+  int nslots;                 // scratch slots (SM ids)
+  int64_t G, N, nb, n_tiles;
+  const void* keys;
+  uint8_t* packed;
+  void* scratch;              // [slot][2][128][d] fp16 residual 2^10 r' hi, lo
+  int* err;
+};
+
+__device__ __forceinline__ void raise(int* err, volatile int* abort) {
+  *abort = 1;
+  atomicExch(err, 1);
+}
+
+__device__ __forceinline__ uint64_t sdesc_k_sw64(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(512u >> 4) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)4 << 61);
+}
+
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+  return v;
+}
+
+// compensated sum (Neumaier) of squares
+struct KSum {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float v = x * x;
+    const float t = s + v;
+    c += fabsf(s) >= fabsf(v) ? (s - t) + v : (v - t) + s;
+    s = t;
+  }
+  __device__ __forceinline__ float value() const { return s + c; }
+};
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// fp16 hi + lo words of the pairs (a0, a1)
+__device__ __forceinline__ void split_h2(float a0, float a1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_h2(a0, a1);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  lo = pack_h2(a0 - f.x, a1 - f.y);
+}
+
+template <int DT>
+__device__ __forceinline__ float2 key_pair(uint32_t w) {
+  if constexpr (DT == 1) return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
+constexpr float kYScale = 65536.f;      // Y = 2^16 Pi u
+constexpr float kRScale = 1.f / 64.f;   // E5 operand 2^10 r' = 2^-6 (2^16 r')
+
+// DT: key dtype, 0 fp32, 1 fp16, 2 bf16.
+template <int L, int DT, bool PX>
+__global__ void __launch_bounds__(kEThreads, 1)
+encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_constant__ CUtensorMap tmM,
+                   const EncWideArgs a) {
+  constexpr int K = L == 2 ? 1 : L == 4 ? 2 : 3;  // code planes
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = smem_u32(smem);
+  const int d = a.lay.d, NC = a.NC, J = a.J, S = a.S;
+  const uint32_t part_bytes = (uint32_t)NC * 64u;  // NC rows x 32 16-bit values
+  const uint32_t stage_bytes = 2 * part_bytes;
+  const uint32_t off_bar = kBStages * stage_bytes;
+  float* s_n = reinterpret_cast<float*>(smem + off_bar + BAR_COUNT * 8);  // [128]
+  float* s_rr = s_n + 128;                                                 // [2][128]
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ uint32_t s_slot;
+  auto bar = [&](int i) { return sb + off_bar + 8u * (uint32_t)i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    s_slot = smid();
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(bar(BAR_BFULL + s), 1);
+      mbar_init(bar(BAR_BEMPTY + s), 1);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(bar(BAR_AFULL + s), 128);
+      mbar_init(bar(BAR_AEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(BAR_DFULL + b), 1);
+      mbar_init(bar(BAR_DEMPTY + b), 256);
+    }
+    mbar_init(bar(BAR_NREADY), 128);
+    mbar_init(bar(BAR_RREADY), 256);
+    mbar_init(bar(BAR_RHO), 256);
+    mbar_init(bar(BAR_DONE), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
+  if (s_slot >= (uint32_t)a.nslots) {  // cannot happen with a plan built on this device
+    if (threadIdx.x == 0) raise(a.err, abort);
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
+  uint16_t* scr = static_cast<uint16_t*>(a.scratch) + (size_t)s_slot * 2 * 128 * d;
+
+  const int64_t n_my = blockIdx.x < a.n_tiles ? (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmPi);
+      prefetch_tmap(&tmM);
+      uint32_t b = 0, ph = 0, issued = 0;
+      bool ok = true;
+      for (int64_t i = 0; ok && i < n_my; ++i) {
+        for (int job = 0; ok && job < 2 * J; ++job) {
+          const CUtensorMap* map = job < J ? &tmPi : &tmM;
+          const int row0 = (job % J) * NC;
+          for (int st = 0; st < S; ++st) {
+            if (!mbar_wait_suspend(bar(BAR_BEMPTY + b), ph ^ 1u, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(BAR_BFULL + b), stage_bytes);
+            tma_load_2d(sb + b * stage_bytes, map, st * kStageK, row0, bar(BAR_BFULL + b));
+            tma_load_2d(sb + b * stage_bytes + part_bytes, map, st * kStageK, d + row0, bar(BAR_BFULL + b));
+            ++issued;
+            if (++b == kBStages) {
+              b = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) raise(a.err, abort);
+      int dummy = 0;
+      for (uint32_t k = 0; k < (issued < kBStages ? issued : kBStages); ++k) {
+        b = b == 0 ? kBStages - 1 : b - 1;
+        if (b == kBStages - 1) ph ^= 1u;
+        mbar_wait(bar(BAR_BFULL + b), ph, &dummy);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(0u, 128, (uint32_t)NC);
+      uint32_t b = 0, bph = 0, s = 0, aph = 0, cq = 0;
+      bool ok = true;
+      for (int64_t i = 0; ok && i < n_my; ++i) {
+        for (int job = 0; ok && job < 2 * J; ++job) {
+          // K in slices of 128 coordinates, each into a fresh partial accumulator
+          for (int c = 0; ok && c < S / kSliceStages; ++c, ++cq) {
+            const uint32_t pb = cq & 1u, d_acc = tmem + pb * kSliceCols;
+            if (!mbar_wait_suspend(bar(BAR_DEMPTY + pb), ((cq >> 1) & 1u) ^ 1u, abort)) {
+              ok = false;
+              break;
+            }
+            for (int st = 0; st < kSliceStages; ++st) {
+              if (!mbar_wait_suspend(bar(BAR_BFULL + b), bph, abort) ||
+                  !mbar_wait_suspend(bar(BAR_AFULL + s), aph, abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t bq = sb + b * stage_bytes;
+              const uint32_t at = tmem + kARing + s * (2 * kAPartCols);
+#pragma unroll
+              for (int ks = 0; ks < 2; ++ks) {
+                const uint64_t b_hi = sdesc_k_sw64(bq) + 2u * ks, b_lo = sdesc_k_sw64(bq + part_bytes) + 2u * ks;
+                const uint32_t a_hi = at + 8 * ks, a_lo = at + kAPartCols + 8 * ks;
+                const uint32_t acc = (st == 0 && ks == 0) ? 0u : 1u;
+                mma_f16_ts(d_acc, a_hi, b_hi, idesc, acc);
+                mma_f16_ts(d_acc, a_hi, b_lo, idesc, 1u);
+                mma_f16_ts(d_acc, a_lo, b_hi, idesc, 1u);
+              }
+              mma_commit(bar(BAR_BEMPTY + b));
+              mma_commit(bar(BAR_AEMPTY + s));
+              if (++b == kBStages) {
+                b = 0;
+                bph ^= 1u;
+              }
+              if (++s == kAStages) {
+                s = 0;
+                aph ^= 1u;
+              }
+            }
+            if (!ok) break;
+            mma_commit(bar(BAR_DFULL + pb));
+          }
+        }
+      }
+      if (!ok) raise(a.err, abort);
+      mma_commit(bar(BAR_DONE));
+      int dummy = 0;
+      mbar_wait(bar(BAR_DONE), 0, &dummy);
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ A operand
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + kARing;
+    const __half* rhi = reinterpret_cast<const __half*>(scr) + (size_t)row * d;
+    const __half* rlo = reinterpret_cast<const __half*>(scr) + (size_t)(128 + row) * d;
+    uint32_t s = 0, aph = 0;
+    bool ok = true;
+    for (int64_t i = 0; ok && i < n_my; ++i) {
+      const int64_t tile = blockIdx.x + i * gridDim.x;
+      const int64_t g = tile / a.nb, blk = tile - g * a.nb;
+      const int64_t tok = blk * kTokensPerBlock + row;
+      const bool live = tok < a.N;
+      const char* xrow = static_cast<const char*>(a.keys) + (g * a.N + (live ? tok : 0)) * (int64_t)d * (DT == 0 ? 4 : 2);
+      // stage t of the tile: job t / S, coordinates 32 (t % S) ..; its raw
+      // 16-byte words are loaded one stage ahead of their conversion
+      const int T = 2 * J * S;
+      auto fetch = [&](int t, uint4 (&r)[8]) {
+        const int c0 = (t % S) * kStageK;
+        if (t < J * S) {
+          if constexpr (DT == 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(xrow) + c0 / 4;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) r[v] = live ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(xrow) + c0 / 8;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) r[v] = live ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+          }
+        } else {
+          const uint4* sh = reinterpret_cast<const uint4*>(rhi + c0);
+          const uint4* sl = reinterpret_cast<const uint4*>(rlo + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            r[v] = __ldcg(sh + v);
+            r[4 + v] = __ldcg(sl + v);
+          }
+        }
+      };
+      uint4 raw[8], nxt[8];
+      fetch(0, raw);
+      // ||x|| over the whole row (eight 16-byte loads in flight), then u = 2^8 x / ||x||
+      KSum n2;
+      if (live) {
+        const uint4* src = reinterpret_cast<const uint4*>(xrow);
+        const int nv = d * (DT == 0 ? 4 : 2) / 16;
+        for (int v0 = 0; v0 < nv; v0 += 8) {
+          uint4 w[8];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) w[v] = __ldg(src + v0 + v);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+            if constexpr (DT == 0) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) n2.add(__uint_as_float(ws[e]));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = key_pair<DT>(ws[e]);
+                n2.add(f.x);
+                n2.add(f.y);
+              }
+            }
+          }
+        }
+      }
+      const float n = sqrtf(n2.value());
+      const float inv = n > 0.f ? 256.f / n : 0.f;
+      s_n[row] = n;
+      mbar_arrive(bar(BAR_NREADY));
+      for (int t = 0; ok && t < T; ++t) {
+        if (t == J * S) {
+          // the residual rows of this tile are in the scratch once the epilogue
+          // has quantised the last E2 job, which needs every E2 stage delivered:
+          // no prefetch crosses this point
+          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_RREADY), (uint32_t)i & 1u, abort))) {
+            ok = false;
+            break;
+          }
+          fetch(t, raw);
+        }
+        if (t + 1 < T && t + 1 != J * S) fetch(t + 1, nxt);
+        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_AEMPTY + s), aph ^ 1u, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t hi[16], lo[16];
+        if (t < J * S) {
+          if constexpr (DT == 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 f = make_float4(__uint_as_float(raw[v].x), __uint_as_float(raw[v].y),
+                                           __uint_as_float(raw[v].z), __uint_as_float(raw[v].w));
+              split_h2(f.x * inv, f.y * inv, hi[2 * v], lo[2 * v]);
+              split_h2(f.z * inv, f.w * inv, hi[2 * v + 1], lo[2 * v + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t ws[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = key_pair<DT>(ws[e]);
+                split_h2(f.x * inv, f.y * inv, hi[4 * v + e], lo[4 * v + e]);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            hi[4 * v] = raw[v].x;
+            hi[4 * v + 1] = raw[v].y;
+            hi[4 * v + 2] = raw[v].z;
+            hi[4 * v + 3] = raw[v].w;
+            lo[4 * v] = raw[4 + v].x;
+            lo[4 * v + 1] = raw[4 + v].y;
+            lo[4 * v + 2] = raw[4 + v].z;
+            lo[4 * v + 3] = raw[4 + v].w;
+          }
+        }
+        const uint32_t col = t_lane + s * (2 * kAPartCols);
+        tmem_st16(col, hi);
+        tmem_st16(col + kAPartCols, lo);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_AFULL + s));
+        if (++s == kAStages) {
+          s = 0;
+          aph ^= 1u;
+        }
+#pragma unroll
+        for (int v = 0; v < 8; ++v) raw[v] = nxt[v];
+      }
+    }
+    if (!ok) raise(a.err, abort);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wg = (warp - kEpiWarp0) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    constexpr int half = kSliceCols / 2;  // columns of this warpgroup per job
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(wg * half);
+    __half* rhi = reinterpret_cast<__half*>(scr) + (size_t)row * d;
+    __half* rlo = reinterpret_cast<__half*>(scr) + (size_t)(128 + row) * d;
+    constexpr int NT = K == 1 ? 1 : K == 2 ? 2 : 4;
+    uint32_t cq = 0;
+    bool ok = true;
+    for (int64_t i = 0; ok && i < n_my; ++i) {
+      const int64_t tile = blockIdx.x + i * gridDim.x;
+      const int64_t blk = tile % a.nb;
+      const bool live = blk * kTokensPerBlock + row < a.N;
+      uint8_t* out = a.packed + tile * a.lay.block_bytes;
+      float n = 0.f, rr = 0.f;
+      float nt[L - 1], nc[L];
+      uint32_t nhalf[NT];
+      float nmid = 0.f;
+      for (int job = 0; ok && job < 2 * J; ++job) {
+        const bool e2 = job < J;
+        if (job == 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_NREADY), (uint32_t)i & 1u, abort))) {
+            ok = false;
+            break;
+          }
+          n = s_n[row];
+          // thresholds and centroids in the scale of Y = 2^16 Pi u (exact)
+#pragma unroll
+          for (int t = 0; t < L - 1; ++t) nt[t] = kYScale * a.cp.t[t];
+#pragma unroll
+          for (int t = 0; t < L; ++t) nc[t] = kYScale * a.cp.c[t];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) nhalf[t] = __float_as_uint(-(kYScale * a.px.half[t]));
+          nmid = kYScale * a.px.mid;
+        }
+        // the job's sums: partial accumulators of 128-coordinate K slices,
+        // added here in fp32 with round-to-nearest
+        float yv[half];
+#pragma unroll
+        for (int e = 0; e < half; ++e) yv[e] = 0.f;
+        for (int c = 0; ok && c < S / kSliceStages; ++c, ++cq) {
+          const uint32_t pb = cq & 1u;
+          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_DFULL + pb), (cq >> 1) & 1u, abort))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int g32 = 0; g32 < half / 32; ++g32) {
+            uint32_t v[32];
+            tmem_ld32(t_lane + pb * kSliceCols + 32 * g32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) yv[32 * g32 + e] += __uint_as_float(v[e]);
+          }
+          tc_fence_before();
+          mbar_arrive(bar(BAR_DEMPTY + pb));
+        }
+        if (!ok) break;
+        const int cbase = (job % J) * NC + wg * half;  // first coordinate of this warpgroup's columns
+        uint32_t pl[K + 1][half / 32];
+#pragma unroll
+        for (int g32 = 0; g32 < half / 32; ++g32) {
+          const float* v = yv + 32 * g32;
+          if (e2) {
+            uint32_t w[K];
+#pragma unroll
+            for (int p = 0; p < K; ++p) w[p] = 0;
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 30; e >= 0; e -= 2) {
+              float r2[2];
+#pragma unroll
+              for (int u = 1; u >= 0; --u) {
+                const float y = v[e + u];
+                uint32_t sbit[L - 1];
+                float cv = nc[0];
+#pragma unroll
+                for (int t = 0; t < L - 1; ++t) {
+                  sbit[t] = __float_as_uint(nt[t] - y);
+                  if constexpr (!PX) cv = (int)sbit[t] < 0 ? nc[t + 1] : cv;
+                }
+                uint32_t xb[K];
+#pragma unroll
+                for (int p = 0; p < K; ++p) {
+                  uint32_t x = 0;
+#pragma unroll
+                  for (int t = 0; t < L - 1; ++t)
+                    if (((t + 1) & ((1 << p) - 1)) == 0) x ^= sbit[t];
+                  xb[p] = x;
+                  w[p] = __funnelshift_l(x, w[p], 1);
+                }
+                if constexpr (PX) {
+                  constexpr uint32_t kS = 0x80000000u;
+                  cv = nmid + __uint_as_float(nhalf[0] ^ (xb[0] & kS));
+                  if constexpr (K >= 2) cv += __uint_as_float(nhalf[1] ^ (xb[1] & kS));
+                  if constexpr (K == 3) {
+                    cv += __uint_as_float(nhalf[2] ^ (xb[2] & kS));
+                    cv += __uint_as_float(nhalf[3] ^ ((xb[0] ^ xb[1] ^ xb[2]) & kS));
+                  }
+                }
+                const float rv = y - cv;
+                rr = fmaf(rv, rv, rr);
+                r2[u] = rv * kRScale;
+              }
+              split_h2(r2[0], r2[1], hi[e >> 1], lo[e >> 1]);
+            }
+            uint4* dh = reinterpret_cast<uint4*>(rhi + cbase + 32 * g32);
+            uint4* dl = reinterpret_cast<uint4*>(rlo + cbase + 32 * g32);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              __stcg(dh + t, make_uint4(hi[4 * t], hi[4 * t + 1], hi[4 * t + 2], hi[4 * t + 3]));
+              __stcg(dl + t, make_uint4(lo[4 * t], lo[4 * t + 1], lo[4 * t + 2], lo[4 * t + 3]));
+            }
+#pragma unroll
+            for (int p = 0; p < K; ++p) pl[p][g32] = w[p];
+          } else {
+            uint32_t z = 0;
+#pragma unroll
+            for (int e = 31; e >= 0; --e) z = __funnelshift_l(__float_as_uint(v[e]), z, 1);
+            pl[K][g32] = n > 0.f ? ~z : 0xFFFFFFFFu;
+          }
+        }
+        // this warpgroup's plane words 2 wg, 2 wg + 1 of the job's 128-coordinate chunk
+        const int chunk = cbase / 128, w0 = (cbase % 128) / 32;
+        for (int p = e2 ? 0 : K; p < (e2 ? K : K + 1); ++p) {
+          uint8_t* dst = out + a.lay.plane_off(p, chunk, row) + 4 * w0;
+          *reinterpret_cast<uint2*>(dst) = live ? make_uint2(pl[p][0], pl[p][1]) : make_uint2(0, 0);
+        }
+        if (e2 && job == J - 1) {  // every residual row of the tile written by this thread
+          mbar_arrive(bar(BAR_RREADY));
+        }
+      }
+      if (!ok) break;
+      // rho: the two warpgroups' partial sums
+      s_rr[wg * 128 + row] = rr;
+      mbar_arrive(bar(BAR_RHO));
+      if (wg == 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_RHO), (uint32_t)i & 1u, abort))) {
+          ok = false;
+          break;
+        }
+        const float rho = n * (sqrtf(s_rr[row] + s_rr[128 + row]) * (1.f / kYScale));
+        *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, rho)
+                                                                             : make_float2(0.f, 0.f);
+      }
+    }
+    if (!ok) raise(a.err, abort);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+__global__ void nsmid_kernel(int* out) {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%nsmid;" : "=r"(v));
+  *out = (int)v;
+}
+
+// at least 120 KB, so that no two CTAs of this kernel share an SM (the
+// residual scratch is indexed by the SM)
+size_t enc_wide_smem(int NC) {
+  const size_t need = (size_t)kBStages * 2 * NC * 64 + BAR_COUNT * 8 + 3 * 128 * sizeof(float) + 1024;
+  return need > 120 * 1024 ? need : 120 * 1024;
+}
+
+int enc_wide_nc(int) { return kSliceCols; }
+
+template <int L, int DT, bool PX>
+cudaError_t launch_ew(const tq_plan* p, const EncWideArgs& a, const CUtensorMap& tPi, const CUtensorMap& tM,
+                      cudaStream_t s) {
+  auto kern = encode_wide_kernel<L, DT, PX>;
+  const size_t smem = enc_wide_smem(a.NC);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t grid = a.n_tiles < sms ? a.n_tiles : sms;
+  kern<<<(unsigned)grid, kEThreads, smem, s>>>(tPi, tM, a);
+  return cudaGetLastError();
+}
+
+template <int DT, bool PX>
+cudaError_t launch_ew_l(const tq_plan* p, const EncWideArgs& a, const CUtensorMap& tPi, const CUtensorMap& tM,
+                        cudaStream_t s) {
+  switch (p->cp.L) {
+    case 2: return launch_ew<2, DT, PX>(p, a, tPi, tM, s);
+    case 4: return launch_ew<4, DT, PX>(p, a, tPi, tM, s);
+    case 8: return launch_ew<8, DT, PX>(p, a, tPi, tM, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+bool odd_masks_w(const ParityExpansion& px, int k) {
+  static const uint32_t want[3][4] = {{1u}, {1u, 2u}, {1u, 2u, 4u, 7u}};
+  const int n = k == 3 ? 4 : k;
+  if (k < 1 || k > 3 || px.n != n) return false;
+  for (int i = 0; i < n; ++i)
+    if (px.mask[i] != want[k - 1][i]) return false;
+  return true;
+}
+
+}  // namespace
+
+int query_nsmid() {
+  int* d = nullptr;
+  int v = 0;
+  if (cudaMalloc(&d, sizeof(int)) != cudaSuccess) return 0;
+  nsmid_kernel<<<1, 1>>>(d);
+  if (cudaMemcpy(&v, d, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) v = 0;
+  cudaFree(d);
+  return v;
+}
+
+bool encode_wide_supported(const tq_plan* p, tq_dtype dt) {
+  (void)dt;
+  return p->lay.prod && p->wide_ops && p->wide_scratch && p->d % 128 == 0 && p->cp.L >= 2 && p->cp.L <= 8 &&
+         enc_wide_smem(enc_wide_nc(p->d)) <= 227 * 1024;
+}
+
+cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N,
+                               uint8_t* packed, cudaStream_t s) {
+  if (G * N == 0) return cudaSuccess;
+  const int d = p->d;
+  EncWideArgs a;
+  a.lay = p->lay;
+  a.cp = p->cp;
+  a.px = p->px;
+  a.NC = enc_wide_nc(d);
+  a.J = d / a.NC;
+  a.S = d / kStageK;
+  a.nslots = p->wide_slots;
+  a.G = G;
+  a.N = N;
+  a.nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
+  a.n_tiles = G * a.nb;
+  a.keys = keys;
+  a.packed = packed;
+  a.scratch = p->wide_scratch;
+  a.err = p->err;
+  // B operands: [hi rows; lo rows] of 2^8 Pi and of M (fp16)
+  const size_t dd = (size_t)d * d;
+  const uint16_t* pi = p->wide_ops;
+  const uint16_t* m = p->wide_ops + 2 * dd;
+  CUtensorMap tPi, tM;
+  cudaError_t e = make_tmap_2d(&tPi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pi, (uint64_t)d, 2 * (uint64_t)d,
+                               (uint64_t)d * 2, kStageK, (uint32_t)a.NC, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (e == cudaSuccess)
+    e = make_tmap_2d(&tM, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, m, (uint64_t)d, 2 * (uint64_t)d, (uint64_t)d * 2, kStageK,
+                     (uint32_t)a.NC, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (e != cudaSuccess) return e;
+  const bool px = odd_masks_w(p->px, p->lay.k);
+  if (dt == TQ_F32) return px ? launch_ew_l<0, true>(p, a, tPi, tM, s) : launch_ew_l<0, false>(p, a, tPi, tM, s);
+  if (dt == TQ_F16) return px ? launch_ew_l<1, true>(p, a, tPi, tM, s) : launch_ew_l<1, false>(p, a, tPi, tM, s);
+  return px ? launch_ew_l<2, true>(p, a, tPi, tM, s) : launch_ew_l<2, false>(p, a, tPi, tM, s);
+}
+
+}  // namespace tq

@@ -25,6 +25,8 @@ void free_plan(tq_plan* p) {
     if (b) cudaFree(b);
   if (p->err) cudaFree(p->err);
   if (p->tc_ops) cudaFree(p->tc_ops);
+  if (p->wide_ops) cudaFree(p->wide_ops);
+  if (p->wide_scratch) cudaFree(p->wide_scratch);
   delete p;
 }
 
@@ -60,6 +62,36 @@ void split_images(const float* A, uint8_t* hi, uint8_t* lo) {
       std::memcpy(hi + sw128_offset(n, k), &h, 2);
       std::memcpy(lo + sw128_offset(n, k), &l, 2);
     }
+}
+
+// Row-major fp16 hi + lo splits of 2^8 Pi and of M for the wide tensor-core
+// encode, and its per-SM residual scratch (PROD, any d).  The power of two
+// keeps the lo parts of Pi's entries (|Pi_ij| ~ d^-1/2) out of the fp16
+// subnormal range; M = S Pi^T has entries of order 1.
+cudaError_t build_wide_ops(tq_plan* p) {
+  const size_t dd = (size_t)p->d * p->d;
+  std::vector<float> Pi(dd), M(dd);
+  cudaError_t e = cudaMemcpy(Pi.data(), p->Pi, dd * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(M.data(), p->M, dd * 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  std::vector<uint16_t> host(4 * dd);
+  auto split = [&](float v, size_t hi_at, size_t lo_at) {
+    const __half h = __float2half_rn(v);
+    const __half l = __float2half_rn(v - __half2float(h));
+    std::memcpy(&host[hi_at], &h, 2);
+    std::memcpy(&host[lo_at], &l, 2);
+  };
+  for (size_t i = 0; i < dd; ++i) {
+    split(Pi[i] * 256.f, i, dd + i);
+    split(M[i], 2 * dd + i, 3 * dd + i);
+  }
+  e = cudaMalloc(&p->wide_ops, host.size() * 2);
+  if (e == cudaSuccess) e = cudaMemcpy(p->wide_ops, host.data(), host.size() * 2, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return e;
+  int slots = tq::query_nsmid();
+  if (slots <= 0) return cudaErrorUnknown;
+  p->wide_slots = slots;
+  return cudaMalloc(&p->wide_scratch, (size_t)slots * 2 * 128 * p->d * 2);
 }
 
 // Operand images for the tensor-core encode (d = 128, PROD).
@@ -139,7 +171,9 @@ int tq_score_path(const tq_plan* p, int H) {
 
 int tq_encode_path(const tq_plan* p, tq_dtype dt) {
   if (!p || (dt != TQ_F32 && dt != TQ_F16 && dt != TQ_BF16)) return TQ_EINVAL;
-  return tq::encode_tc_supported(p, dt) ? TQ_PATH_TENSOR_D128 : TQ_PATH_CUDA_CORE;
+  if (tq::encode_tc_supported(p, dt)) return TQ_PATH_TENSOR_D128;
+  if (tq::encode_wide_supported(p, dt)) return TQ_PATH_TENSOR_WIDE;
+  return TQ_PATH_CUDA_CORE;
 }
 
 tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
@@ -229,6 +263,13 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
       return TQ_ECUDA;
     }
   }
+  if (L.prod) {
+    const cudaError_t we = build_wide_ops(p);
+    if (we != cudaSuccess) {
+      free_plan(p);
+      return we == cudaErrorMemoryAllocation ? TQ_ENOMEM : TQ_ECUDA;
+    }
+  }
   *out = p;
   return TQ_OK;
 }
@@ -255,6 +296,8 @@ tq_status tq_encode(const tq_plan* p, const void* keys, tq_dtype dtype, int64_t 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (encode_tc_supported(p, dtype))
     return from_cuda(launch_encode_tc(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
+  if (encode_wide_supported(p, dtype))
+    return from_cuda(launch_encode_wide(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
   return from_cuda(launch_encode_simt(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
 }
 

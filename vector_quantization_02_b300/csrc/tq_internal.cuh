@@ -69,6 +69,9 @@ struct tq_plan {
   float* ST;          // [d][d] = S^T (PROD)
   float* M;           // [d][d] = S Pi^T (PROD)
   float* MT;          // [d][d] = M^T (PROD)
+  uint16_t* wide_ops;  // (PROD) row-major fp16 [4][d][d]: (2^8 Pi) hi, lo; M hi, lo
+  void* wide_scratch;  // (PROD) residual rows of the wide encode: [wide_slots][2][128][d] bf16
+  int wide_slots;      // SM ids of the device (%nsmid)
   uint8_t* tc_ops;    // tensor-core operand images (d = 128, PROD): Pi hi/lo fp16,
                       // Pi hi/lo bf16, M hi/lo bf16; 32 KB each, K-major 128-byte swizzle
   int* err;           // device error word
@@ -101,6 +104,10 @@ size_t score_tc_workspace_bytes(const tq_plan* p, int64_t G, int H);
 cudaError_t launch_score_tc(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed,
                             int64_t N, float* logits, void* ws, cudaStream_t s);
 
+bool encode_wide_supported(const tq_plan* p, tq_dtype dt);
+cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N,
+                               uint8_t* packed, cudaStream_t s);
+int query_nsmid();
 bool score_wide_supported(const tq_plan* p, int H);
 size_t score_wide_workspace_bytes(const tq_plan* p, int64_t G, int H);
 cudaError_t launch_score_wide(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed,
