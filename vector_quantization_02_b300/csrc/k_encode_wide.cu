@@ -18,8 +18,9 @@
 // 2^16 t; the residual enters E5 as 2^10 r'.  Signs do not see the scales.
 //
 // A tile is 128 keys (one packed block).  Its work is a sequence of jobs,
-// each one fp32 accumulator of 128 keys x NC coordinates (NC = 256, or 128
-// when d is not a multiple of 256) over K = d in stages of 32 coordinates:
+// each 128 keys x 128 coordinates over K = d in stages of 32 coordinates,
+// accumulated in TMEM per 128-coordinate slice of K and summed in fp32 by the
+// epilogue (one tensor-core accumulator over K = 1536 loses too much):
 //   d / NC E2 jobs  Y[:, chunk] = X Pi[chunk]^T, then quantised: code bits
 //                   into the packed block, the residual's split into a
 //                   per-SM scratch row (rows of this SM's CTA only),
@@ -27,14 +28,19 @@
 // The scratch belongs to the SM: this kernel needs a whole SM (all 512 TMEM
 // columns, more than half of the shared memory), so no two of its CTAs, from
 // any launch, share one at a time.
-//  warp 0       producer: TMA loads of the B operand (hi and lo rows of Pi or
-//               M for the job's chunk, 64-byte swizzle) into a 4-stage ring.
-//  warp 1       TMEM owner (accumulator in [0, NC), key-operand ring in
-//               [256, 512)) and MMA issuer (one thread).
-//  warps 2-5    A operand: thread (warp w, lane l) owns key row 32 (w % 4) + l;
-//               per tile it first sums ||x||^2 over the row (compensated), then
-//               writes its 32 coordinates per stage into TMEM (8-stage ring):
-//               the scaled unit key for E2, the residual for E5.
+// ||x|| comes from a pre-pass (key_norm_kernel) that writes it into the packed
+// block's norm slot.
+//  warp 0       producer: TMA loads into a 6-stage shared-memory ring; a stage
+//               holds the B operand (hi and lo rows of 2^8 Pi or M for the
+//               job's 128 columns, 32 coordinates, 64-byte swizzle) and the A
+//               source: the key tile (E2) or the residual tile from the scratch
+//               (E5, read by the MMA straight from shared memory).
+//  warp 1       TMEM owner (two partial accumulators in [0, 256), the E2 key
+//               operand ring in [256, 512)) and MMA issuer (one thread).
+//  warps 2-5    E2 key operand: thread (warp w, lane l) owns key row
+//               32 (w % 4) + l; per stage it reads its 32 coordinates from the
+//               staged key tile and writes u = 2^8 x / ||x|| as fp16 hi, lo into
+//               TMEM (8-stage ring).
 //  warps 6-13   epilogue: two warpgroups, each taking half of a job's columns.
 // Every wait is bounded: on expiry the kernel raises the plan's error word,
 // drains what it issued and frees its TMEM.
@@ -51,8 +57,10 @@ using namespace ptx;
 
 constexpr int kEThreads = 448;
 constexpr int kEpiWarp0 = 6;       // warps 2-5 load the A operand
-constexpr int kBStages = 4;
-constexpr int kAStages = 8;
+constexpr int kStages = 6;         // shared-memory ring (B operand + A source)
+constexpr int kAStages = 8;        // TMEM ring of the E2 key operand
+constexpr uint32_t kPartBytes = 128 * 64;  // 128 rows x 32 16-bit values
+constexpr uint32_t kStageBytes = 4 * kPartBytes;  // B hi, B lo, A source (16 KB)
 constexpr int kStageK = 32;        // coordinates per stage
 constexpr int kARing = 256;        // first TMEM column of the A ring
 constexpr int kAPartCols = 16;     // TMEM columns of one A part per stage (32 16-bit values)
@@ -60,14 +68,14 @@ constexpr int kSliceCols = 128;    // output columns of a job (two partial accum
 constexpr int kSliceStages = 4;    // stages (128 coordinates of K) per partial accumulator
 
 enum {
-  BAR_BFULL = 0,
-  BAR_BEMPTY = BAR_BFULL + kBStages,
-  BAR_AFULL = BAR_BEMPTY + kBStages,
+  BAR_FULL = 0,                       // B operand (and, for E5 stages, the residual tile) landed
+  BAR_XFULL = BAR_FULL + kStages,     // key tile of an E2 stage landed (only E2 fills advance it)
+  BAR_EMPTY = BAR_XFULL + kStages,
+  BAR_AFULL = BAR_EMPTY + kStages,
   BAR_AEMPTY = BAR_AFULL + kAStages,
   BAR_DFULL = BAR_AEMPTY + kAStages,   // [2] partial accumulators
   BAR_DEMPTY = BAR_DFULL + 2,
-  BAR_NREADY = BAR_DEMPTY + 2,
-  BAR_RREADY = BAR_NREADY + 1,
+  BAR_RREADY = BAR_DEMPTY + 2,
   BAR_RHO = BAR_RREADY + 1,
   BAR_DONE = BAR_RHO + 1,
   BAR_COUNT = BAR_DONE + 1
@@ -111,7 +119,6 @@ struct KSum {
     c += fabsf(s) >= fabsf(v) ? (s - t) + v : (v - t) + s;
     s = t;
   }
-  __device__ __forceinline__ float value() const { return s + c; }
 };
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -139,17 +146,15 @@ constexpr float kRScale = 1.f / 64.f;   // E5 operand 2^10 r' = 2^-6 (2^16 r')
 template <int L, int DT, bool PX>
 __global__ void __launch_bounds__(kEThreads, 1)
 encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_constant__ CUtensorMap tmM,
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR,
                    const EncWideArgs a) {
   constexpr int K = L == 2 ? 1 : L == 4 ? 2 : 3;  // code planes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
   const int d = a.lay.d, NC = a.NC, J = a.J, S = a.S;
-  const uint32_t part_bytes = (uint32_t)NC * 64u;  // NC rows x 32 16-bit values
-  const uint32_t stage_bytes = 2 * part_bytes;
-  const uint32_t off_bar = kBStages * stage_bytes;
-  float* s_n = reinterpret_cast<float*>(smem + off_bar + BAR_COUNT * 8);  // [128]
-  float* s_rr = s_n + 128;                                                 // [2][128]
+  const uint32_t off_bar = kStages * kStageBytes;
+  float* s_rr = reinterpret_cast<float*>(smem + off_bar + BAR_COUNT * 8);  // [2][128]
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ uint32_t s_slot;
@@ -159,9 +164,10 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
   if (threadIdx.x == 0) {
     abort_flag = 0;
     s_slot = smid();
-    for (int s = 0; s < kBStages; ++s) {
-      mbar_init(bar(BAR_BFULL + s), 1);
-      mbar_init(bar(BAR_BEMPTY + s), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(BAR_FULL + s), 1);
+      mbar_init(bar(BAR_XFULL + s), 1);
+      mbar_init(bar(BAR_EMPTY + s), 1);
     }
     for (int s = 0; s < kAStages; ++s) {
       mbar_init(bar(BAR_AFULL + s), 128);
@@ -171,7 +177,6 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       mbar_init(bar(BAR_DFULL + b), 1);
       mbar_init(bar(BAR_DEMPTY + b), 256);
     }
-    mbar_init(bar(BAR_NREADY), 128);
     mbar_init(bar(BAR_RREADY), 256);
     mbar_init(bar(BAR_RHO), 256);
     mbar_init(bar(BAR_DONE), 1);
@@ -201,22 +206,48 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
     if (lane == 0) {
       prefetch_tmap(&tmPi);
       prefetch_tmap(&tmM);
+      prefetch_tmap(&tmX);
+      prefetch_tmap(&tmR);
+      constexpr uint32_t kXBytes = DT == 0 ? 2 * kPartBytes : kPartBytes;  // key tile: 128 rows x 32 values
       uint32_t b = 0, ph = 0, issued = 0;
+      uint32_t xmask = 0, last_e2 = 0;  // per slot: parity of its next E2 fill; last fill was E2
       bool ok = true;
       for (int64_t i = 0; ok && i < n_my; ++i) {
+        const int64_t tile = blockIdx.x + i * gridDim.x;
+        const int64_t g = tile / a.nb, blk = tile - g * a.nb;
+        const int32_t xrow0 = (int32_t)(g * a.N + blk * kTokensPerBlock);
         for (int job = 0; ok && job < 2 * J; ++job) {
-          const CUtensorMap* map = job < J ? &tmPi : &tmM;
-          const int row0 = (job % J) * NC;
-          for (int st = 0; st < S; ++st) {
-            if (!mbar_wait_suspend(bar(BAR_BEMPTY + b), ph ^ 1u, abort)) {
+          const bool e2 = job < J;
+          if (job == J) {  // the residual rows of this tile are in the scratch
+            if (!mbar_wait_suspend(bar(BAR_RREADY), (uint32_t)i & 1u, abort)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(bar(BAR_BFULL + b), stage_bytes);
-            tma_load_2d(sb + b * stage_bytes, map, st * kStageK, row0, bar(BAR_BFULL + b));
-            tma_load_2d(sb + b * stage_bytes + part_bytes, map, st * kStageK, d + row0, bar(BAR_BFULL + b));
+          }
+          const CUtensorMap* map = e2 ? &tmPi : &tmM;
+          const int row0 = (job % J) * NC;
+          for (int st = 0; st < S; ++st) {
+            if (!mbar_wait_suspend(bar(BAR_EMPTY + b), ph ^ 1u, abort)) {
+              ok = false;
+              break;
+            }
+            const uint32_t base = sb + b * kStageBytes;
+            mbar_arrive_expect_tx(bar(BAR_FULL + b), e2 ? 2 * kPartBytes : 4 * kPartBytes);
+            tma_load_2d(base, map, st * kStageK, row0, bar(BAR_FULL + b));
+            tma_load_2d(base + kPartBytes, map, st * kStageK, d + row0, bar(BAR_FULL + b));
+            if (e2) {
+              mbar_arrive_expect_tx(bar(BAR_XFULL + b), kXBytes);
+              tma_load_2d(base + 2 * kPartBytes, &tmX, st * kStageK, xrow0, bar(BAR_XFULL + b));
+              xmask ^= 1u << b;
+              last_e2 |= 1u << b;
+            } else {
+              last_e2 &= ~(1u << b);
+              tma_load_2d(base + 2 * kPartBytes, &tmR, st * kStageK, (int32_t)(s_slot * 256), bar(BAR_FULL + b));
+              tma_load_2d(base + 3 * kPartBytes, &tmR, st * kStageK, (int32_t)(s_slot * 256 + 128),
+                          bar(BAR_FULL + b));
+            }
             ++issued;
-            if (++b == kBStages) {
+            if (++b == kStages) {
               b = 0;
               ph ^= 1u;
             }
@@ -224,11 +255,13 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
         }
       }
       if (!ok) raise(a.err, abort);
+      // no copy may still be landing when the CTA exits
       int dummy = 0;
-      for (uint32_t k = 0; k < (issued < kBStages ? issued : kBStages); ++k) {
-        b = b == 0 ? kBStages - 1 : b - 1;
-        if (b == kBStages - 1) ph ^= 1u;
-        mbar_wait(bar(BAR_BFULL + b), ph, &dummy);
+      for (uint32_t k = 0; k < (issued < kStages ? issued : kStages); ++k) {
+        b = b == 0 ? kStages - 1 : b - 1;
+        if (b == kStages - 1) ph ^= 1u;
+        mbar_wait(bar(BAR_FULL + b), ph, &dummy);
+        if ((last_e2 >> b) & 1u) mbar_wait(bar(BAR_XFULL + b), ((xmask >> b) & 1u) ^ 1u, &dummy);
       }
     }
   } else if (warp == 1) {
@@ -239,6 +272,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       bool ok = true;
       for (int64_t i = 0; ok && i < n_my; ++i) {
         for (int job = 0; ok && job < 2 * J; ++job) {
+          const bool e2 = job < J;
           // K in slices of 128 coordinates, each into a fresh partial accumulator
           for (int c = 0; ok && c < S / kSliceStages; ++c, ++cq) {
             const uint32_t pb = cq & 1u, d_acc = tmem + pb * kSliceCols;
@@ -247,32 +281,42 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
               break;
             }
             for (int st = 0; st < kSliceStages; ++st) {
-              if (!mbar_wait_suspend(bar(BAR_BFULL + b), bph, abort) ||
-                  !mbar_wait_suspend(bar(BAR_AFULL + s), aph, abort)) {
+              if (!mbar_wait_suspend(bar(BAR_FULL + b), bph, abort) ||
+                  (e2 && !mbar_wait_suspend(bar(BAR_AFULL + s), aph, abort))) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint32_t bq = sb + b * stage_bytes;
+              const uint32_t bq = sb + b * kStageBytes;
               const uint32_t at = tmem + kARing + s * (2 * kAPartCols);
 #pragma unroll
               for (int ks = 0; ks < 2; ++ks) {
-                const uint64_t b_hi = sdesc_k_sw64(bq) + 2u * ks, b_lo = sdesc_k_sw64(bq + part_bytes) + 2u * ks;
-                const uint32_t a_hi = at + 8 * ks, a_lo = at + kAPartCols + 8 * ks;
+                const uint64_t b_hi = sdesc_k_sw64(bq) + 2u * ks, b_lo = sdesc_k_sw64(bq + kPartBytes) + 2u * ks;
                 const uint32_t acc = (st == 0 && ks == 0) ? 0u : 1u;
-                mma_f16_ts(d_acc, a_hi, b_hi, idesc, acc);
-                mma_f16_ts(d_acc, a_hi, b_lo, idesc, 1u);
-                mma_f16_ts(d_acc, a_lo, b_hi, idesc, 1u);
+                if (e2) {
+                  const uint32_t a_hi = at + 8 * ks, a_lo = at + kAPartCols + 8 * ks;
+                  mma_f16_ts(d_acc, a_hi, b_hi, idesc, acc);
+                  mma_f16_ts(d_acc, a_hi, b_lo, idesc, 1u);
+                  mma_f16_ts(d_acc, a_lo, b_hi, idesc, 1u);
+                } else {
+                  const uint64_t r_hi = sdesc_k_sw64(bq + 2 * kPartBytes) + 2u * ks;
+                  const uint64_t r_lo = sdesc_k_sw64(bq + 3 * kPartBytes) + 2u * ks;
+                  mma_f16_ss(d_acc, r_hi, b_hi, idesc, acc);
+                  mma_f16_ss(d_acc, r_hi, b_lo, idesc, 1u);
+                  mma_f16_ss(d_acc, r_lo, b_hi, idesc, 1u);
+                }
               }
-              mma_commit(bar(BAR_BEMPTY + b));
-              mma_commit(bar(BAR_AEMPTY + s));
-              if (++b == kBStages) {
+              mma_commit(bar(BAR_EMPTY + b));
+              if (++b == kStages) {
                 b = 0;
                 bph ^= 1u;
               }
-              if (++s == kAStages) {
-                s = 0;
-                aph ^= 1u;
+              if (e2) {
+                mma_commit(bar(BAR_AEMPTY + s));
+                if (++s == kAStages) {
+                  s = 0;
+                  aph ^= 1u;
+                }
               }
             }
             if (!ok) break;
@@ -286,126 +330,48 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       mbar_wait(bar(BAR_DONE), 0, &dummy);
     }
   } else if (warp < kEpiWarp0) {
-    // ------------------------------------------------------------ A operand
+    // ------------------------------------------------------------ E2 key operand
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + kARing;
-    const __half* rhi = reinterpret_cast<const __half*>(scr) + (size_t)row * d;
-    const __half* rlo = reinterpret_cast<const __half*>(scr) + (size_t)(128 + row) * d;
-    uint32_t s = 0, aph = 0;
+    uint32_t b = 0, xmask = 0, s = 0, aph = 0;  // ring slot, per-slot parity of its next E2 fill
     bool ok = true;
     for (int64_t i = 0; ok && i < n_my; ++i) {
       const int64_t tile = blockIdx.x + i * gridDim.x;
-      const int64_t g = tile / a.nb, blk = tile - g * a.nb;
-      const int64_t tok = blk * kTokensPerBlock + row;
-      const bool live = tok < a.N;
-      const char* xrow = static_cast<const char*>(a.keys) + (g * a.N + (live ? tok : 0)) * (int64_t)d * (DT == 0 ? 4 : 2);
-      // stage t of the tile: job t / S, coordinates 32 (t % S) ..; its raw
-      // 16-byte words are loaded one stage ahead of their conversion
-      const int T = 2 * J * S;
-      auto fetch = [&](int t, uint4 (&r)[8]) {
-        const int c0 = (t % S) * kStageK;
-        if (t < J * S) {
-          if constexpr (DT == 0) {
-            const uint4* src = reinterpret_cast<const uint4*>(xrow) + c0 / 4;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) r[v] = live ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-          } else {
-            const uint4* src = reinterpret_cast<const uint4*>(xrow) + c0 / 8;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) r[v] = live ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-          }
-        } else {
-          const uint4* sh = reinterpret_cast<const uint4*>(rhi + c0);
-          const uint4* sl = reinterpret_cast<const uint4*>(rlo + c0);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            r[v] = __ldcg(sh + v);
-            r[4 + v] = __ldcg(sl + v);
-          }
-        }
-      };
-      uint4 raw[8], nxt[8];
-      fetch(0, raw);
-      // ||x|| over the whole row (eight 16-byte loads in flight), then u = 2^8 x / ||x||
-      KSum n2;
-      if (live) {
-        const uint4* src = reinterpret_cast<const uint4*>(xrow);
-        const int nv = d * (DT == 0 ? 4 : 2) / 16;
-        for (int v0 = 0; v0 < nv; v0 += 8) {
-          uint4 w[8];
-#pragma unroll
-          for (int v = 0; v < 8; ++v) w[v] = __ldg(src + v0 + v);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
-            if constexpr (DT == 0) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) n2.add(__uint_as_float(ws[e]));
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = key_pair<DT>(ws[e]);
-                n2.add(f.x);
-                n2.add(f.y);
-              }
-            }
-          }
-        }
-      }
-      const float n = sqrtf(n2.value());
+      // ||x|| from the pre-pass (0 for padded rows, whose staged rows may hold
+      // another group's keys)
+      const float n = *reinterpret_cast<const float*>(a.packed + tile * a.lay.block_bytes + a.lay.norms_off + row * 8);
       const float inv = n > 0.f ? 256.f / n : 0.f;
-      s_n[row] = n;
-      mbar_arrive(bar(BAR_NREADY));
-      for (int t = 0; ok && t < T; ++t) {
-        if (t == J * S) {
-          // the residual rows of this tile are in the scratch once the epilogue
-          // has quantised the last E2 job, which needs every E2 stage delivered:
-          // no prefetch crosses this point
-          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_RREADY), (uint32_t)i & 1u, abort))) {
-            ok = false;
-            break;
-          }
-          fetch(t, raw);
-        }
-        if (t + 1 < T && t + 1 != J * S) fetch(t + 1, nxt);
-        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_AEMPTY + s), aph ^ 1u, abort))) {
+      for (int t = 0; ok && t < J * S; ++t) {
+        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_XFULL + b), (xmask >> b) & 1u, abort)) ||
+            !__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_AEMPTY + s), aph ^ 1u, abort))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint8_t* xs = smem + b * kStageBytes + 2 * kPartBytes;
         uint32_t hi[16], lo[16];
-        if (t < J * S) {
-          if constexpr (DT == 0) {
+        if constexpr (DT == 0) {
+          // 128-byte rows, 16-byte chunk c at position c ^ (row % 8)
+          const uint8_t* xr = xs + row * 128;
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 f = make_float4(__uint_as_float(raw[v].x), __uint_as_float(raw[v].y),
-                                           __uint_as_float(raw[v].z), __uint_as_float(raw[v].w));
-              split_h2(f.x * inv, f.y * inv, hi[2 * v], lo[2 * v]);
-              split_h2(f.z * inv, f.w * inv, hi[2 * v + 1], lo[2 * v + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint32_t ws[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = key_pair<DT>(ws[e]);
-                split_h2(f.x * inv, f.y * inv, hi[4 * v + e], lo[4 * v + e]);
-              }
-            }
+          for (int c = 0; c < 8; ++c) {
+            const float4 f = *reinterpret_cast<const float4*>(xr + ((c ^ (row & 7)) << 4));
+            split_h2(f.x * inv, f.y * inv, hi[2 * c], lo[2 * c]);
+            split_h2(f.z * inv, f.w * inv, hi[2 * c + 1], lo[2 * c + 1]);
           }
         } else {
+          // 64-byte rows, 16-byte chunk c at position c ^ ((row / 2) % 4)
+          const uint8_t* xr = xs + row * 64;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            hi[4 * v] = raw[v].x;
-            hi[4 * v + 1] = raw[v].y;
-            hi[4 * v + 2] = raw[v].z;
-            hi[4 * v + 3] = raw[v].w;
-            lo[4 * v] = raw[4 + v].x;
-            lo[4 * v + 1] = raw[4 + v].y;
-            lo[4 * v + 2] = raw[4 + v].z;
-            lo[4 * v + 3] = raw[4 + v].w;
+          for (int c = 0; c < 4; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4*>(xr + ((c ^ ((row >> 1) & 3)) << 4));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = key_pair<DT>(ws[e]);
+              split_h2(f.x * inv, f.y * inv, hi[4 * c + e], lo[4 * c + e]);
+            }
           }
         }
         const uint32_t col = t_lane + s * (2 * kAPartCols);
@@ -418,9 +384,11 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
           s = 0;
           aph ^= 1u;
         }
-#pragma unroll
-        for (int v = 0; v < 8; ++v) raw[v] = nxt[v];
+        xmask ^= 1u << b;
+        if (++b == kStages) b = 0;
       }
+      // the tile's E5 stages pass through the ring without this role
+      b = (uint32_t)((b + (uint32_t)(J * S)) % kStages);
     }
     if (!ok) raise(a.err, abort);
   } else {
@@ -447,11 +415,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       for (int job = 0; ok && job < 2 * J; ++job) {
         const bool e2 = job < J;
         if (job == 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_NREADY), (uint32_t)i & 1u, abort))) {
-            ok = false;
-            break;
-          }
-          n = s_n[row];
+          n = *reinterpret_cast<const float*>(out + a.lay.norms_off + row * 8);
           // thresholds and centroids in the scale of Y = 2^16 Pi u (exact)
 #pragma unroll
           for (int t = 0; t < L - 1; ++t) nt[t] = kYScale * a.cp.t[t];
@@ -555,7 +519,10 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
           uint8_t* dst = out + a.lay.plane_off(p, chunk, row) + 4 * w0;
           *reinterpret_cast<uint2*>(dst) = live ? make_uint2(pl[p][0], pl[p][1]) : make_uint2(0, 0);
         }
-        if (e2 && job == J - 1) {  // every residual row of the tile written by this thread
+        if (e2 && job == J - 1) {
+          // every residual row of the tile written by this thread, made
+          // visible to the TMA loads (async proxy) that read them
+          asm volatile("fence.proxy.async.global;" ::: "memory");
           mbar_arrive(bar(BAR_RREADY));
         }
       }
@@ -590,35 +557,88 @@ __global__ void nsmid_kernel(int* out) {
 
 // at least 120 KB, so that no two CTAs of this kernel share an SM (the
 // residual scratch is indexed by the SM)
-size_t enc_wide_smem(int NC) {
-  const size_t need = (size_t)kBStages * 2 * NC * 64 + BAR_COUNT * 8 + 3 * 128 * sizeof(float) + 1024;
+size_t enc_wide_smem(int) {
+  const size_t need = (size_t)kStages * kStageBytes + BAR_COUNT * 8 + 2 * 128 * sizeof(float) + 1024;
   return need > 120 * 1024 ? need : 120 * 1024;
+}
+
+// ||x|| of every row of every 128-token block (0 for padded rows) into the
+// packed block's norm slot: one warp per row, compensated sums per lane,
+// combined across lanes with error-free additions.
+template <int DT>
+__global__ void key_norm_kernel(const void* __restrict__ keys, int64_t N, int d, int64_t nb, int64_t rows,
+                                Layout lay, uint8_t* __restrict__ packed) {
+  constexpr int kEsize = DT == 0 ? 4 : 2;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nwarps) {
+    const int64_t gb = r >> 7, g = gb / nb;
+    const int t = (int)(r & 127);
+    const int64_t tok = (gb - g * nb) * kTokensPerBlock + t;
+    float n = 0.f;
+    if (tok < N) {
+      KSum acc;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(keys) + (g * N + tok) * (int64_t)d * kEsize);
+      for (int v = lane; v < d * kEsize / 16; v += 32) {
+        const uint4 w = __ldg(src + v);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if constexpr (DT == 0) {
+            acc.add(__uint_as_float(ws[e]));
+          } else {
+            const float2 f = key_pair<DT>(ws[e]);
+            acc.add(f.x);
+            acc.add(f.y);
+          }
+        }
+      }
+      float sum = acc.s, comp = acc.c;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o), c2 = __shfl_xor_sync(0xffffffffu, comp, o);
+        const float tt = sum + s2;
+        comp += c2 + (fabsf(sum) >= fabsf(s2) ? (sum - tt) + s2 : (s2 - tt) + sum);
+        sum = tt;
+      }
+      n = sqrtf(sum + comp);
+    }
+    if (lane == 0) *reinterpret_cast<float*>(packed + gb * lay.block_bytes + lay.norms_off + t * 8) = n;
+  }
 }
 
 int enc_wide_nc(int) { return kSliceCols; }
 
+struct EncMaps {
+  CUtensorMap pi, m, x, r;
+};
+
 template <int L, int DT, bool PX>
-cudaError_t launch_ew(const tq_plan* p, const EncWideArgs& a, const CUtensorMap& tPi, const CUtensorMap& tM,
-                      cudaStream_t s) {
-  auto kern = encode_wide_kernel<L, DT, PX>;
-  const size_t smem = enc_wide_smem(a.NC);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_ew(const tq_plan* p, const EncWideArgs& a, const EncMaps& mp, cudaStream_t s) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t rows = a.n_tiles * kTokensPerBlock;
+  const int64_t nblk = (rows + 7) / 8;
+  key_norm_kernel<DT><<<(unsigned)(nblk < 8 * sms ? nblk : 8 * sms), 256, 0, s>>>(a.keys, a.N, a.lay.d, a.nb, rows,
+                                                                                    a.lay, a.packed);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto kern = encode_wide_kernel<L, DT, PX>;
+  const size_t smem = enc_wide_smem(a.NC);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   const int64_t grid = a.n_tiles < sms ? a.n_tiles : sms;
-  kern<<<(unsigned)grid, kEThreads, smem, s>>>(tPi, tM, a);
+  kern<<<(unsigned)grid, kEThreads, smem, s>>>(mp.pi, mp.m, mp.x, mp.r, a);
   return cudaGetLastError();
 }
 
 template <int DT, bool PX>
-cudaError_t launch_ew_l(const tq_plan* p, const EncWideArgs& a, const CUtensorMap& tPi, const CUtensorMap& tM,
-                        cudaStream_t s) {
+cudaError_t launch_ew_l(const tq_plan* p, const EncWideArgs& a, const EncMaps& mp, cudaStream_t s) {
   switch (p->cp.L) {
-    case 2: return launch_ew<2, DT, PX>(p, a, tPi, tM, s);
-    case 4: return launch_ew<4, DT, PX>(p, a, tPi, tM, s);
-    case 8: return launch_ew<8, DT, PX>(p, a, tPi, tM, s);
+    case 2: return launch_ew<2, DT, PX>(p, a, mp, s);
+    case 4: return launch_ew<4, DT, PX>(p, a, mp, s);
+    case 8: return launch_ew<8, DT, PX>(p, a, mp, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -674,17 +694,32 @@ cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, 
   const size_t dd = (size_t)d * d;
   const uint16_t* pi = p->wide_ops;
   const uint16_t* m = p->wide_ops + 2 * dd;
-  CUtensorMap tPi, tM;
-  cudaError_t e = make_tmap_2d(&tPi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pi, (uint64_t)d, 2 * (uint64_t)d,
-                               (uint64_t)d * 2, kStageK, (uint32_t)a.NC, CU_TENSOR_MAP_SWIZZLE_64B);
+  EncMaps mp;
+  const uint32_t nc = (uint32_t)a.NC;
+  cudaError_t e = make_tmap_2d(&mp.pi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pi, (uint64_t)d, 2 * (uint64_t)d,
+                               (uint64_t)d * 2, kStageK, nc, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e == cudaSuccess)
-    e = make_tmap_2d(&tM, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, m, (uint64_t)d, 2 * (uint64_t)d, (uint64_t)d * 2, kStageK,
-                     (uint32_t)a.NC, CU_TENSOR_MAP_SWIZZLE_64B);
+    e = make_tmap_2d(&mp.m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, m, (uint64_t)d, 2 * (uint64_t)d, (uint64_t)d * 2, kStageK,
+                     nc, CU_TENSOR_MAP_SWIZZLE_64B);
+  // key tiles: 128 rows x 32 values (rows past G N read as zero)
+  if (e == cudaSuccess) {
+    const CUtensorMapDataType xt = dt == TQ_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dt == TQ_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t es = dt == TQ_F32 ? 4 : 2;
+    e = make_tmap_2d(&mp.x, xt, keys, (uint64_t)d, (uint64_t)(G * N), (uint64_t)d * es, kStageK, kTokensPerBlock,
+                     dt == TQ_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  }
+  // residual rows of the per-SM scratch: [slot][hi, lo][128][d] fp16
+  if (e == cudaSuccess)
+    e = make_tmap_2d(&mp.r, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p->wide_scratch, (uint64_t)d,
+                     (uint64_t)p->wide_slots * 256, (uint64_t)d * 2, kStageK, kTokensPerBlock,
+                     CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
   const bool px = odd_masks_w(p->px, p->lay.k);
-  if (dt == TQ_F32) return px ? launch_ew_l<0, true>(p, a, tPi, tM, s) : launch_ew_l<0, false>(p, a, tPi, tM, s);
-  if (dt == TQ_F16) return px ? launch_ew_l<1, true>(p, a, tPi, tM, s) : launch_ew_l<1, false>(p, a, tPi, tM, s);
-  return px ? launch_ew_l<2, true>(p, a, tPi, tM, s) : launch_ew_l<2, false>(p, a, tPi, tM, s);
+  if (dt == TQ_F32) return px ? launch_ew_l<0, true>(p, a, mp, s) : launch_ew_l<0, false>(p, a, mp, s);
+  if (dt == TQ_F16) return px ? launch_ew_l<1, true>(p, a, mp, s) : launch_ew_l<1, false>(p, a, mp, s);
+  return px ? launch_ew_l<2, true>(p, a, mp, s) : launch_ew_l<2, false>(p, a, mp, s);
 }
 
 }  // namespace tq

@@ -296,7 +296,7 @@ tq_status tq_encode(const tq_plan* p, const void* keys, tq_dtype dtype, int64_t 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (encode_tc_supported(p, dtype))
     return from_cuda(launch_encode_tc(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
-  if (encode_wide_supported(p, dtype))
+  if (encode_wide_supported(p, dtype) && G * N < (int64_t)INT32_MAX - 2 * kTokensPerBlock)  // TMA row coordinates
     return from_cuda(launch_encode_wide(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
   return from_cuda(launch_encode_simt(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
 }
