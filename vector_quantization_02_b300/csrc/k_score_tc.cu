@@ -299,6 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
       uint32_t epoch = 0, issued = 0;
       bool ok = true, have_img = false;
       const uint8_t* src = a.packed + t_begin * a.lay.block_bytes;
+      // the first ring's worth of packed blocks does not depend on the query
+      // preparation: it streams while that kernel still runs (programmatic
+      // dependent launch); the query images wait for it to complete
+      const uint32_t pre = n_my < (uint32_t)kStages ? n_my : (uint32_t)kStages;
+      for (uint32_t i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(bar(BAR_FULL + i), blk_bytes);
+        bulk_load(sb + off_ring + i * blk_bytes, src + (int64_t)i * blk_bytes, blk_bytes, bar(BAR_FULL + i));
+      }
+      issued = pre;
+      grid_dependency_wait();
       for (uint32_t i = 0; i < n_my; ++i, src += blk_bytes) {
         if (i > 0) {
           const uint32_t g0 = pos.g;
@@ -315,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
           bulk_load(sb + b * a.img_bytes, a.images + (int64_t)pos.g * a.img_bytes, a.img_bytes, bar(BAR_BFULL + b));
           have_img = true;
         }
+        if (i < pre) continue;  // issued above
         const uint32_t s = i & kStageMask;
         if (!mbar_wait_suspend(bar(BAR_EMPTY + s), ((i / kStages) & 1u) ^ 1u, abort)) {
           ok = false;
@@ -439,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    grid_dependency_wait();  // the per-head constants come from the query preparation
     const uint32_t eg = (uint32_t)(warp - kEpiWarp0) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
@@ -524,6 +536,7 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
                      const float* __restrict__ PiT, const float* __restrict__ ST, uint32_t img_bytes,
                      uint8_t* __restrict__ images, float4* __restrict__ consts, int* err) {
   constexpr int d = 128;
+  grid_dependents_launch();  // the score kernel may start streaming packed blocks now
   extern __shared__ float prep_sm[];
   float* sPi = prep_sm;                 // [d][d] Pi^T
   float* sS = prep_sm + d * d;          // [d][d] S^T
@@ -701,8 +714,20 @@ cudaError_t launch_kernel(const ScoreTcArgs& a, const TcGeom& gm, int64_t grid, 
   auto kern = score_tc_kernel<HP, K, PROD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gm.smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, kThreads, gm.smem, s>>>(a);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs may start while the query
+  // preparation runs; the roles that read its output wait for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = gm.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int HP>

@@ -79,6 +79,16 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Lets the next kernel on the stream (launched with programmatic stream
+// serialisation) begin before this grid completes.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their memory
+// is visible (returns at once when there are none).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
                                             uint32_t bar) {
