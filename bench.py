@@ -17,6 +17,7 @@ data path.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -211,9 +212,16 @@ def _e2e(args, world, plan, keys, q, packed, logits, ws, flush, top_k, stream, e
     return e2e_ms
 
 
+def workload(args):
+    w = tq_synth.WORKLOADS[args.workload]
+    if args.tokens:  # a reduced case of the same shape (profiling), never a bench value
+        w = dataclasses.replace(w, N=min(args.tokens, w.N))
+    return w
+
+
 def run_ours(args, world, rank):
     import vector_quantization_02_b300 as tq
-    w = tq_synth.WORKLOADS[args.workload]
+    w = workload(args)
     bits = args.bits or w.bits[0]
     dev = torch.device("cuda", torch.cuda.current_device())
     G, N, H, d = w.G, w.N, w.H, w.d
@@ -404,7 +412,7 @@ def run_ours(args, world, rank):
 
 
 def run_reference(args, world, rank):
-    w = tq_synth.WORKLOADS[args.workload]
+    w = workload(args)
     bits = args.bits or w.bits[0]
     if rank != 0:
         return None
@@ -432,6 +440,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen25_3b_decode", choices=sorted(tq_synth.WORKLOADS))
     ap.add_argument("--bits", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="cap the tokens per group (a reduced case for profiling; not a bench configuration)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.5,
@@ -445,6 +455,8 @@ def main():
     else:
         line = run_ours(args, world, rank)
     if rank == 0 and line is not None:
+        if args.tokens and "config" in line:
+            line["config"]["reduced_for_profiling"] = True
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
