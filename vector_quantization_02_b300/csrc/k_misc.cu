@@ -300,8 +300,8 @@ score_fp32_d128_kernel(const float* __restrict__ q, const float* __restrict__ x,
 constexpr int kGH = 64, kGT = 128, kGK = 16;
 
 __global__ void __launch_bounds__(256)
-score_fp32_gemm_kernel(const float* __restrict__ q, const float* __restrict__ x, int H, int64_t N, int d,
-                       int h_tiles, int64_t t_tiles, float* __restrict__ logits) {
+score_fp32_gemm_kernel(const float* __restrict__ q, const float* __restrict__ x, int64_t x_gstride, int H,
+                       int64_t N, int d, int h_tiles, int64_t t_tiles, float* __restrict__ logits) {
   __shared__ __align__(16) float qs[kGK][kGH];
   __shared__ __align__(16) float xs[kGK][kGT];
   const int64_t bid = blockIdx.x;
@@ -312,7 +312,7 @@ score_fp32_gemm_kernel(const float* __restrict__ q, const float* __restrict__ x,
   const int64_t t0 = tt * kGT;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const float* qg = q + (g * H) * (int64_t)d;
-  const float* xg = x + (g * N) * (int64_t)d;
+  const float* xg = x + g * x_gstride;
   float acc[4][8];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -403,6 +403,18 @@ static cudaError_t launch_fp32_kt(const float* q, const float* x, int64_t G, int
   return cudaGetLastError();
 }
 
+// out[g][h][t] = sum_j q[g][h][j] x[t][j] with one x [N][d] for every group
+// (d % 16 == 0): e.g. Pi q and S q for many queries at once.
+cudaError_t launch_rows_times_shared(const float* q, const float* x, int64_t G, int H, int64_t N, int d, float* out,
+                                     cudaStream_t s) {
+  if (G * N == 0 || H == 0) return cudaSuccess;
+  if (d % kGK != 0) return cudaErrorInvalidValue;
+  const int h_tiles = (H + kGH - 1) / kGH;
+  const int64_t t_tiles = (N + kGT - 1) / kGT;
+  score_fp32_gemm_kernel<<<(unsigned)(G * t_tiles * h_tiles), 256, 0, s>>>(q, x, 0, H, N, d, h_tiles, t_tiles, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, int64_t N, int d,
                               float* logits, cudaStream_t s) {
   if (G * N == 0 || H == 0) return cudaSuccess;
@@ -411,7 +423,7 @@ cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, 
     const int h_tiles = (H + kGH - 1) / kGH;
     const int64_t t_tiles = (N + kGT - 1) / kGT;
     const int64_t blocks = G * t_tiles * h_tiles;
-    score_fp32_gemm_kernel<<<(unsigned)blocks, 256, 0, s>>>(q, x, H, N, d, h_tiles, t_tiles, logits);
+    score_fp32_gemm_kernel<<<(unsigned)blocks, 256, 0, s>>>(q, x, N * (int64_t)d, H, N, d, h_tiles, t_tiles, logits);
     return cudaGetLastError();
   }
   if (d == 128 && qbytes <= 96 * 1024) {

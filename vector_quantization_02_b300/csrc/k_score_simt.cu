@@ -163,9 +163,12 @@ topk_stage1(const float* __restrict__ x, int64_t N, int K, int splits, float* ws
   float* my_s = cs + t * K;
   int64_t* my_i = ci + t * K;
   int n = 0;
+  // the thread's current k-th best, kept in registers (most values fail the test)
+  float th_s = 0.f;
+  int64_t th_i = 0;
   for (int64_t i = lo + t; i < hi; i += kTopkThreads) {
-    float v = xr[i];
-    if (n == K && !better(v, i, my_s[K - 1], my_i[K - 1])) continue;
+    const float v = __ldg(xr + i);
+    if (n == K && !better(v, i, th_s, th_i)) continue;
     int pos = n < K ? n : K - 1;
     while (pos > 0 && better(v, i, my_s[pos - 1], my_i[pos - 1])) {
       my_s[pos] = my_s[pos - 1];
@@ -175,6 +178,10 @@ topk_stage1(const float* __restrict__ x, int64_t N, int K, int splits, float* ws
     my_s[pos] = v;
     my_i[pos] = i;
     if (n < K) ++n;
+    if (n == K) {
+      th_s = my_s[K - 1];
+      th_i = my_i[K - 1];
+    }
   }
   cnt[t] = n;
   __syncthreads();

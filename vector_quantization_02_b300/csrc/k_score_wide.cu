@@ -339,7 +339,7 @@ score_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const WideArgs a) {
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// qs [G][H][nv][d] fp32 (Pi q, S q) -> ops [G][NPART][N][d] bf16 parts
+// qs [nv][G][H][d] fp32 (Pi q, S q) -> ops [G][NPART][N][d] bf16 parts
 // (Pi q)_hi, (Pi q)_lo [, (S q)_hi, (S q)_lo]; heads H..N-1 are zero.
 __global__ void wide_split_kernel(const float* __restrict__ qs, int64_t G, int H, int N, int d, int nv,
                                   __nv_bfloat16* __restrict__ ops) {
@@ -350,7 +350,7 @@ __global__ void wide_split_kernel(const float* __restrict__ qs, int64_t G, int H
     const int h = (int)(r % N);
     const int64_t g = r / N;
     for (int v = 0; v < nv; ++v) {
-      const float x = h < H ? qs[((g * H + h) * nv + v) * d + j] : 0.f;
+      const float x = h < H ? qs[((v * G + g) * H + h) * d + j] : 0.f;
       const __nv_bfloat16 hi = __float2bfloat16_rn(x);
       const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
       ops[(((g * 2 * nv) + 2 * v + 0) * N + h) * (int64_t)d + j] = hi;
@@ -402,7 +402,10 @@ cudaError_t launch_score_wide(const tq_plan* p, const float* queries, int64_t G,
   float* qs = static_cast<float*>(ws);
   __nv_bfloat16* ops = reinterpret_cast<__nv_bfloat16*>(
       static_cast<char*>(ws) + (((size_t)G * H * nv * p->d * sizeof(float) + 255) & ~(size_t)255));
-  cudaError_t e = launch_query_prep(p, queries, G, H, qs, s);
+  // Pi q and S q of every query: products with matrices shared by all groups
+  cudaError_t e = launch_rows_times_shared(queries, p->Pi, G, H, p->d, p->d, qs, s);
+  if (e == cudaSuccess && nv == 2)
+    e = launch_rows_times_shared(queries, p->S, G, H, p->d, p->d, qs + (size_t)G * H * p->d, s);
   if (e != cudaSuccess) return e;
   wide_split_kernel<<<1184, 256, 0, s>>>(qs, G, H, Np, p->d, nv, ops);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
