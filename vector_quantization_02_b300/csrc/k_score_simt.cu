@@ -166,21 +166,33 @@ topk_stage1(const float* __restrict__ x, int64_t N, int K, int splits, float* ws
   // the thread's current k-th best, kept in registers (most values fail the test)
   float th_s = 0.f;
   int64_t th_i = 0;
-  for (int64_t i = lo + t; i < hi; i += kTopkThreads) {
-    const float v = __ldg(xr + i);
-    if (n == K && !better(v, i, th_s, th_i)) continue;
-    int pos = n < K ? n : K - 1;
-    while (pos > 0 && better(v, i, my_s[pos - 1], my_i[pos - 1])) {
-      my_s[pos] = my_s[pos - 1];
-      my_i[pos] = my_i[pos - 1];
-      --pos;
+  // eight independent loads in flight per step, then the tests in order
+  constexpr int kU = 8;
+  for (int64_t i0 = lo + t; i0 < hi; i0 += kU * kTopkThreads) {
+    float vs[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = i0 + (int64_t)u * kTopkThreads;
+      vs[u] = i < hi ? __ldg(xr + i) : 0.f;
     }
-    my_s[pos] = v;
-    my_i[pos] = i;
-    if (n < K) ++n;
-    if (n == K) {
-      th_s = my_s[K - 1];
-      th_i = my_i[K - 1];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = i0 + (int64_t)u * kTopkThreads;
+      const float v = vs[u];
+      if (i >= hi || (n == K && !better(v, i, th_s, th_i))) continue;
+      int pos = n < K ? n : K - 1;
+      while (pos > 0 && better(v, i, my_s[pos - 1], my_i[pos - 1])) {
+        my_s[pos] = my_s[pos - 1];
+        my_i[pos] = my_i[pos - 1];
+        --pos;
+      }
+      my_s[pos] = v;
+      my_i[pos] = i;
+      if (n < K) ++n;
+      if (n == K) {
+        th_s = my_s[K - 1];
+        th_i = my_i[K - 1];
+      }
     }
   }
   cnt[t] = n;
@@ -224,7 +236,7 @@ topk_stage2(const float* ws_s, const int64_t* ws_i, int splits, int K, float* ou
 }
 
 int topk_splits(int64_t rows, int64_t N, int K) {
-  int64_t s = (296 + rows - 1) / rows;     // about two CTAs per SM in total
+  int64_t s = (1184 + rows - 1) / rows;    // about eight CTAs per SM in total
   int64_t cap = N / (4 * (int64_t)K * kTopkThreads);  // keep every thread busy
   if (s > cap) s = cap;
   if (s < 1) s = 1;
