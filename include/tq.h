@@ -198,6 +198,14 @@ tq_status tq_plan_status(tq_plan* plan);
 
 const char* tq_status_string(tq_status status);
 
+/* Self-test of the device error path (no GPU fault is involved): launches one
+ * small kernel whose mbarrier waits are never satisfied; both bounded-wait
+ * forms the tensor-core kernels use give up after their poll limit (about a
+ * second), raise the plan's error word and return normally.  After the caller
+ * synchronises, tq_plan_status reports TQ_ETIMEOUT (and clears the word); the
+ * context and the plan stay usable.  Errors: TQ_EINVAL (null plan), TQ_ECUDA. */
+tq_status tq_selftest_wait_expiry(tq_plan* plan, void* stream);
+
 /* Version of the packed layout described above (bumped on any change). */
 int tq_format_version(void);
 

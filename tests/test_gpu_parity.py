@@ -240,3 +240,21 @@ def test_dispatch_paths(cuda, d, bits, mode, H, dtype, score_path, encode_path):
     plan = Inputs(d, bits, mode, 11, 12).plan()
     assert plan.score_path(H) == score_path
     assert plan.encode_path(dtype) == encode_path
+
+
+def test_bounded_wait_expiry_is_reported(cuda):
+    """A device wait that nothing satisfies gives up after its poll limit and
+    raises the plan's error word (TQ_ETIMEOUT once); nothing faults, and the
+    context and the plan keep working."""
+    d, G, N = 128, 1, 300
+    w, inp = _case_inputs(d, G, N, torch.float16, 3, "prod", True)
+    plan = inp.plan()
+    plan.selftest_wait_expiry()
+    torch.cuda.synchronize()
+    assert plan.status() == -5
+    assert plan.status() == 0
+    keys = tq_synth.keys(w)
+    packed = tq.tq_encode(plan, keys.to(cuda))
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    compare_encode(inp, packed.cpu().numpy(), keys)

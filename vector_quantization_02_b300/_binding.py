@@ -45,6 +45,7 @@ def _load() -> ctypes.CDLL:
         "tq_codebook_parity_expansion": (c_int, [c_int, vp, vp, vp, vp, vp]),
         "tq_score_path": (c_int, [vp, c_int]),
         "tq_encode_path": (c_int, [vp, c_int]),
+        "tq_selftest_wait_expiry": (c_int, [vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -57,7 +58,7 @@ lib = _load()
 EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_plan_destroy",
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
             "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
-            "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path")
+            "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path", "tq_selftest_wait_expiry")
 PATHS = {0: "tensor_d128", 1: "tensor_wide", 2: "cuda_core"}
 TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
 
@@ -173,6 +174,10 @@ class Plan:
 
     def status(self) -> int:
         return int(lib.tq_plan_status(self.handle))
+
+    def selftest_wait_expiry(self, stream=None) -> None:
+        """Enqueue the bounded-wait self-test; after a sync, status() reports TQ_ETIMEOUT once."""
+        _check(lib.tq_selftest_wait_expiry(self.handle, ctypes.c_void_p(_stream(stream))), "tq_selftest_wait_expiry")
 
     def score_path(self, H: int) -> str:
         """Kernel family tq_score takes for H heads: tensor_d128, tensor_wide or cuda_core."""

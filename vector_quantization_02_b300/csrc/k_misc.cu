@@ -1,4 +1,5 @@
 // Plan derivation, decode, and the uncompressed fp32 baseline.
+#include "ptx_sm100.cuh"
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -371,6 +372,23 @@ score_fp32_gemm_kernel(const float* __restrict__ q, const float* __restrict__ x,
   }
 }
 
+// One mbarrier that nothing arrives on: thread 0 polls it with back-off, thread
+// 32 with suspend hints; each gives up after its bounded number of polls.
+__global__ void wait_expiry_kernel(int* err) {
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  if (threadIdx.x == 0) ok = ptx::mbar_wait(ptx::smem_u32(&bar), 0, &abort_flag);
+  if (threadIdx.x == 32) ok = ptx::mbar_wait_suspend(ptx::smem_u32(&bar), 0, &abort_flag);
+  if (!ok) atomicAdd(err, 1);
+}
+
 }  // namespace
 
 cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s) {
@@ -412,6 +430,11 @@ cudaError_t launch_rows_times_shared(const float* q, const float* x, int64_t G, 
   const int h_tiles = (H + kGH - 1) / kGH;
   const int64_t t_tiles = (N + kGT - 1) / kGT;
   score_fp32_gemm_kernel<<<(unsigned)(G * t_tiles * h_tiles), 256, 0, s>>>(q, x, 0, H, N, d, h_tiles, t_tiles, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_expiry(int* err, cudaStream_t s) {
+  wait_expiry_kernel<<<1, 64, 0, s>>>(err);
   return cudaGetLastError();
 }
 

@@ -162,6 +162,11 @@ const char* tq_status_string(tq_status s) {
 
 int tq_format_version(void) { return 1; }
 
+tq_status tq_selftest_wait_expiry(tq_plan* p, void* stream) {
+  if (!p) return TQ_EINVAL;
+  return from_cuda(tq::launch_wait_expiry(p->err, static_cast<cudaStream_t>(stream)));
+}
+
 int tq_score_path(const tq_plan* p, int H) {
   if (!p || H < 1 || H > 256) return TQ_EINVAL;
   if (tq::score_tc_supported(p, H)) return TQ_PATH_TENSOR_D128;
