@@ -346,7 +346,7 @@ def run_ours(args, world, rank):
     arith = {"encode_tc": "f16/bf16 split operands on tensor cores", "encode_simt": "f32",
              "encode_wide": "f16 split operands on tensor cores",
              "score_tc": "e4m3 bit planes and query slices on tensor cores", "score_wide":
-             "bf16 split operands on tensor cores", "score_simt": "f32"}
+             "bf16 split operands on tensor cores"}
     dtype_desc = (f"encode: {arith[enc_kernel]}; score: {arith[sk.format('score')]}; f32 accumulate")
     # algorithmic flops of the estimate: two length-d dot products per (key, head)
     sc_roof = roof(sc_bytes, sc_cold_ms, sk.format("score"), ss.format("score"),

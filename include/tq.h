@@ -212,9 +212,12 @@ int tq_format_version(void);
 /* Which kernel family a call takes, for reports and tests (no GPU work):
  *   TQ_PATH_TENSOR_D128  tcgen05 kernels specialised for d = 128 (encode: fp16/bf16
  *                        keys, Prod; score: H <= 16, odd-symmetric codebook, k <= 3);
- *   TQ_PATH_TENSOR_WIDE  tcgen05 score for any d (multiple of 128), H <= 256;
- *   TQ_PATH_CUDA_CORE    CUDA-core kernels (every other shape).
- * Returns the path, or TQ_EINVAL for a null plan or an out-of-range argument. */
+ *   TQ_PATH_TENSOR_WIDE  tcgen05 kernels for any d (multiple of 128): encode of
+ *                        every other Prod plan and key dtype, score up to 256 heads;
+ *   TQ_PATH_CUDA_CORE    CUDA-core encode (MSE mode).
+ * Returns the path, or TQ_EINVAL for a null plan or an out-of-range argument
+ * (TQ_EUNSUPPORTED if no kernel takes the shape; none of the shapes the entry
+ * points accept). */
 typedef enum { TQ_PATH_TENSOR_D128 = 0, TQ_PATH_TENSOR_WIDE = 1, TQ_PATH_CUDA_CORE = 2 } tq_path;
 int tq_score_path(const tq_plan* plan, int n_heads);
 int tq_encode_path(const tq_plan* plan, tq_dtype dtype);

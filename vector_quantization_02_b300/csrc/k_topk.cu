@@ -1,110 +1,9 @@
-// Query preparation, score on packed keys (CUDA-core version) and top-k.
-//
-// Score follows the usage listing of "turboquant-pytorch 소개"
-// (``tq.inner_product(query, compressed)``) and its "2단계" paragraph: the
-// inner product is estimated without reconstructing the key,
-//     <q, x> ~ n <Pi q, c[idx]> + rho sqrt(pi/2)/m <S q, sign(S r)>,
-// which equals <q, n Pi^T c[idx]> + the QJL term because Pi is orthogonal.
-// Each query is rotated and projected once (query prep); every packed key
-// byte is then read once for all H query heads of its group (GQA batching).
+// Top-k of each row of the logits (the vector-search step keeps the best 10
+// keys per query): descending score, ties to the lower key index.
 #include "tq_internal.cuh"
 
 namespace tq {
 namespace {
-
-// qs[g][h][0][:] = Pi q, qs[g][h][1][:] = S q (PROD only)
-__global__ void query_prep_kernel(const float* __restrict__ q, int64_t GH, int d, int prod,
-                                  const float* __restrict__ PiT, const float* __restrict__ ST,
-                                  float* __restrict__ qs) {
-  extern __shared__ float sq[];
-  const int64_t row = blockIdx.x;
-  if (row >= GH) return;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) sq[i] = q[row * d + i];
-  __syncthreads();
-  const int nv = prod ? 2 : 1;
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
-    float a = 0.f, b = 0.f;
-    for (int i = 0; i < d; ++i) {
-      a = fmaf(__ldg(PiT + (int64_t)i * d + j), sq[i], a);
-      if (prod) b = fmaf(__ldg(ST + (int64_t)i * d + j), sq[i], b);
-    }
-    qs[(row * nv + 0) * d + j] = a;
-    if (prod) qs[(row * nv + 1) * d + j] = b;
-  }
-}
-
-// One CTA per (group, 128-token block); thread t scores token t against HC heads
-// at a time.
-template <int HC>
-__global__ void __launch_bounds__(128)
-score_simt_kernel(const float* __restrict__ qs, int64_t G, int H, Layout lay, CodeParams cp, float kappa,
-                  const uint8_t* __restrict__ packed, int64_t N, float* __restrict__ logits) {
-  extern __shared__ float sm[];
-  const int d = lay.d;
-  const int nv = lay.prod ? 2 : 1;
-  float* s_qr = sm;              // [HC][d]
-  float* s_sq = sm + HC * d;     // [HC][d]
-  __shared__ float s_c[kMaxLevels];
-  const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
-  const int64_t gb = blockIdx.x;
-  const int64_t g = gb / nb, blk = gb % nb;
-  const int t = threadIdx.x;
-  const int64_t tok = blk * kTokensPerBlock + t;
-  const uint8_t* in = packed + gb * lay.block_bytes;
-  if (t < kMaxLevels) s_c[t] = t < cp.L ? cp.c[t] : 0.f;
-  const float2 nr = *reinterpret_cast<const float2*>(in + lay.norms_off + (int64_t)t * 8);
-
-  for (int h0 = 0; h0 < H; h0 += HC) {
-    const int hc = min(HC, H - h0);
-    __syncthreads();
-    for (int i = t; i < hc * d; i += blockDim.x) {
-      int h = i / d, j = i - h * d;
-      const float* src = qs + (((g * H + h0 + h) * nv) * (int64_t)d);
-      s_qr[i] = src[j];
-      if (lay.prod) s_sq[i] = src[d + j];
-    }
-    __syncthreads();
-    float A[HC], B[HC];
-#pragma unroll
-    for (int h = 0; h < HC; ++h) A[h] = B[h] = 0.f;
-    for (int c = 0; c < lay.C; ++c) {
-      uint4 w[5];
-      for (int p = 0; p < lay.planes; ++p)
-        w[p] = *reinterpret_cast<const uint4*>(in + lay.plane_off(p, c, t));
-      for (int wd = 0; wd < 4; ++wd) {
-        unsigned pw[5];
-        for (int p = 0; p < lay.planes; ++p) pw[p] = wd == 0 ? w[p].x : wd == 1 ? w[p].y : wd == 2 ? w[p].z : w[p].w;
-        for (int i = 0; i < 32; ++i) {
-          const int j = c * kChunk + wd * 32 + i;
-          int idx = 0;
-          for (int p = 0; p < lay.k; ++p) idx |= ((pw[p] >> i) & 1u) << p;
-          const float cv = s_c[idx];
-          const bool pos = lay.prod ? ((pw[lay.k] >> i) & 1u) : false;
-#pragma unroll
-          for (int h = 0; h < HC; ++h) {
-            if (h < hc) {
-              A[h] = fmaf(s_qr[h * d + j], cv, A[h]);
-              if (lay.prod) {
-                float sv = s_sq[h * d + j];
-                B[h] += pos ? sv : -sv;
-              }
-            }
-          }
-        }
-      }
-    }
-    if (tok < N) {
-#pragma unroll
-      for (int h = 0; h < HC; ++h) {
-        if (h < hc) {
-          float v = nr.x * A[h];
-          if (lay.prod) v = fmaf(nr.y * kappa, B[h], v);
-          logits[((g * H) + h0 + h) * N + tok] = v;
-        }
-      }
-    }
-  }
-}
 
 // ---------------------------------------------------------------- top-k
 // Stage 1: CTA (row, split) keeps, per thread, the best K of a strided slice,
@@ -256,32 +155,6 @@ size_t topk_workspace_bytes(int64_t rows, int64_t N, int k) {
   return align256(n * sizeof(float)) + n * sizeof(int64_t);
 }
 
-cudaError_t launch_query_prep(const tq_plan* p, const float* q, int64_t G, int H, float* qs, cudaStream_t s) {
-  const int64_t GH = G * H;
-  if (GH == 0) return cudaSuccess;
-  query_prep_kernel<<<(unsigned)GH, 128, p->d * sizeof(float), s>>>(q, GH, p->d, p->lay.prod, p->PiT, p->ST, qs);
-  return cudaGetLastError();
-}
-
-template <int HC>
-static cudaError_t launch_score_hc(const tq_plan* p, const float* qs, int64_t G, int H, const uint8_t* packed,
-                                   int64_t N, float* logits, cudaStream_t s) {
-  const size_t smem = (size_t)2 * HC * p->d * sizeof(float);
-  auto kern = score_simt_kernel<HC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
-  kern<<<(unsigned)(G * nb), 128, smem, s>>>(qs, G, H, p->lay, p->cp, p->kappa, packed, N, logits);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_score_simt(const tq_plan* p, const float* qs, int64_t G, int H, const uint8_t* packed,
-                              int64_t N, float* logits, cudaStream_t s) {
-  if (G * N == 0) return cudaSuccess;
-  if (p->d <= 512) return launch_score_hc<8>(p, qs, G, H, packed, N, logits, s);
-  if (p->d <= 1024) return launch_score_hc<4>(p, qs, G, H, packed, N, logits, s);
-  return launch_score_hc<2>(p, qs, G, H, packed, N, logits, s);
-}
 
 cudaError_t launch_topk(const float* logits, int64_t rows, int64_t N, int k, float* top_scores,
                         int64_t* top_idx, void* ws, cudaStream_t s) {

@@ -16,7 +16,9 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-tq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ECUDA; }
+tq_status from_cuda(cudaError_t e) {
+  return e == cudaSuccess ? TQ_OK : e == cudaErrorNotSupported ? TQ_EUNSUPPORTED : TQ_ECUDA;
+}
 
 void free_plan(tq_plan* p) {
   if (!p) return;
@@ -30,7 +32,6 @@ void free_plan(tq_plan* p) {
   delete p;
 }
 
-int qs_vectors(const tq_plan* p) { return p->lay.prod ? 2 : 1; }
 
 // Byte offset of element (n, k) of a 128 x 128 16-bit matrix stored as the
 // tensor cores read a K-major operand with the 128-byte swizzle: two 64-wide
@@ -118,7 +119,7 @@ namespace tq {
 size_t score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k) {
   const size_t prep = score_tc_supported(p, H)     ? score_tc_workspace_bytes(p, G, H)
                       : score_wide_supported(p, H) ? score_wide_workspace_bytes(p, G, H)
-                                                   : (size_t)G * H * qs_vectors(p) * p->d * sizeof(float);
+                                                   : 0;
   return align256(prep) + topk_workspace_bytes(G * H, N, top_k) + 256;
 }
 
@@ -133,10 +134,7 @@ cudaError_t score_run(const tq_plan* p, const float* queries, int64_t G, int H, 
     prep = score_wide_workspace_bytes(p, G, H);
     e = launch_score_wide(p, queries, G, H, packed, N, logits, ws, s);
   } else {
-    prep = (size_t)G * H * qs_vectors(p) * p->d * sizeof(float);
-    float* qs = static_cast<float*>(ws);
-    e = launch_query_prep(p, queries, G, H, qs, s);
-    if (e == cudaSuccess) e = launch_score_simt(p, qs, G, H, packed, N, logits, s);
+    return cudaErrorNotSupported;  // every shape the API accepts fits one of the two
   }
   if (e == cudaSuccess && top_k > 0)
     e = launch_topk(logits, G * H, N, top_k, top_scores, top_idx, static_cast<char*>(ws) + align256(prep), s);
@@ -171,7 +169,7 @@ int tq_score_path(const tq_plan* p, int H) {
   if (!p || H < 1 || H > 256) return TQ_EINVAL;
   if (tq::score_tc_supported(p, H)) return TQ_PATH_TENSOR_D128;
   if (tq::score_wide_supported(p, H)) return TQ_PATH_TENSOR_WIDE;
-  return TQ_PATH_CUDA_CORE;
+  return TQ_EUNSUPPORTED;
 }
 
 int tq_encode_path(const tq_plan* p, tq_dtype dt) {

@@ -86,10 +86,6 @@ cudaError_t launch_encode_simt(const tq_plan* p, const void* keys, tq_dtype dt, 
 bool encode_tc_supported(const tq_plan* p, tq_dtype dt);
 cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N, uint8_t* packed,
                              cudaStream_t s);
-cudaError_t launch_query_prep(const tq_plan* p, const float* q, int64_t G, int H, float* qs,
-                              cudaStream_t s);
-cudaError_t launch_score_simt(const tq_plan* p, const float* qs, int64_t G, int H, const uint8_t* packed,
-                              int64_t N, float* logits, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int64_t rows, int64_t N, int k, float* top_scores,
                         int64_t* top_idx, void* ws, cudaStream_t s);
 cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
