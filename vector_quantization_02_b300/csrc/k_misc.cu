@@ -301,8 +301,12 @@ score_fp32_d128_kernel(const float* __restrict__ q, const float* __restrict__ x,
 constexpr int kGH = 64, kGT = 128, kGK = 16;
 
 __global__ void __launch_bounds__(256)
-score_fp32_gemm_kernel(const float* __restrict__ q, const float* __restrict__ x, int64_t x_gstride, int H,
-                       int64_t N, int d, int h_tiles, int64_t t_tiles, float* __restrict__ logits) {
+score_fp32_gemm_kernel(const float* __restrict__ q, const float* __restrict__ x0, const float* __restrict__ x1,
+                       int64_t x_gstride, int H, int64_t N, int d, int h_tiles, int64_t t_tiles,
+                       float* __restrict__ out0, float* __restrict__ out1) {
+  // blockIdx.y picks the matrix (and output) when two products share one launch
+  const float* __restrict__ x = blockIdx.y ? x1 : x0;
+  float* __restrict__ logits = blockIdx.y ? out1 : out0;
   __shared__ __align__(16) float qs[kGK][kGH];
   __shared__ __align__(16) float xs[kGK][kGT];
   const int64_t bid = blockIdx.x;
@@ -421,15 +425,18 @@ static cudaError_t launch_fp32_kt(const float* q, const float* x, int64_t G, int
   return cudaGetLastError();
 }
 
-// out[g][h][t] = sum_j q[g][h][j] x[t][j] with one x [N][d] for every group
+// out0[g][h][t] = sum_j q[g][h][j] x0[t][j] (and out1 with x1, in the same
+// launch, unless x1 is null) with matrices [N][d] shared by every group
 // (d % 16 == 0): e.g. Pi q and S q for many queries at once.
-cudaError_t launch_rows_times_shared(const float* q, const float* x, int64_t G, int H, int64_t N, int d, float* out,
-                                     cudaStream_t s) {
+cudaError_t launch_rows_times_shared(const float* q, const float* x0, const float* x1, int64_t G, int H, int64_t N,
+                                     int d, float* out0, float* out1, cudaStream_t s) {
   if (G * N == 0 || H == 0) return cudaSuccess;
   if (d % kGK != 0) return cudaErrorInvalidValue;
   const int h_tiles = (H + kGH - 1) / kGH;
   const int64_t t_tiles = (N + kGT - 1) / kGT;
-  score_fp32_gemm_kernel<<<(unsigned)(G * t_tiles * h_tiles), 256, 0, s>>>(q, x, 0, H, N, d, h_tiles, t_tiles, out);
+  const dim3 grid((unsigned)(G * t_tiles * h_tiles), x1 ? 2u : 1u);
+  score_fp32_gemm_kernel<<<grid, 256, 0, s>>>(q, x0, x1 ? x1 : x0, 0, H, N, d, h_tiles, t_tiles, out0,
+                                              x1 ? out1 : out0);
   return cudaGetLastError();
 }
 
@@ -446,7 +453,8 @@ cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, 
     const int h_tiles = (H + kGH - 1) / kGH;
     const int64_t t_tiles = (N + kGT - 1) / kGT;
     const int64_t blocks = G * t_tiles * h_tiles;
-    score_fp32_gemm_kernel<<<(unsigned)blocks, 256, 0, s>>>(q, x, N * (int64_t)d, H, N, d, h_tiles, t_tiles, logits);
+    score_fp32_gemm_kernel<<<(unsigned)blocks, 256, 0, s>>>(q, x, x, N * (int64_t)d, H, N, d, h_tiles, t_tiles,
+                                                            logits, logits);
     return cudaGetLastError();
   }
   if (d == 128 && qbytes <= 96 * 1024) {

@@ -403,9 +403,8 @@ cudaError_t launch_score_wide(const tq_plan* p, const float* queries, int64_t G,
   __nv_bfloat16* ops = reinterpret_cast<__nv_bfloat16*>(
       static_cast<char*>(ws) + (((size_t)G * H * nv * p->d * sizeof(float) + 255) & ~(size_t)255));
   // Pi q and S q of every query: products with matrices shared by all groups
-  cudaError_t e = launch_rows_times_shared(queries, p->Pi, G, H, p->d, p->d, qs, s);
-  if (e == cudaSuccess && nv == 2)
-    e = launch_rows_times_shared(queries, p->S, G, H, p->d, p->d, qs + (size_t)G * H * p->d, s);
+  cudaError_t e = launch_rows_times_shared(queries, p->Pi, nv == 2 ? p->S : nullptr, G, H, p->d, p->d, qs,
+                                           qs + (size_t)G * H * p->d, s);
   if (e != cudaSuccess) return e;
   wide_split_kernel<<<1184, 256, 0, s>>>(qs, G, H, Np, p->d, nv, ops);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

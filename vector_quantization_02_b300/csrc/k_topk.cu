@@ -18,30 +18,45 @@ __device__ __forceinline__ bool better(float a, int64_t ia, float b, int64_t ib)
 constexpr int kTopkThreads = 128;
 
 __device__ void block_merge(float* cs, int64_t* ci, int* cnt, int K, float* out_s, int64_t* out_i) {
-  // cs/ci: [kTopkThreads][K] sorted candidate lists (shared); cnt: per-thread lengths
-  __shared__ float rs[kTopkThreads];
-  __shared__ int64_t ri[kTopkThreads];
-  __shared__ int rt[kTopkThreads];
-  const int t = threadIdx.x;
+  // cs/ci: [kTopkThreads][K] sorted candidate lists (shared); cnt: per-thread lengths.
+  // Each round takes the best head of all lists: a butterfly over each warp,
+  // then the four warp winners; the winning thread advances its head.
+  constexpr int kWarps = kTopkThreads / 32;
+  __shared__ float ws_s[kWarps];
+  __shared__ int64_t ws_i[kWarps];
+  __shared__ int ws_t[kWarps];
+  __shared__ int win;
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
   int head = 0;
   for (int r = 0; r < K; ++r) {
-    rs[t] = head < cnt[t] ? cs[t * K + head] : -INFINITY;
-    ri[t] = head < cnt[t] ? ci[t * K + head] : INT64_MAX;
-    rt[t] = t;
-    __syncthreads();
-    for (int s = kTopkThreads / 2; s; s >>= 1) {
-      if (t < s && better(rs[t + s], ri[t + s], rs[t], ri[t])) {
-        rs[t] = rs[t + s];
-        ri[t] = ri[t + s];
-        rt[t] = rt[t + s];
+    float v = head < cnt[t] ? cs[t * K + head] : -INFINITY;
+    int64_t ix = head < cnt[t] ? ci[t * K + head] : INT64_MAX;
+    int tt = t;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+      const int64_t i2 = __shfl_xor_sync(0xffffffffu, ix, o);
+      const int t2 = __shfl_xor_sync(0xffffffffu, tt, o);
+      if (better(v2, i2, v, ix)) {
+        v = v2;
+        ix = i2;
+        tt = t2;
       }
-      __syncthreads();
     }
+    if (lane == 0) {
+      ws_s[wid] = v;
+      ws_i[wid] = ix;
+      ws_t[wid] = tt;
+    }
+    __syncthreads();
     if (t == 0) {
-      out_s[r] = rs[0];
-      out_i[r] = ri[0];
+      int b = 0;
+      for (int w = 1; w < kWarps; ++w)
+        if (better(ws_s[w], ws_i[w], ws_s[b], ws_i[b])) b = w;
+      out_s[r] = ws_s[b];
+      out_i[r] = ws_i[b];
+      win = ws_t[b];
     }
-    const int win = rt[0];
     __syncthreads();
     if (t == win) ++head;
   }

@@ -93,8 +93,8 @@ cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t 
 cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, int64_t N, int d,
                               float* logits, cudaStream_t s);
 cudaError_t launch_wait_expiry(int* err, cudaStream_t s);
-cudaError_t launch_rows_times_shared(const float* q, const float* x, int64_t G, int H, int64_t N, int d, float* out,
-                                     cudaStream_t s);
+cudaError_t launch_rows_times_shared(const float* q, const float* x0, const float* x1, int64_t G, int H, int64_t N,
+                                     int d, float* out0, float* out1, cudaStream_t s);
 
 size_t topk_workspace_bytes(int64_t rows, int64_t N, int k);
 
