@@ -46,7 +46,7 @@ typedef enum {
   TQ_OK = 0,
   TQ_EINVAL = -1,        /* bad size, null pointer, unsupported combination */
   TQ_EALIGN = -2,        /* a pointer is not 16-byte aligned */
-  TQ_EUNSUPPORTED = -3,  /* valid request this build does not handle */
+  TQ_EUNSUPPORTED = -3,  /* valid request that no kernel of the library handles */
   TQ_ECUDA = -4,         /* a CUDA call failed (launch, copy, allocation) */
   TQ_ETIMEOUT = -5,      /* a bounded device wait ran out (see tq_plan_status) */
   TQ_ENOMEM = -6         /* device allocation failed in tq_plan_create */
