@@ -229,8 +229,10 @@ def run_ours(args, world, rank):
 
     keys = tq_synth.keys(w, device=dev, seed_offset=rank)
     q = tq_synth.queries(w, device=dev, seed_offset=rank)
+    mse = args.mode == "mse"
     plan = tq.Plan.from_seeds(d, bits, tq_synth.rotation_gaussian(d, w.seeds["rotation"]),
-                              tq_synth.projection(d, w.seeds["projection"]))
+                              None if mse else tq_synth.projection(d, w.seeds["projection"]),
+                              mode=args.mode)
     packed = torch.empty(plan.packed_bytes(G, N), dtype=torch.uint8, device=dev)
     logits = torch.empty(G, H, N, dtype=torch.float32, device=dev)
     top_k = w.top_k
@@ -324,11 +326,12 @@ def run_ours(args, world, rank):
             r["gbs"] = round(ach, 1)
         return r
 
-    kernels = {"tensor_d128": ("{}_tc", "k_{}_tc.cu"), "tensor_wide": ("{}_wide", "k_{}_wide.cu"),
-               "cuda_core": ("{}_simt", "k_{}_simt.cu")}
+    kernels = {"tensor_d128": ("{}_tc", "k_{}_tc.cu"), "tensor_wide": ("{}_wide", "k_{}_wide.cu")}
     ek, es = kernels[plan.encode_path(w.key_dtype)]
     enc_kernel, enc_src = ek.format("encode"), es.format("encode")
-    enc_roof = roof(enc_bytes, enc_ms, enc_kernel, enc_src, flops=4 * d * d * G * N)
+    # algorithmic flops: one d x d projection per key (Pi u), two in Prod (and S r)
+    enc_roof = roof(enc_bytes, enc_ms, enc_kernel, enc_src,
+                    flops=(2 if plan.mode == "prod" else 1) * 2 * d * d * G * N)
 
     # score alone on a cold L2 (a decode step reads a cache encoded earlier)
     sc_cold = []
@@ -343,7 +346,7 @@ def run_ours(args, world, rank):
     torch.cuda.synchronize()
     sc_cold_ms = statistics.median(a.elapsed_time(b) for a, b in sc_cold)
     sk, ss = kernels[plan.score_path(H)]
-    arith = {"encode_tc": "f16/bf16 split operands on tensor cores", "encode_simt": "f32",
+    arith = {"encode_tc": "f16/bf16 split operands on tensor cores",
              "encode_wide": "f16 split operands on tensor cores",
              "score_tc": "e4m3 bit planes and query slices on tensor cores", "score_wide":
              "bf16 split operands on tensor cores"}
@@ -386,7 +389,7 @@ def run_ours(args, world, rank):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_desc,
         "data": "synthetic",
-        "config": {"workload": w.name, "G": G, "N": N, "H": H, "d": d, "bits": bits,
+        "config": {"workload": w.name, "mode": args.mode, "G": G, "N": N, "H": H, "d": d, "bits": bits,
                    "key_dtype": str(w.key_dtype).replace("torch.", ""), "top_k": top_k,
                    "l2": "flushed between steps (2x L2 memset, outside the step events)"},
         "roofline": enc_roof,
@@ -440,6 +443,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen25_3b_decode", choices=sorted(tq_synth.WORKLOADS))
     ap.add_argument("--bits", type=int, default=0)
+    ap.add_argument("--mode", choices=["prod", "mse"], default="prod",
+                    help="TurboQuantProd (the workloads' method) or TurboQuantMSE codec")
     ap.add_argument("--tokens", type=int, default=0,
                     help="cap the tokens per group (a reduced case for profiling; not a bench configuration)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")

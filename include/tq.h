@@ -127,7 +127,10 @@ size_t tq_packed_bytes(const tq_plan* plan, int64_t n_groups, int64_t n_tokens);
  * z = [S r >= 0].  A zero key stores idx = #{t_i < 0}, z = 1, rho = 0.
  *   keys    device [G][N][d] row-major in `dtype` (fp32, fp16 or bf16).
  *   packed  device, tq_packed_bytes(plan, G, N) bytes, fully overwritten.
- * G >= 0, N >= 0 (G*N == 0 is a no-op).  Errors: TQ_EINVAL, TQ_EALIGN, TQ_ECUDA. */
+ * G >= 0, N >= 0 (G*N == 0 is a no-op).  Errors: TQ_EINVAL, TQ_EALIGN, TQ_ECUDA;
+ * TQ_EUNSUPPORTED for G*N >= 2^31 - 256 keys outside the d = 128 fp16/bf16
+ * TurboQuantProd kernel (key rows are 32-bit copy coordinates; such a call
+ * would hold at least 512 GiB of keys). */
 tq_status tq_encode(const tq_plan* plan, const void* keys, tq_dtype dtype, int64_t n_groups,
                     int64_t n_tokens, void* packed, void* stream);
 
@@ -213,12 +216,12 @@ int tq_format_version(void);
  *   TQ_PATH_TENSOR_D128  tcgen05 kernels specialised for d = 128 (encode: fp16/bf16
  *                        keys, Prod; score: H <= 16, odd-symmetric codebook, k <= 3);
  *   TQ_PATH_TENSOR_WIDE  tcgen05 kernels for any d (multiple of 128): encode of
- *                        every other Prod plan and key dtype, score up to 256 heads;
- *   TQ_PATH_CUDA_CORE    CUDA-core encode (MSE mode).
+ *                        every other plan (Prod or MSE) and key dtype, score up
+ *                        to 256 heads.
  * Returns the path, or TQ_EINVAL for a null plan or an out-of-range argument
  * (TQ_EUNSUPPORTED if no kernel takes the shape; none of the shapes the entry
  * points accept). */
-typedef enum { TQ_PATH_TENSOR_D128 = 0, TQ_PATH_TENSOR_WIDE = 1, TQ_PATH_CUDA_CORE = 2 } tq_path;
+typedef enum { TQ_PATH_TENSOR_D128 = 0, TQ_PATH_TENSOR_WIDE = 1 } tq_path;
 int tq_score_path(const tq_plan* plan, int n_heads);
 int tq_encode_path(const tq_plan* plan, tq_dtype dtype);
 

@@ -35,10 +35,10 @@ def _groups(G: int) -> list:
     return sorted({0, G // 2, G - 1})
 
 
-def _group_fields(packed: torch.Tensor, plan, g: int, N: int, d: int, bits: int) -> dict:
+def _group_fields(packed: torch.Tensor, plan, g: int, N: int, d: int, bits: int, mode: str) -> dict:
     per_group = plan.packed_bytes(1, N)
     buf = packed[g * per_group:(g + 1) * per_group].cpu().numpy()
-    return o.unpack(buf, d, bits, "prod", 1, N)
+    return o.unpack(buf, d, bits, mode, 1, N)
 
 
 def _exact_topk(L: np.ndarray, k: int):
@@ -56,16 +56,19 @@ def _exact_topk(L: np.ndarray, k: int):
     return out_s, out_i
 
 
-CASES = [("single_head_3bit", 3), ("qwen25_3b_decode", 3), ("llama31_8b_prefill", 2),
-         ("llama31_8b_prefill", 3), ("llama31_8b_prefill", 4), ("long_context_131k", 4),
-         ("vector_search_1m", 4)]
+CASES = [("single_head_3bit", 3, "prod"), ("qwen25_3b_decode", 3, "prod"), ("llama31_8b_prefill", 2, "prod"),
+         ("llama31_8b_prefill", 3, "prod"), ("llama31_8b_prefill", 4, "prod"), ("long_context_131k", 4, "prod"),
+         ("vector_search_1m", 4, "prod"),
+         # the MSE codec on the same shapes (many tiles per CTA: d = 128 has a
+         # single K slice per tile, d = 1536 a 16-level codebook)
+         ("qwen25_3b_decode", 3, "mse"), ("vector_search_1m", 4, "mse")]
 
 
-@pytest.mark.parametrize("name,bits", CASES)
-def test_full_size_sampled(cuda, name, bits):
+@pytest.mark.parametrize("name,bits,mode", CASES)
+def test_full_size_sampled(cuda, name, bits, mode):
     w = tq_synth.WORKLOADS[name]
     G, N, H, d = w.G, w.N, w.H, w.d
-    inp = Inputs(d, bits, "prod", w.seeds["rotation"], w.seeds["projection"])
+    inp = Inputs(d, bits, mode, w.seeds["rotation"], w.seeds["projection"])
     plan = inp.plan()
     keys = tq_synth.keys(w, device=cuda)
     q = tq_synth.queries(w, device=cuda)
@@ -82,14 +85,17 @@ def test_full_size_sampled(cuda, name, bits):
     for g in _groups(G):
         toks = _samples(N, seed=1000 * g + bits)
         x = keys[g, torch.from_numpy(toks).to(cuda)].double().cpu().numpy()
-        e = o.encode_prod(x, inp.Pi_o, inp.S_o, inp.c_o)
-        f = _group_fields(packed, plan, g, N, d, bits)
+        e = o.encode_prod(x, inp.Pi_o, inp.S_o, inp.c_o) if mode == "prod" else o.encode_mse(x, inp.Pi_o, inp.c_o)
+        f = _group_fields(packed, plan, g, N, d, bits, mode)
         got = {k: v[toks] for k, v in f.items()}
         compare_fields(inp, got, e, x)
         total_coords += x.size
         # logits from identical packed input: the oracle scores the GPU's fields
         qg = q[g].cpu()
-        want = o.score_prod(qg.numpy(), got["idx"], got["z"], got["n"], got["rho"], inp.Pi_o, inp.S_o, inp.c_o)
+        if mode == "prod":
+            want = o.score_prod(qg.numpy(), got["idx"], got["z"], got["n"], got["rho"], inp.Pi_o, inp.S_o, inp.c_o)
+        else:
+            want = o.score_mse(qg.numpy(), got["idx"], got["n"], inp.Pi_o, inp.c_o)
         gl = logits[g][:, torch.from_numpy(toks).to(cuda)].cpu().numpy()
         compare_logits(gl[None], want[None], qg[None], got["n"].astype(np.float64)[None])
         if name == "long_context_131k":

@@ -32,6 +32,10 @@ ENCODE_CASES = [
     (384, 1, 300, torch.float32, 3, "prod", True),
     (512, 1, 129, torch.bfloat16, 2, "prod", False),
     (1536, 1, 300, torch.float32, 4, "prod", False),
+    # MSE codec on the wide tensor-core encode: 16 levels (select path), d = 384, fp32 at d = 1536
+    (128, 1, 300, torch.bfloat16, 4, "mse", True),
+    (384, 1, 200, torch.float16, 2, "mse", False),
+    (1536, 1, 130, torch.float32, 3, "mse", False),
 ]
 
 
@@ -232,7 +236,8 @@ def test_argument_errors_on_gpu(cuda):
     (128, 3, "prod", 16, torch.float32, "tensor_d128", "tensor_wide"),    # single head, fp32 keys
     (1536, 4, "prod", 256, torch.float32, "tensor_wide", "tensor_wide"),  # vector search
     (128, 3, "prod", 40, torch.float16, "tensor_wide", "tensor_d128"),
-    (256, 4, "mse", 20, torch.bfloat16, "tensor_wide", "cuda_core"),
+    (256, 4, "mse", 20, torch.bfloat16, "tensor_wide", "tensor_wide"),
+    (128, 3, "mse", 8, torch.float16, "tensor_d128", "tensor_wide"),
 ])
 def test_dispatch_paths(cuda, d, bits, mode, H, dtype, score_path, encode_path):
     """The kernel family each workload's shape takes (so bench labels and

@@ -59,7 +59,7 @@ EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_p
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
             "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
             "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path", "tq_selftest_wait_expiry")
-PATHS = {0: "tensor_d128", 1: "tensor_wide", 2: "cuda_core"}
+PATHS = {0: "tensor_d128", 1: "tensor_wide"}
 TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
 
 
@@ -180,7 +180,7 @@ class Plan:
         _check(lib.tq_selftest_wait_expiry(self.handle, ctypes.c_void_p(_stream(stream))), "tq_selftest_wait_expiry")
 
     def score_path(self, H: int) -> str:
-        """Kernel family tq_score takes for H heads: tensor_d128, tensor_wide or cuda_core."""
+        """Kernel family tq_score takes for H heads: tensor_d128 or tensor_wide."""
         r = int(lib.tq_score_path(self.handle, H))
         _check(min(r, 0), "tq_score_path")
         return PATHS[r]

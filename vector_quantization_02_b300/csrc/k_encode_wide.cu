@@ -1,7 +1,8 @@
 // Encode on the tensor cores for any head dimension d (a multiple of 128) and
-// any key dtype, TurboQuantProd: the shape of a vector-search index (10^6
-// fp32 keys of d = 1536), where the two d x d projections are long dense
-// contractions.
+// any key dtype: the shape of a vector-search index (10^6 fp32 keys of
+// d = 1536), where the two d x d projections are long dense contractions.
+// TurboQuantProd runs both projections; TurboQuantMSE ("turboquant-pytorch
+// 소개", "1단계" alone) runs E2 only and stores ||r|| = 0 with no sign plane.
 //
 // Same computation as the other encode kernels ("turboquant-pytorch 소개",
 // "1단계" then "2단계"): y = Pi x, codes idx_j = #{i : n t_i < y_j},
@@ -143,16 +144,17 @@ constexpr float kYScale = 65536.f;      // Y = 2^16 Pi u
 constexpr float kRScale = 1.f / 64.f;   // E5 operand 2^10 r' = 2^-6 (2^16 r')
 
 // DT: key dtype, 0 fp32, 1 fp16, 2 bf16.
-template <int L, int DT, bool PX>
+template <int L, int DT, bool PX, bool PROD>
 __global__ void __launch_bounds__(kEThreads, 1)
 encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_constant__ CUtensorMap tmM,
                    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR,
                    const EncWideArgs a) {
-  constexpr int K = L == 2 ? 1 : L == 4 ? 2 : 3;  // code planes
+  constexpr int K = L == 2 ? 1 : L == 4 ? 2 : L == 8 ? 3 : 4;  // code planes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
   const int d = a.lay.d, NC = a.NC, J = a.J, S = a.S;
+  const int JOBS = PROD ? 2 * J : J;  // E2 jobs, then (Prod) E5 jobs
   const uint32_t off_bar = kStages * kStageBytes;
   float* s_rr = reinterpret_cast<float*>(smem + off_bar + BAR_COUNT * 8);  // [2][128]
   __shared__ uint32_t tmem_slot;
@@ -191,13 +193,15 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &abort_flag;
-  if (s_slot >= (uint32_t)a.nslots) {  // cannot happen with a plan built on this device
+  // (Prod) the residual scratch slot of this SM; cannot be out of range with
+  // a plan built on this device
+  if (PROD && s_slot >= (uint32_t)a.nslots) {
     if (threadIdx.x == 0) raise(a.err, abort);
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, 512);
     return;
   }
-  uint16_t* scr = static_cast<uint16_t*>(a.scratch) + (size_t)s_slot * 2 * 128 * d;
+  uint16_t* scr = PROD ? static_cast<uint16_t*>(a.scratch) + (size_t)s_slot * 2 * 128 * d : nullptr;
 
   const int64_t n_my = blockIdx.x < a.n_tiles ? (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
@@ -216,7 +220,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
         const int64_t tile = blockIdx.x + i * gridDim.x;
         const int64_t g = tile / a.nb, blk = tile - g * a.nb;
         const int32_t xrow0 = (int32_t)(g * a.N + blk * kTokensPerBlock);
-        for (int job = 0; ok && job < 2 * J; ++job) {
+        for (int job = 0; ok && job < JOBS; ++job) {
           const bool e2 = job < J;
           if (job == J) {  // the residual rows of this tile are in the scratch
             if (!mbar_wait_suspend(bar(BAR_RREADY), (uint32_t)i & 1u, abort)) {
@@ -271,7 +275,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       uint32_t b = 0, bph = 0, s = 0, aph = 0, cq = 0;
       bool ok = true;
       for (int64_t i = 0; ok && i < n_my; ++i) {
-        for (int job = 0; ok && job < 2 * J; ++job) {
+        for (int job = 0; ok && job < JOBS; ++job) {
           const bool e2 = job < J;
           // K in slices of 128 coordinates, each into a fresh partial accumulator
           for (int c = 0; ok && c < S / kSliceStages; ++c, ++cq) {
@@ -388,7 +392,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
         if (++b == kStages) b = 0;
       }
       // the tile's E5 stages pass through the ring without this role
-      b = (uint32_t)((b + (uint32_t)(J * S)) % kStages);
+      if constexpr (PROD) b = (uint32_t)((b + (uint32_t)(J * S)) % kStages);
     }
     if (!ok) raise(a.err, abort);
   } else {
@@ -412,7 +416,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       float nt[L - 1], nc[L];
       uint32_t nhalf[NT];
       float nmid = 0.f;
-      for (int job = 0; ok && job < 2 * J; ++job) {
+      for (int job = 0; ok && job < JOBS; ++job) {
         const bool e2 = job < J;
         if (job == 0) {
           n = *reinterpret_cast<const float*>(out + a.lay.norms_off + row * 8);
@@ -495,14 +499,16 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
                 rr = fmaf(rv, rv, rr);
                 r2[u] = rv * kRScale;
               }
-              split_h2(r2[0], r2[1], hi[e >> 1], lo[e >> 1]);
+              if constexpr (PROD) split_h2(r2[0], r2[1], hi[e >> 1], lo[e >> 1]);
             }
-            uint4* dh = reinterpret_cast<uint4*>(rhi + cbase + 32 * g32);
-            uint4* dl = reinterpret_cast<uint4*>(rlo + cbase + 32 * g32);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              __stcg(dh + t, make_uint4(hi[4 * t], hi[4 * t + 1], hi[4 * t + 2], hi[4 * t + 3]));
-              __stcg(dl + t, make_uint4(lo[4 * t], lo[4 * t + 1], lo[4 * t + 2], lo[4 * t + 3]));
+            if constexpr (PROD) {
+              uint4* dh = reinterpret_cast<uint4*>(rhi + cbase + 32 * g32);
+              uint4* dl = reinterpret_cast<uint4*>(rlo + cbase + 32 * g32);
+  #pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                __stcg(dh + t, make_uint4(hi[4 * t], hi[4 * t + 1], hi[4 * t + 2], hi[4 * t + 3]));
+                __stcg(dl + t, make_uint4(lo[4 * t], lo[4 * t + 1], lo[4 * t + 2], lo[4 * t + 3]));
+              }
             }
 #pragma unroll
             for (int p = 0; p < K; ++p) pl[p][g32] = w[p];
@@ -519,7 +525,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
           uint8_t* dst = out + a.lay.plane_off(p, chunk, row) + 4 * w0;
           *reinterpret_cast<uint2*>(dst) = live ? make_uint2(pl[p][0], pl[p][1]) : make_uint2(0, 0);
         }
-        if (e2 && job == J - 1) {
+        if (PROD && e2 && job == J - 1) {
           // every residual row of the tile written by this thread, made
           // visible to the TMA loads (async proxy) that read them
           asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -527,16 +533,25 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
         }
       }
       if (!ok) break;
-      // rho: the two warpgroups' partial sums
-      s_rr[wg * 128 + row] = rr;
-      mbar_arrive(bar(BAR_RHO));
-      if (wg == 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_RHO), (uint32_t)i & 1u, abort))) {
-          ok = false;
-          break;
+      if constexpr (PROD) {
+        // rho: the two warpgroups' partial sums.  Warpgroup 1 cannot run a
+        // whole tile ahead here (the tile's E5 waits for both warpgroups'
+        // residual rows), so this barrier's phases cannot alias.
+        s_rr[wg * 128 + row] = rr;
+        mbar_arrive(bar(BAR_RHO));
+        if (wg == 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_RHO), (uint32_t)i & 1u, abort))) {
+            ok = false;
+            break;
+          }
+          const float rho = n * (sqrtf(s_rr[row] + s_rr[128 + row]) * (1.f / kYScale));
+          *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, rho)
+                                                                               : make_float2(0.f, 0.f);
         }
-        const float rho = n * (sqrtf(s_rr[row] + s_rr[128 + row]) * (1.f / kYScale));
-        *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, rho)
+      } else if (wg == 0) {
+        // MSE stores ||r|| = 0 and needs no exchange (which, with one K slice
+        // per tile at d = 128, would let warpgroup 1 lap this barrier)
+        *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, 0.f)
                                                                              : make_float2(0.f, 0.f);
       }
     }
@@ -613,7 +628,7 @@ struct EncMaps {
   CUtensorMap pi, m, x, r;
 };
 
-template <int L, int DT, bool PX>
+template <int L, int DT, bool PX, bool PROD>
 cudaError_t launch_ew(const tq_plan* p, const EncWideArgs& a, const EncMaps& mp, cudaStream_t s) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -624,7 +639,7 @@ cudaError_t launch_ew(const tq_plan* p, const EncWideArgs& a, const EncMaps& mp,
                                                                                     a.lay, a.packed);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = encode_wide_kernel<L, DT, PX>;
+  auto kern = encode_wide_kernel<L, DT, PX, PROD>;
   const size_t smem = enc_wide_smem(a.NC);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -633,14 +648,22 @@ cudaError_t launch_ew(const tq_plan* p, const EncWideArgs& a, const EncMaps& mp,
   return cudaGetLastError();
 }
 
-template <int DT, bool PX>
+template <int DT, bool PX, bool PROD>
 cudaError_t launch_ew_l(const tq_plan* p, const EncWideArgs& a, const EncMaps& mp, cudaStream_t s) {
   switch (p->cp.L) {
-    case 2: return launch_ew<2, DT, PX>(p, a, mp, s);
-    case 4: return launch_ew<4, DT, PX>(p, a, mp, s);
-    case 8: return launch_ew<8, DT, PX>(p, a, mp, s);
+    case 2: return launch_ew<2, DT, PX, PROD>(p, a, mp, s);
+    case 4: return launch_ew<4, DT, PX, PROD>(p, a, mp, s);
+    case 8: return launch_ew<8, DT, PX, PROD>(p, a, mp, s);
+    case 16:  // 4-bit MSE codebooks take the threshold-by-threshold centroid
+      if constexpr (!PX && !PROD) return launch_ew<16, DT, false, false>(p, a, mp, s);
+      break;
   }
   return cudaErrorInvalidValue;
+}
+
+template <int DT, bool PX>
+cudaError_t launch_ew_m(const tq_plan* p, const EncWideArgs& a, const EncMaps& mp, cudaStream_t s) {
+  return p->lay.prod ? launch_ew_l<DT, PX, true>(p, a, mp, s) : launch_ew_l<DT, PX, false>(p, a, mp, s);
 }
 
 bool odd_masks_w(const ParityExpansion& px, int k) {
@@ -666,8 +689,9 @@ int query_nsmid() {
 
 bool encode_wide_supported(const tq_plan* p, tq_dtype dt) {
   (void)dt;
-  return p->lay.prod && p->wide_ops && p->wide_scratch && p->d % 128 == 0 && p->cp.L >= 2 && p->cp.L <= 8 &&
-         enc_wide_smem(enc_wide_nc(p->d)) <= 227 * 1024;
+  const bool prod = p->lay.prod != 0;
+  return p->wide_ops && (!prod || p->wide_scratch) && p->d % 128 == 0 && p->cp.L >= 2 &&
+         p->cp.L <= (prod ? 8 : 16) && enc_wide_smem(enc_wide_nc(p->d)) <= 227 * 1024;
 }
 
 cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N,
@@ -690,17 +714,19 @@ cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, 
   a.packed = packed;
   a.scratch = p->wide_scratch;
   a.err = p->err;
-  // B operands: [hi rows; lo rows] of 2^8 Pi and of M (fp16)
+  // B operands: [hi rows; lo rows] of 2^8 Pi and (Prod) of M (fp16)
   const size_t dd = (size_t)d * d;
   const uint16_t* pi = p->wide_ops;
-  const uint16_t* m = p->wide_ops + 2 * dd;
+  const uint16_t* m = p->lay.prod ? p->wide_ops + 2 * dd : nullptr;
   EncMaps mp;
   const uint32_t nc = (uint32_t)a.NC;
   cudaError_t e = make_tmap_2d(&mp.pi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pi, (uint64_t)d, 2 * (uint64_t)d,
                                (uint64_t)d * 2, kStageK, nc, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && p->lay.prod)
     e = make_tmap_2d(&mp.m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, m, (uint64_t)d, 2 * (uint64_t)d, (uint64_t)d * 2, kStageK,
                      nc, CU_TENSOR_MAP_SWIZZLE_64B);
+  else if (e == cudaSuccess)
+    mp.m = mp.pi;  // an MSE plan holds no M; its encode has no E5 and never reads this map
   // key tiles: 128 rows x 32 values (rows past G N read as zero)
   if (e == cudaSuccess) {
     const CUtensorMapDataType xt = dt == TQ_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -710,16 +736,21 @@ cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, 
     e = make_tmap_2d(&mp.x, xt, keys, (uint64_t)d, (uint64_t)(G * N), (uint64_t)d * es, kStageK, kTokensPerBlock,
                      dt == TQ_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   }
-  // residual rows of the per-SM scratch: [slot][hi, lo][128][d] fp16
-  if (e == cudaSuccess)
-    e = make_tmap_2d(&mp.r, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p->wide_scratch, (uint64_t)d,
-                     (uint64_t)p->wide_slots * 256, (uint64_t)d * 2, kStageK, kTokensPerBlock,
-                     CU_TENSOR_MAP_SWIZZLE_64B);
+  // residual rows of the per-SM scratch: [slot][hi, lo][128][d] fp16 (Prod; an
+  // MSE encode has no E5 and never reads this map)
+  if (e == cudaSuccess) {
+    if (p->lay.prod)
+      e = make_tmap_2d(&mp.r, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p->wide_scratch, (uint64_t)d,
+                       (uint64_t)p->wide_slots * 256, (uint64_t)d * 2, kStageK, kTokensPerBlock,
+                       CU_TENSOR_MAP_SWIZZLE_64B);
+    else
+      mp.r = mp.pi;
+  }
   if (e != cudaSuccess) return e;
   const bool px = odd_masks_w(p->px, p->lay.k);
-  if (dt == TQ_F32) return px ? launch_ew_l<0, true>(p, a, mp, s) : launch_ew_l<0, false>(p, a, mp, s);
-  if (dt == TQ_F16) return px ? launch_ew_l<1, true>(p, a, mp, s) : launch_ew_l<1, false>(p, a, mp, s);
-  return px ? launch_ew_l<2, true>(p, a, mp, s) : launch_ew_l<2, false>(p, a, mp, s);
+  if (dt == TQ_F32) return px ? launch_ew_m<0, true>(p, a, mp, s) : launch_ew_m<0, false>(p, a, mp, s);
+  if (dt == TQ_F16) return px ? launch_ew_m<1, true>(p, a, mp, s) : launch_ew_m<1, false>(p, a, mp, s);
+  return px ? launch_ew_m<2, true>(p, a, mp, s) : launch_ew_m<2, false>(p, a, mp, s);
 }
 
 }  // namespace tq

@@ -65,17 +65,17 @@ void split_images(const float* A, uint8_t* hi, uint8_t* lo) {
     }
 }
 
-// Row-major fp16 hi + lo splits of 2^8 Pi and of M for the wide tensor-core
-// encode, and its per-SM residual scratch (PROD, any d).  The power of two
+// Row-major fp16 hi + lo splits of 2^8 Pi and (Prod) of M for the wide
+// tensor-core encode, and (Prod) its per-SM residual scratch; any d.  The power of two
 // keeps the lo parts of Pi's entries (|Pi_ij| ~ d^-1/2) out of the fp16
 // subnormal range; M = S Pi^T has entries of order 1.
 cudaError_t build_wide_ops(tq_plan* p) {
   const size_t dd = (size_t)p->d * p->d;
-  std::vector<float> Pi(dd), M(dd);
+  std::vector<float> Pi(dd), M(p->lay.prod ? dd : 0);
   cudaError_t e = cudaMemcpy(Pi.data(), p->Pi, dd * 4, cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemcpy(M.data(), p->M, dd * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && p->lay.prod) e = cudaMemcpy(M.data(), p->M, dd * 4, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return e;
-  std::vector<uint16_t> host(4 * dd);
+  std::vector<uint16_t> host((p->lay.prod ? 4 : 2) * dd);
   auto split = [&](float v, size_t hi_at, size_t lo_at) {
     const __half h = __float2half_rn(v);
     const __half l = __float2half_rn(v - __half2float(h));
@@ -84,11 +84,11 @@ cudaError_t build_wide_ops(tq_plan* p) {
   };
   for (size_t i = 0; i < dd; ++i) {
     split(Pi[i] * 256.f, i, dd + i);
-    split(M[i], 2 * dd + i, 3 * dd + i);
+    if (p->lay.prod) split(M[i], 2 * dd + i, 3 * dd + i);
   }
   e = cudaMalloc(&p->wide_ops, host.size() * 2);
   if (e == cudaSuccess) e = cudaMemcpy(p->wide_ops, host.data(), host.size() * 2, cudaMemcpyHostToDevice);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !p->lay.prod) return e;  // an MSE encode needs no residual scratch
   int slots = tq::query_nsmid();
   if (slots <= 0) return cudaErrorUnknown;
   p->wide_slots = slots;
@@ -176,7 +176,7 @@ int tq_encode_path(const tq_plan* p, tq_dtype dt) {
   if (!p || (dt != TQ_F32 && dt != TQ_F16 && dt != TQ_BF16)) return TQ_EINVAL;
   if (tq::encode_tc_supported(p, dt)) return TQ_PATH_TENSOR_D128;
   if (tq::encode_wide_supported(p, dt)) return TQ_PATH_TENSOR_WIDE;
-  return TQ_PATH_CUDA_CORE;
+  return TQ_EUNSUPPORTED;
 }
 
 tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
@@ -266,7 +266,7 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
       return TQ_ECUDA;
     }
   }
-  if (L.prod) {
+  {
     const cudaError_t we = build_wide_ops(p);
     if (we != cudaSuccess) {
       free_plan(p);
@@ -299,9 +299,10 @@ tq_status tq_encode(const tq_plan* p, const void* keys, tq_dtype dtype, int64_t 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (encode_tc_supported(p, dtype))
     return from_cuda(launch_encode_tc(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
-  if (encode_wide_supported(p, dtype) && G * N < (int64_t)INT32_MAX - 2 * kTokensPerBlock)  // TMA row coordinates
-    return from_cuda(launch_encode_wide(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
-  return from_cuda(launch_encode_simt(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
+  // the wide encode addresses key rows by 32-bit TMA coordinates: 2^31 keys
+  // of the smallest kind (d = 128, 16-bit) would be 512 GiB, beyond the device
+  if (!encode_wide_supported(p, dtype) || G * N >= (int64_t)INT32_MAX - 2 * kTokensPerBlock) return TQ_EUNSUPPORTED;
+  return from_cuda(launch_encode_wide(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
 }
 
 size_t tq_score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k) {

@@ -69,7 +69,7 @@ struct tq_plan {
   float* ST;          // [d][d] = S^T (PROD)
   float* M;           // [d][d] = S Pi^T (PROD)
   float* MT;          // [d][d] = M^T (PROD)
-  uint16_t* wide_ops;  // (PROD) row-major fp16 [4][d][d]: (2^8 Pi) hi, lo; M hi, lo
+  uint16_t* wide_ops;  // row-major fp16 [4][d][d]: (2^8 Pi) hi, lo; (PROD) M hi, lo
   void* wide_scratch;  // (PROD) residual rows of the wide encode: [wide_slots][2][128][d] bf16
   int wide_slots;      // SM ids of the device (%nsmid)
   uint8_t* tc_ops;    // tensor-core operand images (d = 128, PROD): Pi hi/lo fp16,
@@ -81,8 +81,6 @@ namespace tq {
 
 // ---- launchers (one per kernel family); all return cudaGetLastError()
 cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s);
-cudaError_t launch_encode_simt(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N,
-                               uint8_t* packed, cudaStream_t s);
 bool encode_tc_supported(const tq_plan* p, tq_dtype dt);
 cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N, uint8_t* packed,
                              cudaStream_t s);
