@@ -128,9 +128,8 @@ size_t tq_packed_bytes(const tq_plan* plan, int64_t n_groups, int64_t n_tokens);
  *   keys    device [G][N][d] row-major in `dtype` (fp32, fp16 or bf16).
  *   packed  device, tq_packed_bytes(plan, G, N) bytes, fully overwritten.
  * G >= 0, N >= 0 (G*N == 0 is a no-op).  Errors: TQ_EINVAL, TQ_EALIGN, TQ_ECUDA;
- * TQ_EUNSUPPORTED for G*N >= 2^31 - 256 keys outside the d = 128 fp16/bf16
- * TurboQuantProd kernel (key rows are 32-bit copy coordinates; such a call
- * would hold at least 512 GiB of keys). */
+ * TQ_EUNSUPPORTED for G*N >= 2^31 - 256 keys (key rows are 32-bit copy
+ * coordinates; such a call would hold at least 512 GiB of keys). */
 tq_status tq_encode(const tq_plan* plan, const void* keys, tq_dtype dtype, int64_t n_groups,
                     int64_t n_tokens, void* packed, void* stream);
 
@@ -214,10 +213,10 @@ int tq_format_version(void);
 
 /* Which kernel family a call takes, for reports and tests (no GPU work):
  *   TQ_PATH_TENSOR_D128  tcgen05 kernels specialised for d = 128 (encode: fp16/bf16
- *                        keys, Prod; score: H <= 16, odd-symmetric codebook, k <= 3);
+ *                        keys, either mode; score: H <= 16, odd-symmetric
+ *                        codebook, k <= 3);
  *   TQ_PATH_TENSOR_WIDE  tcgen05 kernels for any d (multiple of 128): encode of
- *                        every other plan (Prod or MSE) and key dtype, score up
- *                        to 256 heads.
+ *                        every other plan and key dtype, score up to 256 heads.
  * Returns the path, or TQ_EINVAL for a null plan or an out-of-range argument
  * (TQ_EUNSUPPORTED if no kernel takes the shape; none of the shapes the entry
  * points accept). */

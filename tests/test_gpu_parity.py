@@ -32,8 +32,12 @@ ENCODE_CASES = [
     (384, 1, 300, torch.float32, 3, "prod", True),
     (512, 1, 129, torch.bfloat16, 2, "prod", False),
     (1536, 1, 300, torch.float32, 4, "prod", False),
-    # MSE codec on the wide tensor-core encode: 16 levels (select path), d = 384, fp32 at d = 1536
+    # MSE codec: the d = 128 kernel with 16 levels (select path) and with
+    # several tiles per CTA; the wide kernel at d = 128 (fp32, several tiles
+    # per CTA), d = 384 and fp32 d = 1536
     (128, 1, 300, torch.bfloat16, 4, "mse", True),
+    (128, 2, 40000, torch.float16, 3, "mse", False),
+    (128, 1, 40000, torch.float32, 4, "mse", True),
     (384, 1, 200, torch.float16, 2, "mse", False),
     (1536, 1, 130, torch.float32, 3, "mse", False),
 ]
@@ -237,7 +241,8 @@ def test_argument_errors_on_gpu(cuda):
     (1536, 4, "prod", 256, torch.float32, "tensor_wide", "tensor_wide"),  # vector search
     (128, 3, "prod", 40, torch.float16, "tensor_wide", "tensor_d128"),
     (256, 4, "mse", 20, torch.bfloat16, "tensor_wide", "tensor_wide"),
-    (128, 3, "mse", 8, torch.float16, "tensor_d128", "tensor_wide"),
+    (128, 3, "mse", 8, torch.float16, "tensor_d128", "tensor_d128"),
+    (128, 4, "mse", 8, torch.float32, "tensor_wide", "tensor_wide"),
 ])
 def test_dispatch_paths(cuda, d, bits, mode, H, dtype, score_path, encode_path):
     """The kernel family each workload's shape takes (so bench labels and

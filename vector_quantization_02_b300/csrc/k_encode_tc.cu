@@ -1,5 +1,6 @@
 // Encode on the 5th-generation tensor cores (tcgen05 + TMA + TMEM), d = 128,
-// fp16 or bf16 keys, TurboQuantProd.
+// fp16 or bf16 keys, TurboQuantProd; TurboQuantMSE ("turboquant-pytorch 소개",
+// "1단계" alone) runs E1-E3 and E6 only, with up to 16 levels and rho = 0.
 //
 // Same computation as the CUDA-core encode ("turboquant-pytorch 소개",
 // "1단계" then "2단계"): y = Pi x, codes idx_j = #{i : n t_i < y_j},
@@ -90,10 +91,10 @@ __device__ __forceinline__ float2 pair_to_float2(uint32_t w) {
 // codebook ({1}, {1, 2} or {1, 2, 4, 7}); the centroid n c[idx] is then summed
 // from the code bits' sign words (one LOP3 and one FADD per term) instead of
 // selected threshold by threshold.
-template <int L, bool kBF16, bool PX>
+template <int L, bool kBF16, bool PX, bool PROD>
 __global__ void __launch_bounds__(kThreads, 1)
 encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
-  constexpr int K = L == 2 ? 1 : L == 4 ? 2 : 3;  // code planes
+  constexpr int K = L == 2 ? 1 : L == 4 ? 2 : L == 8 ? 3 : 4;  // code planes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
@@ -136,11 +137,13 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&tmX);
-      mbar_arrive_expect_tx(bar(BAR_OPS), 4 * kOpBytes);
+      mbar_arrive_expect_tx(bar(BAR_OPS), (PROD ? 4 : 2) * kOpBytes);
       bulk_load(sb + kOffPiHi, a.pi_hi, kOpBytes, bar(BAR_OPS));
       bulk_load(sb + kOffPiLo, a.pi_lo, kOpBytes, bar(BAR_OPS));
-      bulk_load(sb + kOffMHi, a.m_hi, kOpBytes, bar(BAR_OPS));
-      bulk_load(sb + kOffMLo, a.m_lo, kOpBytes, bar(BAR_OPS));
+      if constexpr (PROD) {
+        bulk_load(sb + kOffMHi, a.m_hi, kOpBytes, bar(BAR_OPS));
+        bulk_load(sb + kOffMLo, a.m_lo, kOpBytes, bar(BAR_OPS));
+      }
       int64_t issued = 0;
       for (int64_t i = 0; i < n_my; ++i) {
         const int s = (int)(i % kStages);
@@ -169,8 +172,9 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       constexpr uint32_t idesc_x = idesc_f16(kBF16 ? 1u : 0u, 128, 128);
       constexpr uint32_t idesc_r = idesc_f16(1u, 128, 128);
       const bool e2 = warp == 1;
+      const int64_t n_iss = (PROD || e2) ? n_my : 0;  // MSE has no E5
       bool ok = mbar_wait(bar(BAR_OPS), 0, abort);
-      for (int64_t i = 0; ok && i < n_my; ++i) {
+      for (int64_t i = 0; ok && i < n_iss; ++i) {
         const int b = (int)(i & 1);
         const uint32_t j = (uint32_t)(i >> 1);
         if (e2) {
@@ -345,18 +349,24 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
                 cv += __uint_as_float(nhalf[3] ^ ((xb[0] ^ xb[1] ^ xb[2]) & kS));
               }
             }
-            const float rv = y - cv;
-            rr = fmaf(rv, rv, rr);
-            r2[u] = rv;
+            if constexpr (PROD) {
+              const float rv = y - cv;
+              rr = fmaf(rv, rv, rr);
+              r2[u] = rv;
+            }
           }
-          const __nv_bfloat162 h = __floats2bfloat162_rn(r2[0], r2[1]);
-          const float2 hf = __bfloat1622float2(h);
-          const __nv_bfloat162 l = __floats2bfloat162_rn(r2[0] - hf.x, r2[1] - hf.y);
-          hi[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
-          lo[e >> 1] = *reinterpret_cast<const uint32_t*>(&l);
+          if constexpr (PROD) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(r2[0], r2[1]);
+            const float2 hf = __bfloat1622float2(h);
+            const __nv_bfloat162 l = __floats2bfloat162_rn(r2[0] - hf.x, r2[1] - hf.y);
+            hi[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[e >> 1] = *reinterpret_cast<const uint32_t*>(&l);
+          }
         }
-        tmem_st16(t_lane + 32 * cc, hi);
-        tmem_st16(t_lane + 32 * cc + 16, lo);
+        if constexpr (PROD) {
+          tmem_st16(t_lane + 32 * cc, hi);
+          tmem_st16(t_lane + 32 * cc + 16, lo);
+        }
 #pragma unroll
         for (int p = 0; p < K; ++p) {
           pl[p][0] = pl[p][1];
@@ -376,22 +386,24 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
         tmem_ld_wait();
         if (cc + 2 < 4) tmem_ld32(t_lane + 32 * (cc + 2), va);
         chunk(vb, cc + 1);
-        // this half of the residual is in TMEM: E5 may start on it
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(BAR_RFULL + 2 * wg + (cc >> 1)));
+        if constexpr (PROD) {
+          // this half of the residual is in TMEM: E5 may start on it
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(BAR_RFULL + 2 * wg + (cc >> 1)));
+        }
         if (cc + 2 < 4) tmem_ld_wait();
       }
-      const float rho = sqrtf(rr);
+      const float rho = PROD ? sqrtf(rr) : 0.f;
 
-      // E5 result -> sign plane
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PFULL + wg), j & 1, abort))) {
-        raise(a.err, abort);
-        break;
-      }
-      tc_fence_after();
-      uint32_t zs[4];
-      {
+      uint32_t zs[4] = {0u, 0u, 0u, 0u};
+      if constexpr (PROD) {
+        // E5 result -> sign plane
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PFULL + wg), j & 1, abort))) {
+          raise(a.err, abort);
+          break;
+        }
+        tc_fence_after();
         uint32_t v[4][32];
         tmem_ld32(t_lane + 128, v[0]);
         tmem_ld32(t_lane + 160, v[1]);
@@ -407,6 +419,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
           zs[cc] = n > 0.f ? ~z : 0xFFFFFFFFu;
         }
       }
+      // (MSE: every Y column has been read) the accumulator is free
       tc_fence_before();
       mbar_arrive(bar(BAR_ACCEMPTY + wg));
 
@@ -418,8 +431,9 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
                                : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(out + ((int64_t)p * kTokensPerBlock + row) * 16) = val;
       }
-      *reinterpret_cast<uint4*>(out + ((int64_t)K * kTokensPerBlock + row) * 16) =
-          live ? make_uint4(zs[0], zs[1], zs[2], zs[3]) : make_uint4(0, 0, 0, 0);
+      if constexpr (PROD)
+        *reinterpret_cast<uint4*>(out + ((int64_t)K * kTokensPerBlock + row) * 16) =
+            live ? make_uint4(zs[0], zs[1], zs[2], zs[3]) : make_uint4(0, 0, 0, 0);
       *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, rho) : make_float2(0.f, 0.f);
     }
   }
@@ -440,7 +454,7 @@ bool odd_masks(const ParityExpansion& px, int k) {
   return true;
 }
 
-template <int L, bool kBF16, bool PX>
+template <int L, bool kBF16, bool PX, bool PROD>
 cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, uint8_t* packed, cudaStream_t s) {
   CUtensorMap tm;
   const cudaError_t te = make_tmap_2d(&tm, kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -457,11 +471,11 @@ cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, 
   const uint8_t* ops = p->tc_ops;
   a.pi_hi = ops + (kBF16 ? 2 : 0) * kOpBytes;
   a.pi_lo = ops + (kBF16 ? 3 : 1) * kOpBytes;
-  a.m_hi = ops + 4 * kOpBytes;
-  a.m_lo = ops + 5 * kOpBytes;
+  a.m_hi = PROD ? ops + 4 * kOpBytes : nullptr;  // an MSE plan holds the Pi images only
+  a.m_lo = PROD ? ops + 5 * kOpBytes : nullptr;
   a.packed = packed;
   a.err = p->err;
-  auto kern = encode_tc_kernel<L, kBF16, PX>;
+  auto kern = encode_tc_kernel<L, kBF16, PX, PROD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
@@ -475,24 +489,35 @@ cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, 
 }  // namespace
 
 bool encode_tc_supported(const tq_plan* p, tq_dtype dt) {
-  return p->tc_ops != nullptr && p->d == 128 && p->lay.prod && (dt == TQ_F16 || dt == TQ_BF16) &&
-         p->cp.L >= 2 && p->cp.L <= 8;
+  return p->tc_ops != nullptr && p->d == 128 && (dt == TQ_F16 || dt == TQ_BF16) && p->cp.L >= 2 &&
+         p->cp.L <= (p->lay.prod ? 8 : 16);
 }
 
 cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N, uint8_t* packed,
                              cudaStream_t s) {
   const bool bf = dt == TQ_BF16;
-  const int k = p->cp.L == 2 ? 1 : p->cp.L == 4 ? 2 : 3;
+  const int k = p->cp.L == 2 ? 1 : p->cp.L == 4 ? 2 : p->cp.L == 8 ? 3 : 4;
   const bool px = odd_masks(p->px, k);
-#define TQ_ENC_CASE(LV)                                                                                        \
-  case LV:                                                                                                     \
-    if (px) return bf ? launch_tc<LV, true, true>(p, keys, G, N, packed, s)                                    \
-                      : launch_tc<LV, false, true>(p, keys, G, N, packed, s);                                  \
-    return bf ? launch_tc<LV, true, false>(p, keys, G, N, packed, s) : launch_tc<LV, false, false>(p, keys, G, N, packed, s);
+  const bool prod = p->lay.prod != 0;
+#define TQ_ENC_CASE(LV, PR)                                                                                    \
+  if (px) return bf ? launch_tc<LV, true, true, PR>(p, keys, G, N, packed, s)                                  \
+                    : launch_tc<LV, false, true, PR>(p, keys, G, N, packed, s);                                \
+  return bf ? launch_tc<LV, true, false, PR>(p, keys, G, N, packed, s)                                         \
+            : launch_tc<LV, false, false, PR>(p, keys, G, N, packed, s);
   switch (p->cp.L) {
-    TQ_ENC_CASE(2)
-    TQ_ENC_CASE(4)
-    TQ_ENC_CASE(8)
+    case 2:
+      if (prod) { TQ_ENC_CASE(2, true) }
+      TQ_ENC_CASE(2, false)
+    case 4:
+      if (prod) { TQ_ENC_CASE(4, true) }
+      TQ_ENC_CASE(4, false)
+    case 8:
+      if (prod) { TQ_ENC_CASE(8, true) }
+      TQ_ENC_CASE(8, false)
+    case 16:  // 4-bit MSE codebooks: no parity expansion of that size
+      if (!prod) return bf ? launch_tc<16, true, false, false>(p, keys, G, N, packed, s)
+                           : launch_tc<16, false, false, false>(p, keys, G, N, packed, s);
+      break;
   }
 #undef TQ_ENC_CASE
   return cudaErrorInvalidValue;

@@ -95,17 +95,19 @@ cudaError_t build_wide_ops(tq_plan* p) {
   return cudaMalloc(&p->wide_scratch, (size_t)slots * 2 * 128 * p->d * 2);
 }
 
-// Operand images for the tensor-core encode (d = 128, PROD).
+// Operand images for the tensor-core encode (d = 128): Pi hi/lo in fp16 and
+// in bf16, and (PROD) M hi/lo in bf16.
 cudaError_t build_tc_ops(tq_plan* p) {
   constexpr size_t img = 128 * 128 * 2;
-  std::vector<float> Pi(128 * 128), M(128 * 128);
-  std::vector<uint8_t> host(6 * img);
+  const bool prod = p->lay.prod != 0;
+  std::vector<float> Pi(128 * 128), M(prod ? 128 * 128 : 0);
+  std::vector<uint8_t> host((prod ? 6 : 4) * img);
   cudaError_t e = cudaMemcpy(Pi.data(), p->Pi, Pi.size() * 4, cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemcpy(M.data(), p->M, M.size() * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && prod) e = cudaMemcpy(M.data(), p->M, M.size() * 4, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return e;
   split_images<__half>(Pi.data(), host.data(), host.data() + img);
   split_images<__nv_bfloat16>(Pi.data(), host.data() + 2 * img, host.data() + 3 * img);
-  split_images<__nv_bfloat16>(M.data(), host.data() + 4 * img, host.data() + 5 * img);
+  if (prod) split_images<__nv_bfloat16>(M.data(), host.data() + 4 * img, host.data() + 5 * img);
   e = cudaMalloc(&p->tc_ops, host.size());
   if (e == cudaSuccess) e = cudaMemcpy(p->tc_ops, host.data(), host.size(), cudaMemcpyHostToDevice);
   return e;
@@ -260,7 +262,7 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
     p->px.c0 = (float)c0;
     p->px.mid = (float)mid;
   }
-  if (L.prod && d == 128) {
+  if (d == 128) {
     if (build_tc_ops(p) != cudaSuccess) {
       free_plan(p);
       return TQ_ECUDA;
@@ -297,11 +299,12 @@ tq_status tq_encode(const tq_plan* p, const void* keys, tq_dtype dtype, int64_t 
   if (!keys || !packed) return TQ_EINVAL;
   if (!aligned16(keys) || !aligned16(packed)) return TQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // both encodes address key rows by 32-bit TMA coordinates: 2^31 keys of the
+  // smallest kind (d = 128, 16-bit) would be 512 GiB, beyond the device
+  if (G * N >= (int64_t)INT32_MAX - 2 * kTokensPerBlock) return TQ_EUNSUPPORTED;
   if (encode_tc_supported(p, dtype))
     return from_cuda(launch_encode_tc(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
-  // the wide encode addresses key rows by 32-bit TMA coordinates: 2^31 keys
-  // of the smallest kind (d = 128, 16-bit) would be 512 GiB, beyond the device
-  if (!encode_wide_supported(p, dtype) || G * N >= (int64_t)INT32_MAX - 2 * kTokensPerBlock) return TQ_EUNSUPPORTED;
+  if (!encode_wide_supported(p, dtype)) return TQ_EUNSUPPORTED;
   return from_cuda(launch_encode_wide(p, keys, dtype, G, N, static_cast<uint8_t*>(packed), s));
 }
 

@@ -72,8 +72,8 @@ struct tq_plan {
   uint16_t* wide_ops;  // row-major fp16 [4][d][d]: (2^8 Pi) hi, lo; (PROD) M hi, lo
   void* wide_scratch;  // (PROD) residual rows of the wide encode: [wide_slots][2][128][d] bf16
   int wide_slots;      // SM ids of the device (%nsmid)
-  uint8_t* tc_ops;    // tensor-core operand images (d = 128, PROD): Pi hi/lo fp16,
-                      // Pi hi/lo bf16, M hi/lo bf16; 32 KB each, K-major 128-byte swizzle
+  uint8_t* tc_ops;    // tensor-core operand images (d = 128): Pi hi/lo fp16,
+                      // Pi hi/lo bf16, (PROD) M hi/lo bf16; 32 KB each, K-major 128-byte swizzle
   int* err;           // device error word
 };
 
