@@ -377,6 +377,28 @@ def run_ours(args, world, rank):
                 "score_speedup_vs_fp32_keys": round(bms / sc_cold_ms, 3)}
         del keys32, base_l
 
+    # decode of every key (not part of the step), cold L2, where it runs on tensor cores
+    dec = None
+    if plan.decode_path() == "tensor_d128" and d * G * N * 4 < 40e9:
+        xh = torch.empty(G, N, d, dtype=torch.float32, device=dev)
+        dt = []
+        for _ in range(max(3, args.steps)):
+            flush.zero_()
+            lead(300)
+            a, b = ev(), ev()
+            a.record(stream)
+            tq.tq_decode(plan, packed, G, N, out=xh)
+            b.record(stream)
+            dt.append((a, b))
+        torch.cuda.synchronize()
+        assert plan.status() == 0
+        dms = statistics.median(a.elapsed_time(b) for a, b in dt)
+        # algorithmic bytes: the packed keys in, fp32 rows out; flops: one d x d
+        # product per key, two in Prod
+        dec = {"ms": round(dms, 5), "vectors_per_s": G * N / (dms * 1e-3),
+               "roofline": roof(P + G * N * d * 4, dms, "decode_tc", "k_decode_tc.cu",
+                                flops=(2 if plan.mode == "prod" else 1) * 2 * d * d * G * N)}
+        del xh
 
     # end to end through the public API from pinned host memory
     if key_bytes > 8e9:
@@ -399,6 +421,7 @@ def run_ours(args, world, rank):
                       "keys_per_s_cold_l2": G * N / (sc_cold_ms * 1e-3),
                       "logits_per_s_cold_l2": G * N * H / (sc_cold_ms * 1e-3), "roofline_cold_l2": sc_roof},
             "fp32_key_baseline": base,
+            "decode": dec,
         },
         "e2e": None if e2e_ms is None else {
             "value": keys_total / (e2e_ms * 1e-3), "unit": "keys/s", "h2d_bytes_per_step": key_bytes + q_bytes,

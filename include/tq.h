@@ -216,13 +216,16 @@ int tq_format_version(void);
  *                        keys, either mode; score: H <= 16, odd-symmetric
  *                        codebook, k <= 3);
  *   TQ_PATH_TENSOR_WIDE  tcgen05 kernels for any d (multiple of 128): encode of
- *                        every other plan and key dtype, score up to 256 heads.
+ *                        every other plan and key dtype, score up to 256 heads;
+ *   TQ_PATH_CUDA_CORE    CUDA-core kernels: decode for d > 128.
+ * tq_decode takes a tcgen05 kernel at d = 128 (either mode).
  * Returns the path, or TQ_EINVAL for a null plan or an out-of-range argument
  * (TQ_EUNSUPPORTED if no kernel takes the shape; none of the shapes the entry
  * points accept). */
-typedef enum { TQ_PATH_TENSOR_D128 = 0, TQ_PATH_TENSOR_WIDE = 1 } tq_path;
+typedef enum { TQ_PATH_TENSOR_D128 = 0, TQ_PATH_TENSOR_WIDE = 1, TQ_PATH_CUDA_CORE = 2 } tq_path;
 int tq_score_path(const tq_plan* plan, int n_heads);
 int tq_encode_path(const tq_plan* plan, tq_dtype dtype);
+int tq_decode_path(const tq_plan* plan);
 
 #ifdef __cplusplus
 }

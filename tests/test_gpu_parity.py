@@ -141,16 +141,21 @@ def test_score_top_k(cuda, d, G, N, H, k):
     assert np.array_equal(ts.cpu().numpy(), want_s)
 
 
-@pytest.mark.parametrize("d,G,N,bits,mode", [(128, 2, 300, 3, "prod"), (256, 1, 129, 4, "prod"),
-                                             (128, 1, 200, 2, "mse")])
+@pytest.mark.parametrize("d,G,N,bits,mode", [
+    (128, 2, 300, 3, "prod"), (256, 1, 129, 4, "prod"), (128, 1, 200, 2, "mse"),
+    # the d = 128 tensor-core decode: one key, several tiles per CTA (both
+    # modes, 16 levels), 1-bit codes over a ragged tail
+    (128, 1, 1, 2, "prod"), (128, 1, 40000, 4, "prod"), (128, 2, 20000, 4, "mse"), (128, 3, 129, 1, "mse")])
 def test_decode_matches_oracle(cuda, d, G, N, bits, mode):
     w, inp = _case_inputs(d, G, N, torch.float32, bits, mode, False, seed=41)
     keys = tq_synth.keys(w)
     buf, e = oracle_encode(inp, keys)
     want = o.decode_packed(buf, inp.Pi_o, inp.S_o, inp.c_o, d, bits, mode, G, N)
     plan = inp.plan()
+    assert plan.decode_path() == ("tensor_d128" if d == 128 else "cuda_core")
     got = tq.tq_decode(plan, torch.from_numpy(buf.copy()).to(cuda), G, N)
     torch.cuda.synchronize()
+    assert plan.status() == 0
     n = e["n"].reshape(G, N, 1)
     assert np.all(np.abs(got.cpu().numpy() - want) <= 1e-5 * n + 1e-30)
 

@@ -45,6 +45,7 @@ def _load() -> ctypes.CDLL:
         "tq_codebook_parity_expansion": (c_int, [c_int, vp, vp, vp, vp, vp]),
         "tq_score_path": (c_int, [vp, c_int]),
         "tq_encode_path": (c_int, [vp, c_int]),
+        "tq_decode_path": (c_int, [vp]),
         "tq_selftest_wait_expiry": (c_int, [vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -58,8 +59,9 @@ lib = _load()
 EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_plan_destroy",
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
             "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
-            "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path", "tq_selftest_wait_expiry")
-PATHS = {0: "tensor_d128", 1: "tensor_wide"}
+            "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path", "tq_decode_path",
+            "tq_selftest_wait_expiry")
+PATHS = {0: "tensor_d128", 1: "tensor_wide", 2: "cuda_core"}
 TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
 
 
@@ -189,6 +191,12 @@ class Plan:
         """Kernel family tq_encode takes for keys of this dtype."""
         r = int(lib.tq_encode_path(self.handle, _DTYPES[dtype]))
         _check(min(r, 0), "tq_encode_path")
+        return PATHS[r]
+
+    def decode_path(self) -> str:
+        """Kernel family tq_decode takes: tensor_d128 or cuda_core."""
+        r = int(lib.tq_decode_path(self.handle))
+        _check(min(r, 0), "tq_decode_path")
         return PATHS[r]
 
 

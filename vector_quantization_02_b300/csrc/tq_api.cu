@@ -95,19 +95,43 @@ cudaError_t build_wide_ops(tq_plan* p) {
   return cudaMalloc(&p->wide_scratch, (size_t)slots * 2 * 128 * p->d * 2);
 }
 
-// Operand images for the tensor-core encode (d = 128): Pi hi/lo in fp16 and
-// in bf16, and (PROD) M hi/lo in bf16.
+// Operand images for the tensor-core encode and decode (d = 128): Pi hi/lo in
+// fp16 and in bf16, (PROD) M hi/lo in bf16, then 2^8 Pi^T hi/lo and (PROD)
+// 2^8 S^T hi/lo in fp16; and the decode's split codebook 2^8 c_i.
 cudaError_t build_tc_ops(tq_plan* p) {
   constexpr size_t img = 128 * 128 * 2;
   const bool prod = p->lay.prod != 0;
-  std::vector<float> Pi(128 * 128), M(prod ? 128 * 128 : 0);
-  std::vector<uint8_t> host((prod ? 6 : 4) * img);
+  std::vector<float> Pi(128 * 128), M(prod ? 128 * 128 : 0), S(prod ? 128 * 128 : 0);
+  std::vector<uint8_t> host((prod ? 10 : 6) * img);
   cudaError_t e = cudaMemcpy(Pi.data(), p->Pi, Pi.size() * 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && prod) e = cudaMemcpy(M.data(), p->M, M.size() * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && prod) e = cudaMemcpy(S.data(), p->S, S.size() * 4, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return e;
   split_images<__half>(Pi.data(), host.data(), host.data() + img);
   split_images<__nv_bfloat16>(Pi.data(), host.data() + 2 * img, host.data() + 3 * img);
   if (prod) split_images<__nv_bfloat16>(M.data(), host.data() + 4 * img, host.data() + 5 * img);
+  // decode B operands: row j of the image holds column j of Pi (of S), scaled by 2^8
+  std::vector<float> T(128 * 128);
+  auto transposed_scaled = [&](const std::vector<float>& A) {
+    for (int n = 0; n < 128; ++n)
+      for (int k = 0; k < 128; ++k) T[n * 128 + k] = 256.f * A[k * 128 + n];
+  };
+  transposed_scaled(Pi);
+  split_images<__half>(T.data(), host.data() + tq::tc_dec_image(p, 0) * img, host.data() + tq::tc_dec_image(p, 1) * img);
+  if (prod) {
+    transposed_scaled(S);
+    split_images<__half>(T.data(), host.data() + tq::tc_dec_image(p, 2) * img,
+                         host.data() + tq::tc_dec_image(p, 3) * img);
+  }
+  for (int i = 0; i < 16; ++i) {
+    const float v = i < p->cp.L ? 256.f * p->cp.c[i] : 0.f;
+    const __half h = __float2half_rn(v);
+    const __half l = __float2half_rn(v - __half2float(h));
+    uint16_t hb, lb;
+    std::memcpy(&hb, &h, 2);
+    std::memcpy(&lb, &l, 2);
+    p->dec_ctab[i] = (uint32_t)hb | ((uint32_t)lb << 16);
+  }
   e = cudaMalloc(&p->tc_ops, host.size());
   if (e == cudaSuccess) e = cudaMemcpy(p->tc_ops, host.data(), host.size(), cudaMemcpyHostToDevice);
   return e;
@@ -172,6 +196,11 @@ int tq_score_path(const tq_plan* p, int H) {
   if (tq::score_tc_supported(p, H)) return TQ_PATH_TENSOR_D128;
   if (tq::score_wide_supported(p, H)) return TQ_PATH_TENSOR_WIDE;
   return TQ_EUNSUPPORTED;
+}
+
+int tq_decode_path(const tq_plan* p) {
+  if (!p) return TQ_EINVAL;
+  return tq::decode_tc_supported(p) ? TQ_PATH_TENSOR_D128 : TQ_PATH_CUDA_CORE;
 }
 
 int tq_encode_path(const tq_plan* p, tq_dtype dt) {
@@ -335,6 +364,7 @@ tq_status tq_decode(const tq_plan* p, const void* packed, int64_t G, int64_t N, 
   if (!packed || !out) return TQ_EINVAL;
   if (!aligned16(packed) || !aligned16(out)) return TQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (decode_tc_supported(p)) return from_cuda(launch_decode_tc(p, static_cast<const uint8_t*>(packed), G, N, out, s));
   return from_cuda(launch_decode_simt(p, static_cast<const uint8_t*>(packed), G, N, out, s));
 }
 

@@ -72,8 +72,10 @@ struct tq_plan {
   uint16_t* wide_ops;  // row-major fp16 [4][d][d]: (2^8 Pi) hi, lo; (PROD) M hi, lo
   void* wide_scratch;  // (PROD) residual rows of the wide encode: [wide_slots][2][128][d] bf16
   int wide_slots;      // SM ids of the device (%nsmid)
-  uint8_t* tc_ops;    // tensor-core operand images (d = 128): Pi hi/lo fp16,
-                      // Pi hi/lo bf16, (PROD) M hi/lo bf16; 32 KB each, K-major 128-byte swizzle
+  uint8_t* tc_ops;    // tensor-core operand images (d = 128), 32 KB each, K-major
+                      // 128-byte swizzle: Pi hi/lo fp16, Pi hi/lo bf16, (PROD) M hi/lo
+                      // bf16; then for decode 2^8 Pi^T hi/lo and (PROD) 2^8 S^T hi/lo, fp16
+  uint32_t dec_ctab[16];  // decode: fp16 bits of hi (low half) and lo (high half) of 2^8 c_i
   int* err;           // device error word
 };
 
@@ -88,6 +90,11 @@ cudaError_t launch_topk(const float* logits, int64_t rows, int64_t N, int k, flo
                         int64_t* top_idx, void* ws, cudaStream_t s);
 cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
                                cudaStream_t s);
+bool decode_tc_supported(const tq_plan* p);
+cudaError_t launch_decode_tc(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
+                             cudaStream_t s);
+// index of decode image j in tc_ops (0, 1: Pi^T hi, lo; 2, 3: S^T hi, lo)
+inline int tc_dec_image(const tq_plan* p, int j) { return (p->lay.prod ? 6 : 4) + j; }
 cudaError_t launch_score_fp32(const float* q, const float* x, int64_t G, int H, int64_t N, int d,
                               float* logits, cudaStream_t s);
 cudaError_t launch_wait_expiry(int* err, cudaStream_t s);
