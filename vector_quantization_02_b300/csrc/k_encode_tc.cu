@@ -2,8 +2,8 @@
 // fp16 or bf16 keys, TurboQuantProd; TurboQuantMSE ("turboquant-pytorch 소개",
 // "1단계" alone) runs E1-E3 and E6 only, with up to 16 levels and rho = 0.
 //
-// Same computation as the CUDA-core encode ("turboquant-pytorch 소개",
-// "1단계" then "2단계"): y = Pi x, codes idx_j = #{i : n t_i < y_j},
+// The computation ("turboquant-pytorch 소개", "1단계" then "2단계"):
+// y = Pi x, codes idx_j = #{i : n t_i < y_j},
 // r = y - n c[idx] (rotated frame, unnormalised), rho = ||r||,
 // z = [M r >= 0] with M = S Pi^T, so that sign(M r) = sign(S (x - n Pi^T c[idx])).
 //
