@@ -148,7 +148,7 @@ def max_over_ranks(world, v: float) -> float:
 
 # ---------------------------------------------------------------- oracle timing (CPU)
 
-def oracle_throughput(w, bits, budget_s: float):
+def oracle_throughput(w, bits, mode: str, budget_s: float):
     """Time the oracle (encode + score of one group's keys against H heads) on a
     bounded sample; returns (keys/s, sample description, threads)."""
     import numpy as np
@@ -156,15 +156,15 @@ def oracle_throughput(w, bits, budget_s: float):
     from oracle import tq_oracle as o
     d = w.d
     Pi = o.haar_rotation(tq_synth.rotation_gaussian(d, w.seeds["rotation"]).numpy()).astype(np.float32)
-    S = tq_synth.projection(d, w.seeds["projection"]).numpy()
-    c = o.codebook_f32(1 << (bits - 1), d)
+    S = tq_synth.projection(d, w.seeds["projection"]).numpy() if mode == "prod" else None
+    c = o.codebook_f32(1 << (bits - 1 if mode == "prod" else bits), d)
     q = tq_synth.queries(w, G=1).numpy()
 
     def run(n):
         keys = tq_synth.keys(w, G=1, N=n)
         t0 = time.perf_counter()
-        buf, _ = o.encode_pack(keys.double().numpy(), Pi, S, c, bits, "prod", 1, n)
-        o.score_packed(q, buf, Pi, S, c, bits, "prod", 1, n)
+        buf, _ = o.encode_pack(keys.double().numpy(), Pi, S, c, bits, mode, 1, n)
+        o.score_packed(q, buf, Pi, S, c, bits, mode, 1, n)
         return time.perf_counter() - t0
 
     n = 256
@@ -178,6 +178,12 @@ def oracle_throughput(w, bits, budget_s: float):
     except ImportError:
         threads = len(os.sched_getaffinity(0))
     return n / t, f"encode+score of {n} keys of group 0 against its {w.H} heads (numpy fp64)", threads
+
+
+def workload_config(w, mode: str, bits: int) -> dict:
+    """The workload as both arms report it."""
+    return {"workload": w.name, "mode": mode, "G": w.G, "N": w.N, "H": w.H, "d": w.d, "bits": bits,
+            "key_dtype": str(w.key_dtype).replace("torch.", ""), "top_k": w.top_k}
 
 
 # ---------------------------------------------------------------- our path
@@ -411,9 +417,8 @@ def run_ours(args, world, rank):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_desc,
         "data": "synthetic",
-        "config": {"workload": w.name, "mode": args.mode, "G": G, "N": N, "H": H, "d": d, "bits": bits,
-                   "key_dtype": str(w.key_dtype).replace("torch.", ""), "top_k": top_k,
-                   "l2": "flushed between steps (2x L2 memset, outside the step events)"},
+        "config": dict(workload_config(w, args.mode, bits),
+                       l2="flushed between steps (2x L2 memset, outside the step events)"),
         "roofline": enc_roof,
         "parts": {
             "encode": {"ms": round(enc_ms, 5), "vectors_per_s": G * N / (enc_ms * 1e-3), "roofline": enc_roof},
@@ -431,7 +436,7 @@ def run_ours(args, world, rank):
         "wall_s_timed_region": round(wall, 4),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        v, sample, cores = oracle_throughput(w, bits, args.cpu_budget)
+        v, sample, cores = oracle_throughput(w, bits, args.mode, args.cpu_budget)
         line["cpu_baseline"] = {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample}
     plan.close()
     return line
@@ -445,14 +450,14 @@ def run_reference(args, world, rank):
     vals = []
     sample = cores = None
     for _ in range(args.warmup + args.steps):
-        v, sample, cores = oracle_throughput(w, bits, args.cpu_budget / max(1, args.steps + args.warmup))
+        v, sample, cores = oracle_throughput(w, bits, args.mode, args.cpu_budget / max(1, args.steps + args.warmup))
         vals.append(v)
     v = statistics.median(vals[args.warmup:]) if len(vals) > args.warmup else vals[-1]
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "G": w.G, "N": w.N, "H": w.H, "d": w.d, "bits": bits},
+        "config": workload_config(w, args.mode, bits),
         "cpu_baseline": {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -82,3 +82,13 @@ def test_committed_traffic_entries_name_existing_summaries():
             continue
         assert os.path.exists(os.path.join(ROOT, v["summary"])), v["summary"]
         assert v["dram_bytes_per_launch"] > 0 and v["workload"] in tq_synth.WORKLOADS
+
+
+def test_both_bench_arms_report_the_same_workload_config():
+    w = tq_synth.WORKLOADS["vector_search_1m"]
+    c = bench.workload_config(w, "mse", 4)
+    assert c == {"workload": w.name, "mode": "mse", "G": w.G, "N": w.N, "H": w.H, "d": w.d, "bits": 4,
+                 "key_dtype": "float32", "top_k": w.top_k}
+    # the reference arm prints exactly this dict; ours adds only how L2 was handled
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert src.count("workload_config(w, args.mode, bits)") == 2
