@@ -1,5 +1,7 @@
 // The C ABI of libtq.so: argument checks, plan lifetime, dispatch.
 // Declarations, layouts and error behaviour are documented in include/tq.h.
+#include <cuda.h>
+
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -7,6 +9,7 @@
 #include <type_traits>
 #include <vector>
 
+#include "ptx_sm100.cuh"
 #include "tq_internal.cuh"
 
 using namespace tq;
@@ -140,6 +143,38 @@ cudaError_t build_tc_ops(tq_plan* p) {
 }  // namespace
 
 namespace tq {
+
+// ---- tensor maps (host): cuTensorMapEncodeTiled through the runtime's
+// driver entry point, looked up once (thread-safe static initialisation)
+using EncodeTmapFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTmapFn tmap_encoder() {
+  static const EncodeTmapFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<EncodeTmapFn>(p);
+    return static_cast<EncodeTmapFn>(nullptr);
+  }();
+  return fn;
+}
+
+cudaError_t make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                         uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTmapFn enc = tmap_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 // Workspace: [tensor-core query images and constants | Pi q, S q] [top-k candidates]
 size_t score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k) {
