@@ -65,6 +65,11 @@ def test_argument_errors_need_no_gpu():
     assert lib.tq_lloyd_max_codebook(3, 128, vp(16)) == -1
     assert lib.tq_haar_rotation(0, vp(16), vp(16)) == -1
     assert lib.tq_plan_status(None) == -1
+    # path queries and the self-test reject a null plan
+    assert lib.tq_score_path(None, 8) == -1
+    assert lib.tq_encode_path(None, 1) == -1
+    assert lib.tq_decode_path(None) == -1
+    assert lib.tq_selftest_wait_expiry(None, None) == -1
 
 
 @pytest.mark.parametrize("levels", [2, 4, 8, 16])
