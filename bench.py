@@ -8,9 +8,12 @@ One step = tq_encode of every key of the workload (E0-E6) + tq_score of one
 query per head against all of them (S0-S4).  The default workload is the
 Qwen2.5-3B-shaped decode step (72 groups x 8,192 fp16 keys, 8 query heads per
 group, d = 128, 3 bits).  The value is keys encoded-and-scored per second over
-the whole step; per-kernel numbers, rooflines, the fp32-key baseline, an
-end-to-end run from pinned host memory and the CPU oracle are reported beside
-it in the same JSON line.  Multi-GPU runs (torchrun) are replicas: every rank
+the whole step; the score-only and encode-only rates (``headline``),
+per-kernel numbers, rooflines, the fp32-key baseline, an end-to-end run from
+pinned host memory and the CPU oracle are reported beside it in the same JSON
+line.  With the default workload the line also carries a score-only leg on the
+other 3-bit d = 128 shape, the Llama-3.1-8B-shaped cache (4,096 groups x 32,768
+bf16 keys, 4 heads per group), under ``parts.score_llama31_b3``.  Multi-GPU runs (torchrun) are replicas: every rank
 runs the full workload on its own GPU (weak scaling), no collective on the
 data path.
 """
@@ -34,6 +37,7 @@ sys.path.insert(0, ROOT)
 import tq_synth  # noqa: E402
 
 METRIC = "tq_score keys scored/s & % HBM roofline at 3-bit d=128; tq_encode vectors/s"
+DEFAULT_WORKLOAD = "qwen25_3b_decode"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 SPIN_CYCLES_PER_US = 2100  # at or above the maximum SM clock, so a spin lasts at least as long as asked
@@ -188,6 +192,79 @@ def workload_config(w, mode: str, bits: int) -> dict:
 
 # ---------------------------------------------------------------- our path
 
+def roofline(bytes_, ms, kernel, source, workload, flops=None):
+    """HBM roofline, or the bf16 tensor roofline where the algorithmic flops
+    at that peak take longer than the bytes at HBM speed."""
+    pk, pk_kind = peaks()
+    hbm = pk["hbm_gbs"]
+    tflops_peak = pk.get("bf16_tflops", FALLBACK_PEAKS.get("bf16_tflops"))
+    ach = bytes_ / (ms * 1e-3) / 1e9
+    tensor = flops is not None and flops / (tflops_peak * 1e12) > bytes_ / (hbm * 1e9)
+    if tensor:
+        tf = flops / (ms * 1e-3) / 1e12
+        r = {"bound": "tensor", "achieved": round(tf, 2), "peak": tflops_peak, "unit": "TFLOP/s",
+             "frac": round(tf / tflops_peak, 4)}
+    else:
+        r = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4)}
+    r.update({"traffic": kernel_traffic(kernel, source, workload), "algorithmic_bytes": bytes_,
+              "peak_source": pk_kind, "kernel": kernel})
+    if flops is not None:
+        r["algorithmic_flops"] = flops
+        r["tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
+        r["gbs"] = round(ach, 1)
+    return r
+
+
+def score_only_leg(name: str, bits: int, flush, reps: int, dev, lead):
+    """tq_score alone on a second workload, cold L2: the keys are encoded once,
+    64 groups at a time (untimed), then one query per head is scored against
+    every packed key.  Returns the leg's report."""
+    import vector_quantization_02_b300 as tq
+    w = tq_synth.WORKLOADS[name]
+    G, N, H, d = w.G, w.N, w.H, w.d
+    plan = tq.Plan.from_seeds(d, bits, tq_synth.rotation_gaussian(d, w.seeds["rotation"]),
+                              tq_synth.projection(d, w.seeds["projection"]))
+    per_group = plan.packed_bytes(1, N)
+    packed = torch.empty(plan.packed_bytes(G, N), dtype=torch.uint8, device=dev)
+    chunks = -(-G // tq_synth.KEY_CHUNK_GROUPS)
+    for c in range(chunks):
+        kc = tq_synth.key_chunk(w, c, device=dev)
+        g0 = c * tq_synth.KEY_CHUNK_GROUPS
+        tq.tq_encode(plan, kc, packed=packed[g0 * per_group:(g0 + kc.shape[0]) * per_group])
+        del kc
+    q = tq_synth.queries(w, device=dev)
+    logits = torch.empty(G, H, N, dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.score_workspace_bytes(plan, G, H, N), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(2):
+        tq.tq_score(plan, q, packed, N, logits=logits, workspace=ws)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        lead(300)
+        a, b = ev(), ev()
+        a.record(stream)
+        tq.tq_score(plan, q, packed, N, logits=logits, workspace=ws)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    ms = statistics.median(a.elapsed_time(b) for a, b in times)
+    P = plan.packed_bytes(G, N)
+    sk = {"tensor_d128": ("score_tc", "k_score_tc.cu"), "tensor_wide": ("score_wide", "k_score_wide.cu")}
+    kern, src = sk[plan.score_path(H)]
+    out = {"workload": name, "bits": bits, "G": G, "N": N, "H": H, "d": d,
+           "key_dtype": str(w.key_dtype).replace("torch.", ""), "ms_cold_l2": round(ms, 5),
+           "keys_per_s_cold_l2": G * N / (ms * 1e-3), "logits_per_s_cold_l2": G * N * H / (ms * 1e-3),
+           "roofline_cold_l2": roofline(P + G * H * N * 4 + q.numel() * 4, ms, kern, src, name,
+                                        flops=2 * 2 * d * H * G * N),
+           "launches": 2, "reps": reps}
+    plan.close()
+    del packed, logits, ws
+    torch.cuda.empty_cache()
+    return out
+
 def _e2e(args, world, plan, keys, q, packed, logits, ws, flush, top_k, stream, ev):
     """Median step time with the inputs copied from pinned host memory and the
     logits copied back inside the timed events."""
@@ -231,7 +308,6 @@ def run_ours(args, world, rank):
     bits = args.bits or w.bits[0]
     dev = torch.device("cuda", torch.cuda.current_device())
     G, N, H, d = w.G, w.N, w.H, w.d
-    pk, pk_kind = peaks()
 
     keys = tq_synth.keys(w, device=dev, seed_offset=rank)
     q = tq_synth.queries(w, device=dev, seed_offset=rank)
@@ -309,28 +385,9 @@ def run_ours(args, world, rank):
     q_bytes = q.numel() * 4
     enc_bytes = key_bytes + P
     sc_bytes = P + logit_bytes + q_bytes
-    hbm = pk["hbm_gbs"]
-
-    tflops_peak = pk.get("bf16_tflops", FALLBACK_PEAKS.get("bf16_tflops"))
 
     def roof(bytes_, ms, kernel, source, flops=None):
-        """HBM roofline, or the bf16 tensor roofline where the algorithmic flops
-        at that peak take longer than the bytes at HBM speed."""
-        ach = bytes_ / (ms * 1e-3) / 1e9
-        tensor = flops is not None and flops / (tflops_peak * 1e12) > bytes_ / (hbm * 1e9)
-        if tensor:
-            tf = flops / (ms * 1e-3) / 1e12
-            r = {"bound": "tensor", "achieved": round(tf, 2), "peak": tflops_peak, "unit": "TFLOP/s",
-                 "frac": round(tf / tflops_peak, 4)}
-        else:
-            r = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4)}
-        r.update({"traffic": kernel_traffic(kernel, source, w.name), "algorithmic_bytes": bytes_,
-                  "peak_source": pk_kind, "kernel": kernel})
-        if flops is not None:
-            r["algorithmic_flops"] = flops
-            r["tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
-            r["gbs"] = round(ach, 1)
-        return r
+        return roofline(bytes_, ms, kernel, source, w.name, flops=flops)
 
     kernels = {"tensor_d128": ("{}_tc", "k_{}_tc.cu"), "tensor_wide": ("{}_wide", "k_{}_wide.cu")}
     ek, es = kernels[plan.encode_path(w.key_dtype)]
@@ -417,8 +474,14 @@ def run_ours(args, world, rank):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_desc,
         "data": "synthetic",
-        "config": dict(workload_config(w, args.mode, bits),
-                       l2="flushed between steps (2x L2 memset, outside the step events)"),
+        "config": workload_config(w, args.mode, bits),
+        "l2": "flushed between steps (2x L2 memset, outside the step events)",
+        "headline": {
+            "step_keys_per_s": value,
+            "score_keys_per_s_cold_l2": G * N / (sc_cold_ms * 1e-3), "score_hbm_frac": sc_roof["frac"],
+            "encode_vectors_per_s": G * N / (enc_ms * 1e-3), "encode_roofline_frac": enc_roof["frac"],
+            "note": "value = keys encoded and scored per second over the whole step (encode + score); the "
+                    "score-only and encode-only rates are given here and under parts"},
         "roofline": enc_roof,
         "parts": {
             "encode": {"ms": round(enc_ms, 5), "vectors_per_s": G * N / (enc_ms * 1e-3), "roofline": enc_roof},
@@ -435,10 +498,16 @@ def run_ours(args, world, rank):
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }
+    plan.close()
+    if args.second_leg and args.workload == DEFAULT_WORKLOAD and args.mode == "prod" and not args.tokens:
+        # the other 3-bit d = 128 headline shape: score alone on the Llama-3.1-8B cache
+        del keys, packed, logits, ws
+        torch.cuda.empty_cache()
+        line["parts"]["score_llama31_b3"] = score_only_leg("llama31_8b_prefill", 3, flush, max(5, args.steps), dev,
+                                                           lead)
     if rank == 0 and not args.no_cpu_baseline:
         v, sample, cores = oracle_throughput(w, bits, args.mode, args.cpu_budget)
         line["cpu_baseline"] = {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample}
-    plan.close()
     return line
 
 
@@ -469,7 +538,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen25_3b_decode", choices=sorted(tq_synth.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(tq_synth.WORKLOADS))
     ap.add_argument("--bits", type=int, default=0)
     ap.add_argument("--mode", choices=["prod", "mse"], default="prod",
                     help="TurboQuantProd (the workloads' method) or TurboQuantMSE codec")
@@ -477,6 +546,8 @@ def main():
                     help="cap the tokens per group (a reduced case for profiling; not a bench configuration)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-second-leg", dest="second_leg", action="store_false",
+                    help="skip the score-only leg on the Llama-3.1-8B-shaped cache at 3 bits")
     ap.add_argument("--soak-s", type=float, default=1.5,
                     help="seconds (from the start of the timed region) the step keeps running while clocks are sampled")
     args = ap.parse_args()

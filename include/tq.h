@@ -170,7 +170,10 @@ tq_status tq_score(const tq_plan* plan, const float* queries, int64_t n_groups, 
  *    TQ_EUNSUPPORTED and enqueue nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept per CUDA context: after
+ *    cudaDeviceReset (which frees the array with the context; plans made
+ *    before it are invalid too) or under another context, the next call looks
+ *    it up again, so that call should likewise come before any capture.
  *  - Every call shares the one array: calls whose work overlaps on the GPU
  *    (several streams or threads) race and must be serialised by the caller.
  *    The array keeps the last call's contents; nothing in it needs clearing.

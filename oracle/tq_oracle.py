@@ -337,6 +337,54 @@ def unpack(buf, d: int, bits: int, mode: str, G: int, N: int) -> dict:
                 n=n[:, :N].reshape(G * N), rho=rho[:, :N].reshape(G * N))
 
 
+def unpack_blocks(buf, d: int, bits: int, mode: str, n_blocks: int) -> dict:
+    """The same layout as ``unpack``, read for whole 128-token blocks at once
+    (numpy's little-endian bit order within each 16-byte chunk is exactly
+    "coordinate 128c + 32w + i is bit i of little-endian word w").  Returns
+    idx [n_blocks*128][d] (uint8), z [n_blocks*128][d] (bool), n, rho (fp64);
+    padded tokens included.  Used where ``unpack``'s per-block loop is too
+    slow (a million keys)."""
+    k, planes = plane_count(bits, mode)
+    T = TOKENS_PER_BLOCK
+    C = d // CHUNK_COORDS
+    bb = block_bytes(d, bits, mode)
+    buf = np.asarray(buf, dtype=np.uint8).reshape(n_blocks, bb)
+    plane_bytes = planes * C * T * 16
+    chunks = buf[:, :plane_bytes].reshape(n_blocks, planes, C, T, 16)
+    bits_arr = np.unpackbits(chunks, axis=-1, bitorder="little")            # [B][planes][C][T][128]
+    bits_arr = bits_arr.transpose(0, 3, 1, 2, 4).reshape(n_blocks * T, planes, d)
+    idx = np.zeros((n_blocks * T, d), dtype=np.uint8)
+    for p in range(k):
+        idx |= bits_arr[:, p, :] << p
+    z = bits_arr[:, k, :].astype(bool) if mode == "prod" else np.zeros((n_blocks * T, d), dtype=bool)
+    nr = np.ascontiguousarray(buf[:, plane_bytes:]).view("<f4").reshape(n_blocks * T, 2).astype(np.float64)
+    return dict(idx=idx, z=z, n=nr[:, 0], rho=nr[:, 1])
+
+
+def score_prod_rotated(q, idx, z, n, rho, Pi, S, c) -> np.ndarray:
+    """The estimator of ``score_prod`` evaluated in the rotated frame,
+    n <Pi q, c[idx]> + rho sqrt(pi/2)/m <S q, 2z - 1>, which equals it for an
+    orthogonal Pi (<q, n Pi^T c[idx]> = n <Pi q, c[idx]>).  With the fp32 Pi
+    the two differ by Pi's non-orthogonality (about 1e-7 relative).  It costs
+    O(H d) per key instead of O(d^2), for scoring a million keys.
+    q [H][d] -> logits [H][N]."""
+    q = _as64(q)
+    S = _as64(S)
+    m = S.shape[0]
+    qr = q @ _as64(Pi).T                          # [H][d]: Pi q per query
+    sq = q @ S.T                                  # [H][m]: S q per query
+    ytil = _as64(c)[np.asarray(idx)]              # [N][d]
+    return (_as64(n)[None, :] * (qr @ ytil.T) +
+            (_as64(rho)[None, :] * (KAPPA_NUM / m)) * (sq @ qjl_vector(z).T))
+
+
+def score_mse_rotated(q, idx, n, Pi, c) -> np.ndarray:
+    """``score_mse`` in the rotated frame, n <Pi q, c[idx]> (see
+    ``score_prod_rotated``).  q [H][d] -> logits [H][N]."""
+    qr = _as64(q) @ _as64(Pi).T
+    return _as64(n)[None, :] * (qr @ _as64(c)[np.asarray(idx)].T)
+
+
 # ----------------------------------------------------------------------------
 # Whole-path helpers the tests and the CPU baseline use
 # ----------------------------------------------------------------------------

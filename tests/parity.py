@@ -22,21 +22,26 @@ from oracle import tq_oracle as o
 
 
 class Inputs:
-    """Plan inputs for both sides from one set of seeded draws: the GPU plan is
-    built by the library's own host helpers, the oracle builds its own."""
+    """Plan inputs for both sides from one set of seeded draws.
+
+    The oracle builds the rotation (LAPACK QR of the seeded Gaussian) and the
+    fp32 codebook; the GPU plan is built from exactly those fp32 values, so
+    both sides compute on identical Pi, S and centroids.  The library's own
+    host helpers (tq_haar_rotation, tq_lloyd_max_codebook) are pinned against
+    the oracle separately, on the CPU."""
 
     def __init__(self, d, bits, mode, rot_seed, proj_seed):
         self.d, self.bits, self.mode = d, bits, mode
         self.k = bits - 1 if mode == "prod" else bits
         self.G_rot = tq_synth.rotation_gaussian(d, rot_seed)
         self.S = tq_synth.projection(d, proj_seed)
-        self.Pi_o = o.haar_rotation(self.G_rot.numpy()).astype(np.float32)
+        self.Pi_o = np.ascontiguousarray(o.haar_rotation(self.G_rot.numpy()).astype(np.float32))
         self.c_o = o.codebook_f32(1 << self.k, d)
         self.S_o = self.S.numpy()
 
     def plan(self):
-        return tq.Plan.from_seeds(self.d, self.bits, self.G_rot, self.S if self.mode == "prod" else None,
-                                  mode=self.mode)
+        return tq.Plan(self.d, self.bits, torch.from_numpy(self.Pi_o), self.S if self.mode == "prod" else None,
+                       torch.from_numpy(self.c_o.copy()), mode=self.mode)
 
 
 def oracle_encode(inp: Inputs, keys: torch.Tensor):
@@ -45,15 +50,20 @@ def oracle_encode(inp: Inputs, keys: torch.Tensor):
     return o.encode_pack(keys.detach().cpu().double().numpy(), inp.Pi_o, inp.S_o, inp.c_o, inp.bits, inp.mode, G, N)
 
 
-def compare_fields(inp: Inputs, got: dict, e: dict, x: np.ndarray) -> dict:
+def compare_fields(inp: Inputs, got: dict, e: dict, x: np.ndarray, pool: dict | None = None) -> dict:
     """Assert the GPU's per-key fields (idx, z, n, rho of keys ``x`` [n][d],
     fp64) agree with the oracle's encoding ``e`` of the same keys.
 
     A coordinate within 1e-5 of a boundary may take either neighbouring code;
     the key's residual, rho and signs then follow the code taken, so such a key
     is compared against the oracle's own encoding with that boundary resolved
-    the other way (``qjl_stage`` on the alternative codes)."""
-    total = x.size
+    the other way (``qjl_stage`` on the alternative codes).
+
+    The mismatch rate is over every compared value (code coordinates, and sign
+    bits in Prod).  With ``pool`` given, the counts are added to it and the
+    rate is asserted later on the pooled total (``assert_pooled_rate``);
+    otherwise it is asserted here."""
+    total = x.size * (2 if inp.mode == "prod" else 1)
     code_bad = got["idx"] != e["idx"]
     assert not np.any(code_bad & ~e["code_exempt"]), "code mismatch outside the boundary band"
     # a flipped code must be the neighbour across the near boundary
@@ -80,12 +90,27 @@ def compare_fields(inp: Inputs, got: dict, e: dict, x: np.ndarray) -> dict:
         assert np.all(np.abs(got["rho"] - rho_ref.astype(np.float32)) <= 1e-5 * n + 1e-30), "residual norm mismatch"
     else:
         assert np.all(got["rho"] == 0)
-    # the rate can only be resolved on large samples: below 10^6 coordinates a
-    # couple of band-exempt flips are allowed, above it the rate must be <= 1e-5
+    stats["mismatches"] = mism
+    stats["compared"] = total
+    if pool is not None:
+        pool["mismatches"] = pool.get("mismatches", 0) + mism
+        pool["compared"] = pool.get("compared", 0) + total
+        return stats
+    # the rate can only be resolved on large samples: below 10^6 compared
+    # values a couple of band-exempt flips are allowed, above it the rate must
+    # be <= 1e-5
     assert mism <= max(1e-5 * total, 2 if total < 10 ** 6 else 0), \
         f"mismatch rate {mism / total:.2e} above 1e-5 ({mism} of {total})"
-    stats["mismatches"] = mism
     return stats
+
+
+def assert_pooled_rate(pool: dict, min_compared: int = 10 ** 6) -> float:
+    """The band-exempt mismatch rate over a pooled sample of at least
+    ``min_compared`` values is at most 1e-5."""
+    total, mism = pool["compared"], pool["mismatches"]
+    assert total >= min_compared, f"pooled sample too small to resolve a 1e-5 rate ({total})"
+    assert mism <= 1e-5 * total, f"pooled mismatch rate {mism / total:.2e} above 1e-5 ({mism} of {total})"
+    return mism / total
 
 
 def compare_encode(inp: Inputs, gpu_bytes: np.ndarray, keys: torch.Tensor, check_bytes=True) -> dict:
@@ -121,3 +146,33 @@ def compare_logits(got: np.ndarray, want: np.ndarray, q: torch.Tensor, n: np.nda
     err = np.abs(got.astype(np.float64) - want)
     assert np.all(err <= bound + 1e-30), f"max err/bound {np.max(err / (bound + 1e-30)):.3g}"
     return float(np.max(err / (bound + 1e-30)))
+
+
+def oracle_logits_of_packed(inp: Inputs, packed: np.ndarray, q: np.ndarray, G: int, N: int) -> np.ndarray:
+    """The oracle's logits [G][H][N] (fp64) for packed bytes (identical packed
+    input: whatever the bytes hold is scored), through ``score_prod`` /
+    ``score_mse`` on the fields ``unpack_blocks`` reads."""
+    nb = -(-N // 128)
+    u = o.unpack_blocks(packed, inp.d, inp.bits, inp.mode, G * nb)
+    out = np.empty((G, q.shape[1], N))
+    for g in range(G):
+        r = slice(g * nb * 128, g * nb * 128 + N)
+        if inp.mode == "prod":
+            out[g] = o.score_prod(q[g], u["idx"][r], u["z"][r], u["n"][r], u["rho"][r], inp.Pi_o, inp.S_o, inp.c_o)
+        else:
+            out[g] = o.score_mse(q[g], u["idx"][r], u["n"][r], inp.Pi_o, inp.c_o)
+    return out
+
+
+def check_topk_against_oracle(top_s: np.ndarray, top_i: np.ndarray, oracle_at: np.ndarray, kth_best: np.ndarray,
+                              qn: np.ndarray, n_at: np.ndarray, tol=1e-4):
+    """Top-k validity: every returned key's oracle score is at least the
+    oracle's k-th best score minus tol ||q|| n, and the returned score is the
+    oracle's within tol ||q|| n.  Rows are (group, head); ``oracle_at`` holds
+    the oracle's scores at the returned indices, ``n_at`` those keys' norms."""
+    bound = tol * qn[:, None] * n_at
+    assert np.all(oracle_at >= kth_best[:, None] - bound), "a returned key is not among the oracle's top k"
+    assert np.all(np.abs(top_s.astype(np.float64) - oracle_at) <= bound), "returned scores disagree with the oracle"
+    assert np.all(np.diff(top_s, axis=-1) <= 0), "top-k scores not in descending order"
+    for r in range(top_i.shape[0]):
+        assert np.unique(top_i[r]).size == top_i.shape[1], "repeated index in a top-k row"

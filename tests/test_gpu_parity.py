@@ -8,7 +8,8 @@ import tq_synth
 import vector_quantization_02_b300 as tq
 from oracle import tq_oracle as o
 
-from parity import Inputs, compare_encode, compare_logits, oracle_encode
+from parity import (Inputs, check_topk_against_oracle, compare_encode, compare_logits, oracle_encode,
+                    oracle_logits_of_packed)
 
 pytestmark = pytest.mark.gpu
 
@@ -136,9 +137,19 @@ def test_score_top_k(cuda, d, G, N, H, k):
     logits, ts, ti = tq.tq_score(plan, q.to(cuda), packed, N, top_k=k)
     torch.cuda.synchronize()
     L = logits.cpu().numpy()
+    ts, ti = ts.cpu().numpy(), ti.cpu().numpy()
+    # exact selection on the GPU's own logits
     want_s, want_i = o.topk(L, k)
-    assert np.array_equal(ti.cpu().numpy(), want_i)
-    assert np.array_equal(ts.cpu().numpy(), want_s)
+    assert np.array_equal(ti, want_i)
+    assert np.array_equal(ts, want_s)
+    # valid against the oracle's scores of the same packed keys
+    ol = oracle_logits_of_packed(inp, packed.cpu().numpy(), q.numpy().astype(np.float64), G, N).reshape(G * H, N)
+    kth = np.sort(ol, axis=1)[:, -k]
+    ti2, ts2 = ti.reshape(G * H, k), ts.reshape(G * H, k)
+    at = np.take_along_axis(ol, ti2, axis=1)
+    n_all = np.repeat(o.unpack(packed.cpu().numpy(), d, 4, "prod", G, N)["n"].reshape(G, 1, N), H, axis=1)
+    n_at = np.take_along_axis(n_all.reshape(G * H, N), ti2, axis=1)
+    check_topk_against_oracle(ts2, ti2, at, kth, np.linalg.norm(q.double().numpy(), axis=-1).reshape(-1), n_at)
 
 
 @pytest.mark.parametrize("d,G,N,bits,mode", [

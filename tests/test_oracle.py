@@ -388,3 +388,55 @@ def test_packed_bytes_per_key_and_footprint():
     assert abs(fp16_mib - g["kv_cache_fp16_mb_qwen25_3b_8k"]) / 289 < 0.01
     # 3-bit payload (48 B) + two fp16 norms (4 B) per vector reproduces 58 MB
     assert abs(vectors * (3 * 128 / 8 + 4) / 2 ** 20 - g["kv_cache_3bit_mb_qwen25_3b_8k"]) / 58 < 0.02
+
+
+@pytest.mark.parametrize("bits,mode,d", [(3, "prod", 128), (4, "prod", 256), (4, "mse", 128)])
+def test_unpack_blocks_reads_the_same_layout(bits, mode, d):
+    # the vectorised reader agrees with unpack (itself pinned to hand-computed
+    # bit addresses above) on every token, padding included
+    G, N = 2, 300
+    rng = _rng(34)
+    k, _ = o.plane_count(bits, mode)
+    idx = rng.integers(0, 1 << k, size=(G * N, d))
+    z = rng.integers(0, 2, size=(G * N, d)).astype(bool)
+    n = rng.random(G * N).astype(np.float32)
+    rho = rng.random(G * N).astype(np.float32)
+    buf = o.pack(idx, z, n, rho, d, bits, mode, G, N)
+    nb = 3
+    b = o.unpack_blocks(buf, d, bits, mode, G * nb)
+    u = o.unpack(buf, d, bits, mode, G, N)
+    rows = np.concatenate([g * nb * 128 + np.arange(N) for g in range(G)])
+    assert np.array_equal(b["idx"][rows].astype(np.int64), u["idx"])
+    assert np.array_equal(b["n"][rows], u["n"])
+    if mode == "prod":
+        assert np.array_equal(b["z"][rows], u["z"])
+        assert np.array_equal(b["rho"][rows], u["rho"])
+    pad = np.setdiff1d(np.arange(G * nb * 128), rows)
+    assert not b["idx"][pad].any() and not b["z"][pad].any() and not b["n"][pad].any()
+
+
+def test_score_in_the_rotated_frame_equals_score_prod():
+    d = 128
+    rng = _rng(35)
+    S = rng.standard_normal((d, d)).astype(np.float32)
+    c = o.codebook_f32(4, d)
+    x = rng.standard_normal((50, d))
+    q = rng.standard_normal((3, d))
+    # fp64 Haar rotation: the identity <q, n Pi^T c> = n <Pi q, c> holds to rounding
+    Pi = _haar(d, 36)
+    e = o.encode_prod(x, Pi, S, c)
+    a = o.score_prod(q, e["idx"], e["z"], e["n"], e["rho"], Pi, S, c)
+    b = o.score_prod_rotated(q, e["idx"], e["z"], e["n"], e["rho"], Pi, S, c)
+    assert np.max(np.abs(a - b)) <= 1e-12 * np.max(np.abs(a))
+    # fp32 rotation: within its non-orthogonality
+    Pi32 = Pi.astype(np.float32)
+    e = o.encode_prod(x, Pi32, S, c)
+    a = o.score_prod(q, e["idx"], e["z"], e["n"], e["rho"], Pi32, S, c)
+    b = o.score_prod_rotated(q, e["idx"], e["z"], e["n"], e["rho"], Pi32, S, c)
+    bound = 1e-6 * np.linalg.norm(q, axis=1)[:, None] * e["n"][None, :]
+    assert np.all(np.abs(a - b) <= bound)
+    # the MSE-only estimate likewise
+    m = o.encode_mse(x, Pi, c)
+    a = o.score_mse(q, m["idx"], m["n"], Pi, c)
+    b = o.score_mse_rotated(q, m["idx"], m["n"], Pi, c)
+    assert np.max(np.abs(a - b)) <= 1e-12 * np.max(np.abs(a))

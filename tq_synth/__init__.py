@@ -39,7 +39,7 @@ import dataclasses
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "gaussian", "rotation_gaussian", "projection",
-           "channel_scales", "keys", "queries", "small_case"]
+           "channel_scales", "keys", "key_chunk", "queries", "small_case"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -149,20 +149,28 @@ def keys(w: Workload, G: int | None = None, N: int | None = None, device="cpu",
     G = w.G if G is None else G
     N = w.N if N is None else N
     out = torch.empty((G, N, w.d), dtype=w.key_dtype, device=device)
-    sc = None
-    if w.outliers and not w.unit_keys:
-        sc = channel_scales(w).to(device)[_group_scale_index(w, G).to(device)]
     for c0 in range(0, G, KEY_CHUNK_GROUPS):
         c1 = min(G, c0 + KEY_CHUNK_GROUPS)
-        seed = 1_000_003 * w.seeds["keys"] + c0 // KEY_CHUNK_GROUPS + seed_offset
-        z = gaussian((c1 - c0, N, w.d), seed, torch.float32, device)
-        if w.unit_keys:
-            z /= torch.linalg.vector_norm(z, dim=-1, keepdim=True)
-        elif sc is not None:
-            z *= sc[c0:c1, None, :]
-        out[c0:c1] = z.to(w.key_dtype)
-        del z
+        out[c0:c1] = key_chunk(w, c0 // KEY_CHUNK_GROUPS, G, N, device, seed_offset)
     return out
+
+
+def key_chunk(w: Workload, chunk: int, G: int | None = None, N: int | None = None, device="cpu",
+              seed_offset: int = 0) -> torch.Tensor:
+    """Groups [64 chunk, 64 chunk + 64) of ``keys(w, G, N)``, drawn alone (the
+    same values), so that a large workload can be produced chunk by chunk."""
+    G = w.G if G is None else G
+    N = w.N if N is None else N
+    c0 = chunk * KEY_CHUNK_GROUPS
+    c1 = min(G, c0 + KEY_CHUNK_GROUPS)
+    seed = 1_000_003 * w.seeds["keys"] + chunk + seed_offset
+    z = gaussian((c1 - c0, N, w.d), seed, torch.float32, device)
+    if w.unit_keys:
+        z /= torch.linalg.vector_norm(z, dim=-1, keepdim=True)
+    elif w.outliers:
+        sc = channel_scales(w).to(device)[_group_scale_index(w, G)[c0:c1].to(device)]
+        z *= sc[:, None, :]
+    return z.to(w.key_dtype)
 
 
 def queries(w: Workload, G: int | None = None, H: int | None = None, device="cpu",

@@ -17,12 +17,19 @@
 // host it names a stand-in object), so the first call on each device looks up
 // the real address with cudaGetSymbolAddress while that device is current and
 // keeps it.  That first call should therefore come before any stream capture.
+// The address belongs to the CUDA context the library's module was loaded
+// into: the kept address is tagged with that context's process-unique id
+// (cuCtxGetId), and a call made under another context -- for example after
+// cudaDeviceReset, which destroys the device's primary context and with it
+// the array -- looks the address up again instead of reusing a stale one.
 //
 // All calls share the one array.  Calls whose work overlaps on the GPU (two
 // streams, or two threads) race on it and must be serialised by the caller.
 // The array keeps whatever the last call left in it; nothing in it needs to
 // start at zero, because every byte the kernels read in a call was written
 // earlier in the same call.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "tq_internal.cuh"
@@ -32,23 +39,69 @@ namespace {
 static __device__ __align__(256) unsigned char g_score_scratch[TQ_SCORE_NOALLOC_MAX_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id;  // cuCtxGetId of the context the address belongs to
+  void* ptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of g_score_scratch on the current device (looked up once).
+// The two driver calls used here, through the runtime's entry-point lookup
+// (the library does not link the driver library directly, so that it loads on
+// machines without one).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+template <typename Fn>
+Fn driver_entry(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  return nullptr;
+}
+
+// Process-unique id of the current context (0 if there is none).
+cudaError_t current_context_id(unsigned long long* id) {
+  static const CtxGetCurrentFn get_current = driver_entry<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_entry<CtxGetIdFn>("cuCtxGetId");
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  *id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx == nullptr) return cudaSuccess;
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of g_score_scratch in the current device's current context
+// (looked up once per context).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  unsigned long long id = 0;
+  e = current_context_id(&id);
+  if (e != cudaSuccess) return e;
+  if (id == 0) {
+    // no context yet: the runtime's lookup makes the primary one current
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_score_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    if (id == 0) return cudaErrorDeviceUninitialized;
   }
-  *out = g_scratch_addr[dev];
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (a.ptr == nullptr || a.ctx_id != id) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_score_scratch);
+    if (e != cudaSuccess) return e;
+    a.ctx_id = id;
+    a.ptr = p;
+  }
+  *out = a.ptr;
   return cudaSuccess;
 }
 
