@@ -152,14 +152,17 @@ def max_over_ranks(world, v: float) -> float:
 
 # ---------------------------------------------------------------- oracle timing (CPU)
 
-def oracle_throughput(w, bits, mode: str, budget_s: float):
+def oracle_throughput(w, bits, mode: str, budget_s: float, rotation: str = "dense"):
     """Time the oracle (encode + score of one group's keys against H heads) on a
     bounded sample; returns (keys/s, sample description, threads)."""
     import numpy as np
 
     from oracle import tq_oracle as o
     d = w.d
-    Pi = o.haar_rotation(tq_synth.rotation_gaussian(d, w.seeds["rotation"]).numpy()).astype(np.float32)
+    if rotation == "hadamard":
+        Pi = o.hadamard_rotation(tq_synth.hadamard_signs(d, w.seeds["rotation"]).double().numpy()).astype(np.float32)
+    else:
+        Pi = o.haar_rotation(tq_synth.rotation_gaussian(d, w.seeds["rotation"]).numpy()).astype(np.float32)
     S = tq_synth.projection(d, w.seeds["projection"]).numpy() if mode == "prod" else None
     c = o.codebook_f32(1 << (bits - 1 if mode == "prod" else bits), d)
     q = tq_synth.queries(w, G=1).numpy()
@@ -184,10 +187,10 @@ def oracle_throughput(w, bits, mode: str, budget_s: float):
     return n / t, f"encode+score of {n} keys of group 0 against its {w.H} heads (numpy fp64)", threads
 
 
-def workload_config(w, mode: str, bits: int) -> dict:
+def workload_config(w, mode: str, bits: int, rotation: str = "dense") -> dict:
     """The workload as both arms report it."""
     return {"workload": w.name, "mode": mode, "G": w.G, "N": w.N, "H": w.H, "d": w.d, "bits": bits,
-            "key_dtype": str(w.key_dtype).replace("torch.", ""), "top_k": w.top_k}
+            "key_dtype": str(w.key_dtype).replace("torch.", ""), "top_k": w.top_k, "rotation": rotation}
 
 
 # ---------------------------------------------------------------- our path
@@ -213,6 +216,50 @@ def roofline(bytes_, ms, kernel, source, workload, flops=None):
         r["tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
         r["gbs"] = round(ach, 1)
     return r
+
+
+def make_plan(w, bits: int, mode: str, rotation: str):
+    """The workload's plan: the dense Haar rotation (QR of the seeded Gaussian)
+    or the randomised Walsh-Hadamard rotation (signs seeded the same way)."""
+    import vector_quantization_02_b300 as tq
+    d = w.d
+    S = None if mode == "mse" else tq_synth.projection(d, w.seeds["projection"])
+    if rotation == "hadamard":
+        k = bits - 1 if mode == "prod" else bits
+        return tq.Plan.hadamard(d, bits, tq_synth.hadamard_signs(d, w.seeds["rotation"]), S,
+                                tq.tq_lloyd_max_codebook(1 << k, d), mode=mode)
+    return tq.Plan.from_seeds(d, bits, tq_synth.rotation_gaussian(d, w.seeds["rotation"]), S, mode=mode)
+
+
+def encode_only_leg(w, bits: int, mode: str, rotation: str, keys, flush, reps: int, lead):
+    """tq_encode alone on the step's keys with another plan (cold L2)."""
+    import vector_quantization_02_b300 as tq
+    plan = make_plan(w, bits, mode, rotation)
+    G, N, d = keys.shape
+    packed = torch.empty(plan.packed_bytes(G, N), dtype=torch.uint8, device=keys.device)
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        tq.tq_encode(plan, keys, packed=packed)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        lead(300)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        tq.tq_encode(plan, keys, packed=packed)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    ms = statistics.median(a.elapsed_time(b) for a, b in times)
+    kern = {"tensor_d128": ("encode_tc", "k_encode_tc.cu"), "tensor_wide": ("encode_wide", "k_encode_wide.cu")}
+    kn, src = kern[plan.encode_path(w.key_dtype)]
+    nbytes = keys.numel() * keys.element_size() + plan.packed_bytes(G, N)
+    out = {"rotation": rotation, "ms_cold_l2": round(ms, 5), "vectors_per_s": G * N / (ms * 1e-3),
+           "roofline_cold_l2": roofline(nbytes, ms, kn, src, w.name,
+                                        flops=(2 if mode == "prod" else 1) * 2 * d * d * G * N), "reps": reps}
+    plan.close()
+    return out
 
 
 def score_only_leg(name: str, bits: int, flush, reps: int, dev, lead):
@@ -312,9 +359,7 @@ def run_ours(args, world, rank):
     keys = tq_synth.keys(w, device=dev, seed_offset=rank)
     q = tq_synth.queries(w, device=dev, seed_offset=rank)
     mse = args.mode == "mse"
-    plan = tq.Plan.from_seeds(d, bits, tq_synth.rotation_gaussian(d, w.seeds["rotation"]),
-                              None if mse else tq_synth.projection(d, w.seeds["projection"]),
-                              mode=args.mode)
+    plan = make_plan(w, bits, args.mode, args.rotation)
     packed = torch.empty(plan.packed_bytes(G, N), dtype=torch.uint8, device=dev)
     logits = torch.empty(G, H, N, dtype=torch.float32, device=dev)
     top_k = w.top_k
@@ -463,6 +508,13 @@ def run_ours(args, world, rank):
                                 flops=(2 if plan.mode == "prod" else 1) * 2 * d * d * G * N)}
         del xh
 
+    # the same encode with the randomised Walsh-Hadamard rotation (or, when the
+    # step itself uses it, with the dense rotation)
+    other = "dense" if args.rotation == "hadamard" else "hadamard"
+    enc_other = None
+    if (d & (d - 1)) == 0:
+        enc_other = encode_only_leg(w, bits, args.mode, other, keys, flush, max(5, args.steps), lead)
+
     # end to end through the public API from pinned host memory
     if key_bytes > 8e9:
         e2e_ms = None
@@ -474,7 +526,7 @@ def run_ours(args, world, rank):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_desc,
         "data": "synthetic",
-        "config": workload_config(w, args.mode, bits),
+        "config": workload_config(w, args.mode, bits, args.rotation),
         "l2": "flushed between steps (2x L2 memset, outside the step events)",
         "headline": {
             "step_keys_per_s": value,
@@ -490,6 +542,7 @@ def run_ours(args, world, rank):
                       "logits_per_s_cold_l2": G * N * H / (sc_cold_ms * 1e-3), "roofline_cold_l2": sc_roof},
             "fp32_key_baseline": base,
             "decode": dec,
+            f"encode_{other}": enc_other,
         },
         "e2e": None if e2e_ms is None else {
             "value": keys_total / (e2e_ms * 1e-3), "unit": "keys/s", "h2d_bytes_per_step": key_bytes + q_bytes,
@@ -506,7 +559,7 @@ def run_ours(args, world, rank):
         line["parts"]["score_llama31_b3"] = score_only_leg("llama31_8b_prefill", 3, flush, max(5, args.steps), dev,
                                                            lead)
     if rank == 0 and not args.no_cpu_baseline:
-        v, sample, cores = oracle_throughput(w, bits, args.mode, args.cpu_budget)
+        v, sample, cores = oracle_throughput(w, bits, args.mode, args.cpu_budget, args.rotation)
         line["cpu_baseline"] = {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample}
     return line
 
@@ -519,14 +572,15 @@ def run_reference(args, world, rank):
     vals = []
     sample = cores = None
     for _ in range(args.warmup + args.steps):
-        v, sample, cores = oracle_throughput(w, bits, args.mode, args.cpu_budget / max(1, args.steps + args.warmup))
+        v, sample, cores = oracle_throughput(w, bits, args.mode, args.cpu_budget / max(1, args.steps + args.warmup),
+                                             args.rotation)
         vals.append(v)
     v = statistics.median(vals[args.warmup:]) if len(vals) > args.warmup else vals[-1]
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, args.mode, bits),
+        "config": workload_config(w, args.mode, bits, args.rotation),
         "cpu_baseline": {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -542,6 +596,8 @@ def main():
     ap.add_argument("--bits", type=int, default=0)
     ap.add_argument("--mode", choices=["prod", "mse"], default="prod",
                     help="TurboQuantProd (the workloads' method) or TurboQuantMSE codec")
+    ap.add_argument("--rotation", choices=["dense", "hadamard"], default="dense",
+                    help="dense Haar rotation (QR of a seeded Gaussian) or randomised Walsh-Hadamard rotation")
     ap.add_argument("--tokens", type=int, default=0,
                     help="cap the tokens per group (a reduced case for profiling; not a bench configuration)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")

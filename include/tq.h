@@ -10,7 +10,9 @@
  *           inner products; a 1-bit QJL residual pass removes the bias; 4-bit
  *           keys speed up attention logits versus 32-bit keys.
  *  [P5]     "알고리즘보다 커널이 성패를 가른다" (tistory27), section 3: the
- *           bit-packed format with QJL metadata needs a dedicated kernel.
+ *           bit-packed format with QJL metadata needs a dedicated kernel;
+ *           section 4: structured (Walsh-Hadamard) rotations as an
+ *           acceleration (turboquant_plus).
  *
  * Notation: d = head dimension (a multiple of 128), m = d rows of S,
  * b = total bits per coordinate, k = b-1 Lloyd-Max bits (PROD) or k = b (MSE),
@@ -107,6 +109,25 @@ tq_status tq_haar_rotation(int d, const double* gaussian, float* Pi_out);
  * TQ_MSE bits in {1,2,3,4}.  Errors: TQ_EINVAL, TQ_ENOMEM, TQ_ECUDA. */
 tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const float* S,
                          const float* codebook, void* stream, tq_plan** out);
+
+/* Create a plan whose rotation is the randomised Walsh-Hadamard transform
+ * ("알고리즘보다 커널이 성패를 가른다" section 4: a structured WHT rotation in
+ * place of the dense random one, as turboquant_plus does):
+ *   Pi = H_d diag(signs) / sqrt(d),
+ * H_d the Sylvester Hadamard matrix ((-1)^popcount(i & j)).  Each entry of Pi
+ * is +-c with c = (float)(1 / sqrt(d)) computed in double, so Pi is
+ * determined exactly by the signs.
+ *   signs     device fp32, d entries, each +1 or -1.
+ *   S, codebook, mode, bits: as tq_plan_create.
+ * Everything tq_plan_create documents holds for the resulting plan (every
+ * kernel computes with this Pi).  In addition, the d = 128 tensor-core encode
+ * forms the rotation with one exact product of the keys and the +-1 matrix
+ * H diag(signs), the scale c being folded into the plan's thresholds,
+ * centroids and M, instead of the two-product split a dense Pi needs.
+ * Constraints: d a power of two, 128 <= d <= 2048.  Errors: TQ_EINVAL (also
+ * for a sign that is not +-1), TQ_ENOMEM, TQ_ECUDA. */
+tq_status tq_plan_create_hadamard(int d, int bits, tq_mode mode, const float* signs, const float* S,
+                                  const float* codebook, void* stream, tq_plan** out);
 tq_status tq_plan_destroy(tq_plan* plan);
 
 /* Bytes of the packed buffer for G groups of N tokens.  Layout ([P5] §3):

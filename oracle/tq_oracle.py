@@ -120,6 +120,49 @@ def haar_rotation(gaussian: np.ndarray) -> np.ndarray:
     return q * s[None, :]
 
 
+def hadamard_matrix(d: int) -> np.ndarray:
+    """Sylvester's Walsh-Hadamard matrix of order d (a power of two), entries
+    +-1, built by its recursive definition H_1 = [1], H_2n = [[H_n, H_n],
+    [H_n, -H_n]]."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("the Walsh-Hadamard matrix needs d a power of two")
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def hadamard_rotation(signs) -> np.ndarray:
+    """Randomised Walsh-Hadamard rotation Pi = H_d diag(signs) / sqrt(d), the
+    structured rotation of "알고리즘보다 커널이 성패를 가른다" section 4 (WHT
+    rotation, turboquant_plus).  READING: the pages name the transform only;
+    the random sign flip before it is the usual way to randomise a fixed
+    orthogonal transform (without it every key would see the same H).  The
+    signs are an input (+-1, seeded by the caller).  fp64."""
+    signs = np.asarray(signs, dtype=np.float64)
+    if not np.all(np.abs(signs) == 1.0):
+        raise ValueError("signs must be +-1")
+    d = signs.size
+    return hadamard_matrix(d) * signs[None, :] / math.sqrt(d)
+
+
+def fwht(v) -> np.ndarray:
+    """Fast Walsh-Hadamard transform (unnormalised) of the last axis by
+    butterflies: returns H_d v for each row, in O(d log d)."""
+    v = np.array(v, dtype=np.float64, copy=True)
+    d = v.shape[-1]
+    if d & (d - 1):
+        raise ValueError("the Walsh-Hadamard transform needs d a power of two")
+    h = 1
+    while h < d:
+        w = v.reshape(v.shape[:-1] + (d // (2 * h), 2, h))
+        a, b = w[..., 0, :].copy(), w[..., 1, :].copy()
+        w[..., 0, :] = a + b
+        w[..., 1, :] = a - b
+        h *= 2
+    return v
+
+
 def boundaries(c: np.ndarray) -> np.ndarray:
     """Decision boundaries t_i = (c_i + c_{i+1}) / 2, in fp64."""
     c = np.asarray(c, dtype=np.float64)
@@ -383,6 +426,94 @@ def score_mse_rotated(q, idx, n, Pi, c) -> np.ndarray:
     ``score_prod_rotated``).  q [H][d] -> logits [H][N]."""
     qr = _as64(q) @ _as64(Pi).T
     return _as64(n)[None, :] * (qr @ _as64(c)[np.asarray(idx)].T)
+
+
+# ----------------------------------------------------------------------------
+# Values and the attention output of one decode step
+#
+# The value cache holds TurboQuantMSE codes ([PT-KR] "1단계"; the pages' 58 MB
+# figure compresses K and V at 3 bits) in a coordinate-major layout: per group,
+# blocks of 128 tokens; per block, for every code plane p (LSB first) and every
+# coordinate j, 16 bytes holding bit p of the code of coordinate j of the
+# block's 128 tokens, token t at bit t % 32 of little-endian word t // 32;
+# then the 128 tokens' {float ||v||, float 0}.  It holds the same bits as
+# ``pack`` in MSE mode, transposed within each block (READING: the pages fix
+# no layout; this one lets a kernel read one coordinate across a block's
+# tokens as one 16-byte chunk).
+# ----------------------------------------------------------------------------
+
+def pack_values(idx, n, d: int, bits: int, G: int, N: int) -> np.ndarray:
+    """Pack MSE value codes [G*N][d] (bits-bit) and norms [G*N] in the
+    coordinate-major value layout."""
+    T = TOKENS_PER_BLOCK
+    nb = -(-N // T)
+    idx = np.asarray(idx).reshape(G, N, d)
+    planes = np.zeros((G, nb * T, bits, d), dtype=np.uint64)
+    for p in range(bits):
+        planes[:, :N, p, :] = (idx >> p) & 1
+    b = planes.reshape(G, nb, 4, 32, bits, d)                          # token t = 32 w + i
+    words = (b << np.arange(32, dtype=np.uint64)[None, None, None, :, None, None]).sum(axis=3)
+    words = words.astype(np.uint32).transpose(0, 1, 3, 4, 2)           # [G][nb][bits][d][4]
+    norms = np.zeros((G, nb * T, 2), dtype=np.float32)
+    norms[:, :N, 0] = np.asarray(n, dtype=np.float32).reshape(G, N)
+    out = bytearray()
+    for g in range(G):
+        for blk in range(nb):
+            out += words[g, blk].astype("<u4").tobytes()
+            out += norms[g, blk * T:(blk + 1) * T].astype("<f4").tobytes()
+    return np.frombuffer(bytes(out), dtype=np.uint8)
+
+
+def unpack_values(buf, d: int, bits: int, G: int, N: int) -> dict:
+    """Inverse of ``pack_values``: idx [G*N][d], n [G*N] (fp64 of the stored fp32)."""
+    T = TOKENS_PER_BLOCK
+    nb = -(-N // T)
+    bb = block_bytes(d, bits, "mse")
+    buf = np.asarray(buf, dtype=np.uint8).reshape(G * nb, bb)
+    plane_bytes = bits * d * 16
+    w = np.ascontiguousarray(buf[:, :plane_bytes]).view("<u4").reshape(G * nb, bits, d, 4)
+    tbits = (w[..., None] >> np.arange(32, dtype=np.uint32)) & 1      # [B][bits][d][4][32]
+    tbits = tbits.reshape(G * nb, bits, d, T).transpose(0, 3, 1, 2)    # [B][T][bits][d]
+    idx = np.zeros((G * nb, T, d), dtype=np.int64)
+    for p in range(bits):
+        idx |= tbits[:, :, p, :].astype(np.int64) << p
+    nr = np.ascontiguousarray(buf[:, plane_bytes:]).view("<f4").reshape(G, nb * T, 2)
+    idx = idx.reshape(G, nb * T, d)
+    return dict(idx=idx[:, :N].reshape(G * N, d), n=nr[:, :N, 0].astype(np.float64).reshape(G * N))
+
+
+def attend(q, kidx, kz, kn, krho, Pi_k, S, c_k, vidx, vn, Pi_v, c_v, scale: float) -> np.ndarray:
+    """One decode step of attention on the compressed cache, for one group:
+    logits from the compressed keys ([PT-KR] usage listing ``inner_product``;
+    [TAMBUR]: attention logits computed directly on the compressed keys),
+    softmax over the tokens of scale * logit, and the probability-weighted sum
+    of the values reconstructed from their MSE codes (``mse_reconstruct``,
+    [PT-KR] ``decompress``):
+        out_h = sum_t softmax_t(scale * l_h)_t * v_hat_t.
+    READING: the pages name no scale; the caller passes it (1/sqrt(d) for the
+    usual scaled dot-product attention).  q [H][d] -> [H][d]."""
+    logits = score_prod(q, kidx, kz, kn, krho, Pi_k, S, c_k)           # [H][N]
+    z = scale * logits
+    z = z - np.max(z, axis=1, keepdims=True)
+    e = np.exp(z)
+    p = e / np.sum(e, axis=1, keepdims=True)
+    return p @ mse_reconstruct(vidx, vn, Pi_v, c_v)
+
+
+def attend_packed(q, kbuf, vbuf, Pi_k, S, c_k, kbits: int, Pi_v, c_v, vbits: int, G: int, N: int,
+                  scale: float) -> np.ndarray:
+    """``attend`` for every group: q [G][H][d], keys packed by ``pack`` (Prod),
+    values by ``pack_values`` -> [G][H][d]."""
+    q = _as64(q)
+    d = q.shape[-1]
+    ku = unpack(kbuf, d, kbits, "prod", G, N)
+    vu = unpack_values(vbuf, d, vbits, G, N)
+    out = np.zeros(q.shape)
+    for g in range(G):
+        r = slice(g * N, (g + 1) * N)
+        out[g] = attend(q[g], ku["idx"][r], ku["z"][r], ku["n"][r], ku["rho"][r], Pi_k, S, c_k,
+                        vu["idx"][r], vu["n"][r], Pi_v, c_v, scale)
+    return out
 
 
 # ----------------------------------------------------------------------------

@@ -44,6 +44,26 @@ class Inputs:
                        torch.from_numpy(self.c_o.copy()), mode=self.mode)
 
 
+class HadamardInputs(Inputs):
+    """Plan inputs with the randomised Walsh-Hadamard rotation: the oracle's
+    Pi = H diag(signs) / sqrt(d) in fp32 (each entry +-fl32(1/sqrt(d)), the
+    value the library computes from the same signs), the GPU plan from the
+    signs."""
+
+    def __init__(self, d, bits, mode, sign_seed, proj_seed):
+        self.d, self.bits, self.mode = d, bits, mode
+        self.k = bits - 1 if mode == "prod" else bits
+        self.signs = tq_synth.hadamard_signs(d, sign_seed)
+        self.S = tq_synth.projection(d, proj_seed)
+        self.Pi_o = np.ascontiguousarray(o.hadamard_rotation(self.signs.double().numpy()).astype(np.float32))
+        self.c_o = o.codebook_f32(1 << self.k, d)
+        self.S_o = self.S.numpy()
+
+    def plan(self):
+        return tq.Plan.hadamard(self.d, self.bits, self.signs, self.S if self.mode == "prod" else None,
+                                torch.from_numpy(self.c_o.copy()), mode=self.mode)
+
+
 def oracle_encode(inp: Inputs, keys: torch.Tensor):
     """Oracle encode of keys [G][N][d] (any dtype) -> (bytes, encode dict)."""
     G, N, d = keys.shape

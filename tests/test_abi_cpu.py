@@ -53,6 +53,12 @@ def test_argument_errors_need_no_gpu():
     assert lib.tq_plan_create(128, 1, 0, vp(16), vp(16), vp(16), None, ctypes.byref(h)) == -1
     assert lib.tq_plan_create(128, 3, 0, vp(16), None, vp(16), None, ctypes.byref(h)) == -1
     assert lib.tq_plan_create(128, 3, 0, vp(16), vp(16), vp(16), None, None) == -1
+    # the Walsh-Hadamard rotation needs d a power of two (128..2048) and signs
+    assert lib.tq_plan_create_hadamard(384, 3, 0, vp(16), vp(16), vp(16), None, ctypes.byref(h)) == -1
+    assert lib.tq_plan_create_hadamard(64, 3, 0, vp(16), vp(16), vp(16), None, ctypes.byref(h)) == -1
+    assert lib.tq_plan_create_hadamard(4096, 3, 0, vp(16), vp(16), vp(16), None, ctypes.byref(h)) == -1
+    assert lib.tq_plan_create_hadamard(128, 3, 0, None, vp(16), vp(16), None, ctypes.byref(h)) == -1
+    assert lib.tq_plan_create_hadamard(128, 3, 0, vp(16), vp(16), vp(16), None, None) == -1
     assert lib.tq_packed_bytes(None, 1, 1) == 0
     assert lib.tq_encode(None, vp(16), 0, 1, 1, vp(16), None) == -1
     assert lib.tq_score(None, vp(16), 1, 1, vp(16), 1, vp(16), 0, None, None, vp(256), 1 << 20, None) == -1

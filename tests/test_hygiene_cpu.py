@@ -86,9 +86,9 @@ def test_committed_traffic_entries_name_existing_summaries():
 
 def test_both_bench_arms_report_the_same_workload_config():
     w = tq_synth.WORKLOADS["vector_search_1m"]
-    c = bench.workload_config(w, "mse", 4)
+    c = bench.workload_config(w, "mse", 4, "hadamard")
     assert c == {"workload": w.name, "mode": "mse", "G": w.G, "N": w.N, "H": w.H, "d": w.d, "bits": 4,
-                 "key_dtype": "float32", "top_k": w.top_k}
-    # the reference arm prints exactly this dict; ours adds only how L2 was handled
+                 "key_dtype": "float32", "top_k": w.top_k, "rotation": "hadamard"}
+    # both arms print exactly this dict as their config (how L2 was handled is a separate key)
     src = open(os.path.join(ROOT, "bench.py")).read()
-    assert src.count("workload_config(w, args.mode, bits)") == 2
+    assert src.count('"config": workload_config(w, args.mode, bits, args.rotation)') == 2

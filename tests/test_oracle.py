@@ -440,3 +440,165 @@ def test_score_in_the_rotated_frame_equals_score_prod():
     a = o.score_mse(q, m["idx"], m["n"], Pi, c)
     b = o.score_mse_rotated(q, m["idx"], m["n"], Pi, c)
     assert np.max(np.abs(a - b)) <= 1e-12 * np.max(np.abs(a))
+
+
+# ---------------------------------------------------------------- Walsh-Hadamard rotation
+
+def test_hadamard_small_orders_by_hand():
+    assert np.array_equal(o.hadamard_matrix(1), [[1.0]])
+    assert np.array_equal(o.hadamard_matrix(2), [[1, 1], [1, -1]])
+    assert np.array_equal(o.hadamard_matrix(4), [[1, 1, 1, 1], [1, -1, 1, -1], [1, 1, -1, -1], [1, -1, -1, 1]])
+    with pytest.raises(ValueError):
+        o.hadamard_matrix(12)
+
+
+@pytest.mark.parametrize("d", [8, 128, 1024])
+def test_hadamard_rotation_orthogonal_and_matches_the_butterflies(d):
+    rng = _rng(40)
+    signs = np.where(rng.standard_normal(d) >= 0, 1.0, -1.0)
+    Pi = o.hadamard_rotation(signs)
+    # H H^T = d I, so Pi is orthogonal (symmetric H, diagonal signs)
+    assert np.max(np.abs(Pi @ Pi.T - np.eye(d))) <= 1e-12
+    assert np.array_equal(o.hadamard_matrix(d), o.hadamard_matrix(d).T)
+    # the matrix and the O(d log d) transform agree: Pi u = H (signs * u) / sqrt(d)
+    u = rng.standard_normal((5, d))
+    assert np.max(np.abs(u @ Pi.T - o.fwht(u * signs) / math.sqrt(d))) <= 1e-12
+    # entry (i, j) is (-1)^popcount(i & j) * signs[j] / sqrt(d)
+    for i, j in [(0, 0), (1, 1), (3, 5), (d - 1, d - 1), (d // 2, 1)]:
+        want = (-1.0) ** bin(i & j).count("1") * signs[j] / math.sqrt(d)
+        assert Pi[i, j] == pytest.approx(want, abs=1e-15)
+
+
+def test_hadamard_rotation_spreads_a_basis_vector():
+    # every rotated coordinate of e_j has magnitude 1/sqrt(d): the structured
+    # rotation flattens a spike, as a random rotation does on average
+    d = 128
+    signs = np.where(_rng(41).standard_normal(d) >= 0, 1.0, -1.0)
+    Pi = o.hadamard_rotation(signs)
+    for j in (0, 7, 127):
+        assert np.allclose(np.abs(Pi[:, j]), 1 / math.sqrt(d), atol=1e-15)
+    with pytest.raises(ValueError):
+        o.hadamard_rotation(np.array([1.0, 0.5]))
+
+
+def test_mse_distortion_3bit_with_the_hadamard_rotation():
+    # the structured rotation keeps the pages' 3-bit distortion on random unit
+    # vectors (the same bound as the dense Haar rotation)
+    d, n = 128, 20000
+    rng = _rng(42)
+    signs = np.where(rng.standard_normal(d) >= 0, 1.0, -1.0)
+    Pi = o.hadamard_rotation(signs).astype(np.float32)
+    x = rng.standard_normal((n, d))
+    x /= np.linalg.norm(x, axis=1, keepdims=True)
+    c = o.codebook_f32(8, d)
+    e = o.encode_mse(x, Pi, c)
+    D = np.mean(np.sum((x - o.mse_reconstruct(e["idx"], e["n"], Pi, c)) ** 2, axis=1))
+    g = _golden("pages_printed_values.json")
+    assert D <= g["mse_distortion_3bit_bound"]
+    assert abs(D - g["mse_distortion_3bit_measured"]) <= 0.002
+
+
+# ---------------------------------------------------------------- value layout and attention
+
+@pytest.mark.parametrize("bits", [1, 3, 4])
+def test_value_layout_roundtrip_and_bit_addresses(bits):
+    G, N, d = 2, 300, 256
+    rng = _rng(50)
+    idx = rng.integers(0, 1 << bits, size=(G * N, d))
+    n = rng.random(G * N).astype(np.float32)
+    buf = o.pack_values(idx, n, d, bits, G, N)
+    # the same number of bytes per key as the MSE layout
+    assert buf.size == o.packed_bytes(G, N, d, bits, "mse")
+    u = o.unpack_values(buf, d, bits, G, N)
+    assert np.array_equal(u["idx"], idx) and np.array_equal(u["n"], n.astype(np.float64))
+    # hand-computed addresses: plane p, coordinate j, token t of a block is bit
+    # t % 32 of word t // 32 of the 16 bytes at ((p d + j) 16) in the block
+    bb = 128 * (bits * d // 8 + 8)
+    nb = 3
+    for (g, tok, p, j) in [(0, 0, 0, 0), (1, 299, bits - 1, d - 1), (1, 130, 0, 37), (0, 257, bits - 1, 129),
+                           (0, 31, 0, 5), (1, 33, bits - 1, 200)]:
+        blk, t = divmod(tok, 128)
+        w, i = divmod(t, 32)
+        off = (g * nb + blk) * bb + (p * d + j) * 16 + 4 * w
+        word = int.from_bytes(bytes(buf[off:off + 4]), "little")
+        assert (word >> i) & 1 == (idx[g * N + tok, j] >> p) & 1
+        noff = (g * nb + blk) * bb + bits * d * 16 + t * 8
+        assert np.frombuffer(bytes(buf[noff:noff + 8]), "<f4").tolist() == [n[g * N + tok], 0.0]
+    # the same codes as the token-major MSE layout
+    m = o.unpack(o.pack(idx, None, n, None, d, bits, "mse", G, N), d, bits, "mse", G, N)
+    assert np.array_equal(m["idx"], u["idx"])
+
+
+def _attention_case(N, seed, d=16, H=3):
+    rng = _rng(seed)
+    Pi_k, Pi_v = _haar(d, seed + 1), _haar(d, seed + 2)
+    S = rng.standard_normal((d, d))
+    c_k, c_v = o.codebook_f32(4, d), o.codebook_f32(8, d)
+    x = rng.standard_normal((N, d))
+    v = rng.standard_normal((N, d))
+    q = rng.standard_normal((H, d))
+    ke = o.encode_prod(x, Pi_k, S, c_k)
+    ve = o.encode_mse(v, Pi_v, c_v)
+    kf = (ke["idx"], ke["z"], ke["n"], ke["rho"], Pi_k, S, c_k)
+    return q, kf, ve, Pi_v, c_v
+
+
+def test_attention_two_tokens_is_the_logistic_weighting():
+    q, kf, ve, Pi_v, c_v = _attention_case(2, 51)
+    scale = 0.3
+    out = o.attend(q, *kf, ve["idx"], ve["n"], Pi_v, c_v, scale)
+    l = o.score_prod(q, *kf)
+    vh = o.mse_reconstruct(ve["idx"], ve["n"], Pi_v, c_v)
+    p1 = 1.0 / (1.0 + np.exp(-scale * (l[:, 1] - l[:, 0])))
+    want = (1 - p1)[:, None] * vh[0] + p1[:, None] * vh[1]
+    assert np.max(np.abs(out - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+def test_attention_invariants():
+    q, kf, ve, Pi_v, c_v = _attention_case(40, 52)
+    vh = o.mse_reconstruct(ve["idx"], ve["n"], Pi_v, c_v)
+    # scale 0: the plain mean of the reconstructed values, for every head
+    out0 = o.attend(q, *kf, ve["idx"], ve["n"], Pi_v, c_v, 0.0)
+    assert np.allclose(out0, vh.mean(axis=0)[None, :], atol=1e-12)
+    # every value equal: the output is that value whatever the logits
+    same_idx = np.repeat(ve["idx"][:1], 40, axis=0)
+    same_n = np.repeat(ve["n"][:1], 40)
+    outs = o.attend(q, *kf, same_idx, same_n, Pi_v, c_v, 0.7)
+    assert np.allclose(outs, o.mse_reconstruct(same_idx[:1], same_n[:1], Pi_v, c_v), atol=1e-12)
+    # a large scale selects the value of each head's largest logit
+    l = o.score_prod(q, *kf)
+    outb = o.attend(q, *kf, ve["idx"], ve["n"], Pi_v, c_v, 1e4)
+    assert np.allclose(outb, vh[np.argmax(l, axis=1)], atol=1e-9)
+    # permuting the tokens (keys and values together) changes nothing
+    perm = _rng(53).permutation(40)
+    kp = (kf[0][perm], kf[1][perm], kf[2][perm], kf[3][perm]) + kf[4:]
+    outp = o.attend(q, *kp, ve["idx"][perm], ve["n"][perm], Pi_v, c_v, 0.7)
+    assert np.allclose(outp, o.attend(q, *kf, ve["idx"], ve["n"], Pi_v, c_v, 0.7), atol=1e-12)
+    # the weights are a softmax over tokens (rows sum to one): a value of zero
+    # norm at every token but one gives p_t v_t at that token
+    n1 = np.zeros(40)
+    n1[7] = ve["n"][7]
+    out1 = o.attend(q, *kf, ve["idx"], n1, Pi_v, c_v, 0.7)
+    z = 0.7 * l
+    p7 = np.exp(z[:, 7] - z.max(axis=1)) / np.exp(z - z.max(axis=1, keepdims=True)).sum(axis=1)
+    assert np.allclose(out1, p7[:, None] * vh[7][None, :], atol=1e-12)
+
+
+def test_attend_packed_matches_per_group_attend():
+    d, G, N, H = 128, 2, 200, 4
+    rng = _rng(54)
+    Pi_k, Pi_v = _haar(d, 55).astype(np.float32), _haar(d, 56).astype(np.float32)
+    S = rng.standard_normal((d, d)).astype(np.float32)
+    c_k, c_v = o.codebook_f32(4, d), o.codebook_f32(8, d)
+    x = rng.standard_normal((G, N, d))
+    v = rng.standard_normal((G, N, d))
+    q = rng.standard_normal((G, H, d))
+    kbuf, ke = o.encode_pack(x, Pi_k, S, c_k, 3, "prod", G, N)
+    ve = o.encode_mse(v.reshape(G * N, d), Pi_v, c_v)
+    vbuf = o.pack_values(ve["idx"], ve["n"].astype(np.float32), d, 3, G, N)
+    out = o.attend_packed(q, kbuf, vbuf, Pi_k, S, c_k, 3, Pi_v, c_v, 3, G, N, 1 / math.sqrt(d))
+    for g in range(G):
+        r = slice(g * N, (g + 1) * N)
+        want = o.attend(q[g], ke["idx"][r], ke["z"][r], ke["n"][r].astype(np.float32), ke["rho"][r].astype(np.float32),
+                        Pi_k, S, c_k, ve["idx"][r], ve["n"][r].astype(np.float32), Pi_v, c_v, 1 / math.sqrt(d))
+        assert np.allclose(out[g], want, rtol=0, atol=1e-12 * np.max(np.abs(want)))

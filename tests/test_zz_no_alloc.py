@@ -10,6 +10,8 @@ caller-allocated workspace), and that oversized requests are refused.  It is
 named so that pytest collects it last; it passes run alone in a fresh
 process and after the other tests.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -95,11 +97,13 @@ def test_noalloc_call_allocates_nothing(cuda):
     ti = torch.empty(G, H, k, dtype=torch.int64, device=cuda)
     tq.tq_score_noalloc(plan, q, packed, N, top_k=k, logits=logits, top_scores=ts, top_idx=ti)
     torch.cuda.synchronize()
+    gc.collect()  # tensors of earlier tests freed now, not during the measured call
     before = (torch.cuda.memory_allocated(cuda), torch.cuda.mem_get_info(cuda)[0])
     tq.tq_score_noalloc(plan, q, packed, N, top_k=k, logits=logits, top_scores=ts, top_idx=ti)
     torch.cuda.synchronize()
     after = (torch.cuda.memory_allocated(cuda), torch.cuda.mem_get_info(cuda)[0])
-    assert after == before
+    assert after[0] <= before[0]   # nothing allocated through torch
+    assert after[1] == before[1]   # nor through the driver: the device's free memory is unchanged
     want, want_s, want_i = tq.tq_score(plan, q, packed, N, top_k=k)
     torch.cuda.synchronize()
     assert torch.equal(ti, want_i)

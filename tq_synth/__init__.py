@@ -38,7 +38,7 @@ import dataclasses
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "gaussian", "rotation_gaussian", "projection",
+__all__ = ["Workload", "WORKLOADS", "gaussian", "rotation_gaussian", "hadamard_signs", "projection",
            "channel_scales", "keys", "key_chunk", "queries", "small_case"]
 
 
@@ -102,6 +102,14 @@ def gaussian(shape, seed: int, dtype=torch.float64, device="cpu") -> torch.Tenso
 def rotation_gaussian(d: int, seed: int) -> torch.Tensor:
     """The d x d fp64 Gaussian matrix whose (sign-fixed) QR factor is the rotation."""
     return gaussian((d, d), seed, torch.float64)
+
+
+def hadamard_signs(d: int, seed: int) -> torch.Tensor:
+    """d random signs (+1 or -1, fp32) for a randomised Walsh-Hadamard
+    rotation: the signs of seeded N(0,1) draws (a draw of exactly 0 counts as
+    +1)."""
+    g = gaussian((d,), seed, torch.float64)
+    return torch.where(g >= 0, 1.0, -1.0).to(torch.float32)
 
 
 def projection(d: int, seed: int, m: int | None = None) -> torch.Tensor:

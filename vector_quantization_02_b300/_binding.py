@@ -31,6 +31,7 @@ def _load() -> ctypes.CDLL:
         "tq_lloyd_max_codebook": (c_int, [c_int, c_int, vp]),
         "tq_haar_rotation": (c_int, [c_int, vp, vp]),
         "tq_plan_create": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, ctypes.POINTER(vp)]),
+        "tq_plan_create_hadamard": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, ctypes.POINTER(vp)]),
         "tq_plan_destroy": (c_int, [vp]),
         "tq_packed_bytes": (c_sz, [vp, c_i64, c_i64]),
         "tq_encode": (c_int, [vp, vp, c_int, c_i64, c_i64, vp, vp]),
@@ -56,7 +57,8 @@ def _load() -> ctypes.CDLL:
 
 
 lib = _load()
-EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_plan_destroy",
+EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_plan_create_hadamard",
+            "tq_plan_destroy",
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
             "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
             "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path", "tq_decode_path",
@@ -133,11 +135,19 @@ def tq_codebook_parity_expansion(codebook: torch.Tensor):
 class Plan:
     """A TurboQuant plan: rotation Pi, projection S and codebook on the GPU."""
 
-    def __init__(self, d: int, bits: int, Pi: torch.Tensor, S: torch.Tensor | None,
-                 codebook: torch.Tensor, mode: str = "prod", stream=None):
+    def __init__(self, d: int, bits: int, Pi: torch.Tensor | None, S: torch.Tensor | None,
+                 codebook: torch.Tensor, mode: str = "prod", stream=None, signs: torch.Tensor | None = None):
+        """A plan with a dense rotation Pi, or (``signs`` given, Pi None) the
+        randomised Walsh-Hadamard rotation Pi = H diag(signs) / sqrt(d)."""
         self.d, self.bits, self.mode = d, bits, mode
+        self.hadamard = signs is not None
         dev = torch.device("cuda", torch.cuda.current_device())
-        Pi_d = Pi.to(dev, torch.float32).contiguous()
+        if self.hadamard:
+            rot_d = signs.to(dev, torch.float32).contiguous()
+            if rot_d.numel() != d:
+                raise ValueError("signs must hold d entries")
+        else:
+            rot_d = Pi.to(dev, torch.float32).contiguous()
         S_d = S.to(dev, torch.float32).contiguous() if S is not None else None
         cb_d = codebook.to(dev, torch.float32).contiguous()
         k = bits - 1 if mode == "prod" else bits
@@ -146,10 +156,12 @@ class Plan:
         if (S_d is None) != (mode == "mse"):
             raise ValueError("S is required for mode 'prod' and unused for 'mse'")
         h = ctypes.c_void_p()
-        st = lib.tq_plan_create(d, bits, _MODES[mode], _dev(Pi_d, "Pi", shape=(d, d)),
-                                _dev(S_d, "S", shape=(d, d)) if S_d is not None else None,
-                                _dev(cb_d, "codebook"), ctypes.c_void_p(_stream(stream)), ctypes.byref(h))
-        _check(st, "tq_plan_create")
+        create = lib.tq_plan_create_hadamard if self.hadamard else lib.tq_plan_create
+        st = create(d, bits, _MODES[mode],
+                    _dev(rot_d, "signs", shape=(d,)) if self.hadamard else _dev(rot_d, "Pi", shape=(d, d)),
+                    _dev(S_d, "S", shape=(d, d)) if S_d is not None else None,
+                    _dev(cb_d, "codebook"), ctypes.c_void_p(_stream(stream)), ctypes.byref(h))
+        _check(st, "tq_plan_create_hadamard" if self.hadamard else "tq_plan_create")
         self.handle = h
         self.levels = cb_d.numel()
 
@@ -159,6 +171,12 @@ class Plan:
         """Build Pi and the codebook with the library's host helpers."""
         k = bits - 1 if mode == "prod" else bits
         return cls(d, bits, tq_haar_rotation(rotation_gaussian), S, tq_lloyd_max_codebook(1 << k, d), mode)
+
+    @classmethod
+    def hadamard(cls, d: int, bits: int, signs: torch.Tensor, S: torch.Tensor | None, codebook: torch.Tensor,
+                 mode: str = "prod"):
+        """The randomised Walsh-Hadamard rotation (tq_plan_create_hadamard)."""
+        return cls(d, bits, None, S, codebook, mode, signs=signs)
 
     def close(self):
         if getattr(self, "handle", None):

@@ -71,6 +71,10 @@ struct EncTcArgs {
   const uint8_t* m_lo;
   uint8_t* packed;
   int* err;
+  // 1 for a Walsh-Hadamard plan: the rotation is one exact product with the
+  // +-1 matrix (pi_hi), whose scale c is folded into cp, px and M; rho = c ||r'||
+  int e2_single;
+  float rho_scale;
 };
 
 __device__ __forceinline__ void raise(int* err, volatile int* abort) {
@@ -172,6 +176,12 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       constexpr uint32_t idesc_x = idesc_f16(kBF16 ? 1u : 0u, 128, 128);
       constexpr uint32_t idesc_r = idesc_f16(1u, 128, 128);
       const bool e2 = warp == 1;
+      // shared-memory descriptors computed once: every MMA below takes one of
+      // these plus a compile-time offset (descriptor units of 16 B), so the
+      // issuing thread does no address arithmetic between MMAs
+      const uint64_t dx0 = sdesc_k_sw128(sb + kOffX), dpih = sdesc_k_sw128(sb + kOffPiHi),
+                     dpil = sdesc_k_sw128(sb + kOffPiLo), dmh = sdesc_k_sw128(sb + kOffMHi),
+                     dml = sdesc_k_sw128(sb + kOffMLo);
       const int64_t n_iss = (PROD || e2) ? n_my : 0;  // MSE has no E5
       bool ok = mbar_wait(bar(BAR_OPS), 0, abort);
       for (int64_t i = 0; ok && i < n_iss; ++i) {
@@ -187,12 +197,12 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
           }
           tc_fence_after();
           const uint32_t d = tmem + 256u * b;
+          const uint64_t dx = dx0 + (uint64_t)(((uint32_t)s * kOpBytes) >> 4);
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
-            const uint32_t off = (kb >> 2) * kAtomBytes + (kb & 3) * 32;
-            const uint64_t ad = sdesc_k_sw128(sb + kOffX + s * kOpBytes + off);
-            mma_f16_ss(d, ad, sdesc_k_sw128(sb + kOffPiHi + off), idesc_x, kb > 0);
-            mma_f16_ss(d, ad, sdesc_k_sw128(sb + kOffPiLo + off), idesc_x, 1);
+            const uint32_t off16 = ((kb >> 2) * kAtomBytes + (kb & 3) * 32) >> 4;
+            mma_f16_ss(d, dx + off16, dpih + off16, idesc_x, kb > 0);
+            if (!a.e2_single) mma_f16_ss(d, dx + off16, dpil + off16, idesc_x, 1);
           }
           mma_commit(bar(BAR_YFULL + b));
           mma_commit(bar(BAR_XEMPTY + s));
@@ -210,12 +220,11 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
               }
               tc_fence_after();
             }
-            const uint32_t off = (kb >> 2) * kAtomBytes + (kb & 3) * 32;
+            const uint32_t off16 = ((kb >> 2) * kAtomBytes + (kb & 3) * 32) >> 4;
             const uint32_t a_hi = r + 32 * (kb >> 1) + 8 * (kb & 1), a_lo = a_hi + 16;
-            const uint64_t mh = sdesc_k_sw128(sb + kOffMHi + off), ml = sdesc_k_sw128(sb + kOffMLo + off);
-            mma_f16_ts(d, a_hi, mh, idesc_r, kb > 0);
-            mma_f16_ts(d, a_hi, ml, idesc_r, 1);
-            mma_f16_ts(d, a_lo, mh, idesc_r, 1);
+            mma_f16_ts(d, a_hi, dmh + off16, idesc_r, kb > 0);
+            mma_f16_ts(d, a_hi, dml + off16, idesc_r, 1);
+            mma_f16_ts(d, a_lo, dmh + off16, idesc_r, 1);
           }
           if (!ok) break;
           mma_commit(bar(BAR_PFULL + b));
@@ -394,7 +403,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
         }
         if (cc + 2 < 4) tmem_ld_wait();
       }
-      const float rho = PROD ? sqrtf(rr) : 0.f;
+      const float rho = PROD ? sqrtf(rr) * a.rho_scale : 0.f;
 
       uint32_t zs[4] = {0u, 0u, 0u, 0u};
       if constexpr (PROD) {
@@ -462,8 +471,10 @@ cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, 
   if (te != cudaSuccess) return te;
   EncTcArgs a;
   a.lay = p->lay;
-  a.cp = p->cp;
-  a.px = p->px;
+  a.cp = p->cp_enc;
+  a.px = p->px_enc;
+  a.e2_single = p->hadamard;
+  a.rho_scale = p->rot_scale;
   a.G = G;
   a.N = N;
   a.nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;

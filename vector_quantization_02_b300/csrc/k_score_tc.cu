@@ -64,28 +64,53 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kIssuers = 4;
-constexpr int kExpWarps = 8;        // two expansion warpgroups
-constexpr int kEpiWarps = 8;        // two epilogue warpgroups
-constexpr int kThreads = 32 * (kIssuers + kExpWarps + kEpiWarps + 1);
-constexpr int kExpWarp0 = kIssuers, kEpiWarp0 = kIssuers + kExpWarps, kProducerWarp = kEpiWarp0 + kEpiWarps;
-constexpr int kStages = 8;          // packed-block ring (power of two)
-constexpr int kMaxGroups = 4;       // TMEM plane-slot groups (one tile each)
-constexpr int kMaxDStages = 4;      // accumulator stages
+constexpr int kMaxStages = 16;      // packed-block ring entries (a multiple of the warpgroups per role)
+constexpr int kMaxR = 4;            // TMEM tiles in flight: plane-slot groups = accumulator stages = R
+constexpr int kMaxIssuers = kMaxR;
 constexpr int kSlices = 4;          // e4m3 slices of the query operand
 constexpr int kPlaneCols = 32;      // TMEM columns of one expanded plane (128 e4m3)
 
+// MMA-term planes of an odd-symmetric codebook with k code bits.
+__host__ __device__ constexpr int planes_of(int k) { return k == 3 ? 4 : k; }
+
+// TMEM tiles in flight R for a plane-slot group of gcols columns and an
+// accumulator stage of dcols (512 columns in all); 0 if not even two fit.
+__host__ __device__ constexpr int tiles_in_flight(int gcols, int dcols) {
+  return 4 * (gcols + dcols) <= 512 ? 4 : 3 * (gcols + dcols) <= 512 ? 3 : 2 * (gcols + dcols) <= 512 ? 2 : 0;
+}
+
+// Roles of the kernel for H_p heads, k code bits, Prod or MSE.  Tile i of a
+// CTA's range uses TMEM entry i % R (its plane slots and accumulators), MMA
+// issuer i % I, expansion warpgroup i % WE, epilogue warpgroup i % WP and
+// packed-block slot i % stages, with I, WE and WP dividing R and WE dividing
+// stages: every entry of every ring then has a single waiter per role, which
+// waits for each of its phases in turn.  (A parity wait cannot tell phase k
+// from k - 2 or k + 2, so a waiter that skipped phases could take a stale
+// completion for the one it wants.)
+template <int HP, int K, int PROD>
+struct TcRoles {
+  static constexpr int N = kSlices * HP;
+  static constexpr int NA = planes_of(K), NP = NA + PROD, NJ = 1 + PROD;
+  // (a shape where fewer than two tiles fit is never launched: fits is false)
+  static constexpr bool fits = tiles_in_flight(NP * kPlaneCols, NJ * N) >= 2;
+  static constexpr int R = fits ? tiles_in_flight(NP * kPlaneCols, NJ * N) : 2;
+  static constexpr int I = R;                     // MMA issuers
+  static constexpr int WE = R == 3 ? 3 : 2;       // expansion warpgroups
+  static constexpr int WP = R;                    // epilogue warpgroups (the slower role)
+  static constexpr int kExpWarp0 = I, kEpiWarp0 = I + 4 * WE, kProducerWarp = I + 4 * WE + 4 * WP;
+  static constexpr int kThreads = 32 * (kProducerWarp + 1);
+};
+
 enum {
   BAR_FULL = 0,
-  BAR_EMPTY = BAR_FULL + kStages,
-  BAR_BFULL = BAR_EMPTY + kStages,
+  BAR_EMPTY = BAR_FULL + kMaxStages,
+  BAR_BFULL = BAR_EMPTY + kMaxStages,
   BAR_BEMPTY = BAR_BFULL + 2,
   BAR_PFULL = BAR_BEMPTY + 2,
-  BAR_PEMPTY = BAR_PFULL + kMaxGroups,
-  BAR_DFULL = BAR_PEMPTY + kMaxGroups,
-  BAR_DEMPTY = BAR_DFULL + kMaxDStages,
-  BAR_DONE = BAR_DEMPTY + kMaxDStages,
-  BAR_COUNT = BAR_DONE + kIssuers
+  BAR_MDONE = BAR_PFULL + kMaxR,   // a tile's MMAs complete: plane slots free, accumulators full
+  BAR_DEMPTY = BAR_MDONE + kMaxR,
+  BAR_DONE = BAR_DEMPTY + kMaxR,
+  BAR_COUNT = BAR_DONE + kMaxIssuers
 };
 
 // reciprocal of the e4m3 value of bit 3 + i of a byte (2^-6, 2^-5, 2^-3, 2)
@@ -93,14 +118,10 @@ __constant__ float c_comp[4] = {64.f, 32.f, 8.f, 0.5f};
 // source bit (within each byte of the plane word) of expanded word o
 __constant__ int c_src[8] = {3, 4, 5, 6, 0, 1, 2, 7};
 
-// MMA-term planes of an odd-symmetric codebook with k code bits.
-__host__ __device__ constexpr int planes_of(int k) { return k == 3 ? 4 : k; }
-
 struct ScoreTcArgs {
   Layout lay;
   int H, Hp;                  // heads, padded heads (4, 8 or 16)
-  int SG, DS;                 // TMEM plane-slot groups, accumulator stages
-  uint32_t slot0;             // first slot column (groups of NP x 32 columns)
+  uint32_t stages;            // packed-block ring entries (a multiple of the warpgroups per role)
   uint32_t img_bytes;         // per group: planes x (4 Hp rows x 128 B)
   int64_t N, nb, n_tiles;
   const uint8_t* packed;
@@ -217,6 +238,27 @@ __device__ __forceinline__ void load_terms(uint32_t taddr, float (&accA)[HP], fl
     }
 }
 
+// One term's accumulators (N <= 32 columns), every TMEM load issued before a
+// single wait: acc[h] = sum over slices of D[slice * HP + h] / 16^slice.
+template <int HP>
+__device__ __forceinline__ void load_term_all(uint32_t taddr, float (&acc)[HP]) {
+  constexpr int N = kSlices * HP;
+  static_assert(N <= 32, "at most 32 columns in flight");
+  uint32_t v[N / 16][16];
+#pragma unroll
+  for (int c = 0; c < N / 16; ++c) tmem_ld16(taddr + 16 * c, v[c]);
+  tmem_ld_wait();
+#pragma unroll
+  for (int h = 0; h < HP; ++h) acc[h] = 0.f;
+#pragma unroll
+  for (int c = 0; c < N / 16; ++c)
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int col = 16 * c + e, sl = col / HP, h = col % HP;
+      acc[h] = fmaf(__uint_as_float(v[c][e]), slice_weight(sl), acc[h]);
+    }
+}
+
 // Tokens' accumulators of one term: sum over slices of D[slice * HP + h] / 16^slice.
 template <int HP>
 __device__ __forceinline__ void load_term(uint32_t taddr, float (&acc)[HP]) {
@@ -237,45 +279,63 @@ __device__ __forceinline__ void load_term(uint32_t taddr, float (&acc)[HP]) {
   }
 }
 
+// One job's MMAs for one tile: planes [P0, P1) x 4 K steps into one
+// accumulator.  Every operand is a per-tile base plus a compile-time offset,
+// so the issuing thread does no address arithmetic between MMAs (a thread
+// that computes its descriptors between MMAs issues one only every ~250
+// cycles; this form, ~60).
+template <int P0, int P1, int N>
+__device__ __forceinline__ void issue_job(uint32_t d, uint32_t at, uint64_t b, uint32_t idesc) {
+#pragma unroll
+  for (int p = P0; p < P1; ++p)
+#pragma unroll
+    for (uint32_t kb = 0; kb < 4; ++kb)
+      // plane p of the image: N rows x 128 B (one swizzle atom column), p N 128
+      // bytes in; K step kb starts 32 bytes further (descriptor units of 16 B)
+      mma_f8_ts(d, at + (uint32_t)(p * kPlaneCols) + 8u * kb,
+                b + (uint64_t)(((uint32_t)p * (uint32_t)N * 128u) >> 4) + 2u * kb, idesc,
+                (p > P0 || kb > 0) ? 1u : 0u);
+}
+
 template <int HP, int K, int PROD>
-__global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs a) {
-  constexpr int N = kSlices * HP;               // MMA N: slice-major rows of the query image
-  constexpr int NA = planes_of(K);              // MMA-term planes
-  constexpr int NP = NA + PROD;                 // planes per tile
-  constexpr int NJ = 1 + PROD;                  // MMA jobs per tile
-  constexpr uint32_t kStageMask = kStages - 1;
+__global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_kernel(const ScoreTcArgs a) {
+  using Cfg = TcRoles<HP, K, PROD>;
+  constexpr int N = Cfg::N, NA = Cfg::NA, NP = Cfg::NP, NJ = Cfg::NJ;
+  constexpr uint32_t R = Cfg::R, I = Cfg::I, WE = Cfg::WE, WP = Cfg::WP;
+  constexpr int kExpWarp0 = Cfg::kExpWarp0, kEpiWarp0 = Cfg::kEpiWarp0, kProducerWarp = Cfg::kProducerWarp;
+  static_assert(R >= 2 && R % I == 0 && R % WE == 0 && R % WP == 0, "ring entries must have a single waiter each");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
+  const uint32_t n_stages = a.stages;
   const uint32_t off_ring = 2 * a.img_bytes;
   const uint32_t blk_bytes = (uint32_t)a.lay.block_bytes;
-  const uint32_t off_bar = (off_ring + kStages * blk_bytes + 7) & ~7u;
+  const uint32_t off_bar = (off_ring + n_stages * blk_bytes + 7) & ~7u;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ float4 s_cst[kEpiWarps][HP];  // constants of each epilogue warp's current tile
+  __shared__ float4 s_cst[4 * WP][HP];  // per-head constants of each epilogue warp's current group
   auto bar = [&](int i) { return sb + off_bar + 8u * (uint32_t)i; };
+  // TMEM: accumulators of entry r at r NJ N; plane slots of entry r at kSlot0 + r NP 32
+  constexpr uint32_t kSlot0 = R * (uint32_t)(NJ * N);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t SG = (uint32_t)a.SG, DS = (uint32_t)a.DS, nb = (uint32_t)a.nb;
+  const uint32_t nb = (uint32_t)a.nb;
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (uint32_t s = 0; s < n_stages; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
-      mbar_init(bar(BAR_EMPTY + s), 256);  // one expansion and one epilogue warpgroup
+      mbar_init(bar(BAR_EMPTY + s), 128);  // the expansion warpgroup that read it
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(BAR_BFULL + b), 1);
-      mbar_init(bar(BAR_BEMPTY + b), kIssuers);
+      mbar_init(bar(BAR_BEMPTY + b), I);
     }
-    for (int s = 0; s < kMaxGroups; ++s) {
-      mbar_init(bar(BAR_PFULL + s), 128);
-      mbar_init(bar(BAR_PEMPTY + s), NJ);
+    for (uint32_t r = 0; r < R; ++r) {
+      mbar_init(bar(BAR_PFULL + r), 128);
+      mbar_init(bar(BAR_MDONE + r), 1);
+      mbar_init(bar(BAR_DEMPTY + r), 128);
     }
-    for (int d = 0; d < kMaxDStages; ++d) {
-      mbar_init(bar(BAR_DFULL + d), NJ);
-      mbar_init(bar(BAR_DEMPTY + d), 128);
-    }
-    for (int w = 0; w < kIssuers; ++w) mbar_init(bar(BAR_DONE + w), 1);
+    for (uint32_t w = 0; w < I; ++w) mbar_init(bar(BAR_DONE + w), 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -302,14 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
       // the first ring's worth of packed blocks does not depend on the query
       // preparation: it streams while that kernel still runs (programmatic
       // dependent launch); the query images wait for it to complete
-      const uint32_t pre = n_my < (uint32_t)kStages ? n_my : (uint32_t)kStages;
+      const uint32_t pre = n_my < n_stages ? n_my : n_stages;
       for (uint32_t i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(bar(BAR_FULL + i), blk_bytes);
         bulk_load(sb + off_ring + i * blk_bytes, src + (int64_t)i * blk_bytes, blk_bytes, bar(BAR_FULL + i));
       }
       issued = pre;
       grid_dependency_wait();
-      for (uint32_t i = 0; i < n_my; ++i, src += blk_bytes) {
+      Ring slot;  // packed-block slot of tile i
+      for (uint32_t i = 0; i < n_my; ++i, src += blk_bytes, slot.advance(1, n_stages)) {
         if (i > 0) {
           const uint32_t g0 = pos.g;
           pos.advance(1, nb);
@@ -326,35 +387,40 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
           have_img = true;
         }
         if (i < pre) continue;  // issued above
-        const uint32_t s = i & kStageMask;
-        if (!mbar_wait_suspend(bar(BAR_EMPTY + s), ((i / kStages) & 1u) ^ 1u, abort)) {
+        if (!mbar_wait_suspend(bar(BAR_EMPTY + slot.idx), slot.phase ^ 1u, abort)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(BAR_FULL + s), blk_bytes);
-        bulk_load(sb + off_ring + s * blk_bytes, src, blk_bytes, bar(BAR_FULL + s));
+        mbar_arrive_expect_tx(bar(BAR_FULL + slot.idx), blk_bytes);
+        bulk_load(sb + off_ring + slot.idx * blk_bytes, src, blk_bytes, bar(BAR_FULL + slot.idx));
         issued = i + 1;
       }
       if (!ok) raise(a.err, abort);
       // no copy may still be landing when the CTA exits
       int dummy = 0;
-      for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        mbar_wait(bar(BAR_FULL + (i & kStageMask)), (i / kStages) & 1u, &dummy);
+      for (uint32_t i = issued > n_stages ? issued - n_stages : 0; i < issued; ++i)
+        mbar_wait(bar(BAR_FULL + i % n_stages), (i / n_stages) & 1u, &dummy);
       if (have_img) {
         for (uint32_t e = epoch > 0 ? epoch - 1 : 0; e <= epoch; ++e)
           mbar_wait(bar(BAR_BFULL + (e & 1u)), (e >> 1) & 1u, &dummy);
       }
     }
-  } else if (warp < kIssuers) {
+  } else if (warp < (int)I) {
     // ------------------------------------------------------------ MMA issuers
+    // warp w issues every MMA of the tiles i with i % I == w (TMEM entries
+    // i % R), then one commit: the tile's plane slots are free and its
+    // accumulators full (the expansion and the epilogue of that entry both
+    // wait on it, each for every phase in turn)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3(128, N);
+      // descriptors of the two query-image buffers, computed once
+      const uint64_t bdesc0 = sdesc_k_sw128(sb), bdesc1 = sdesc_k_sw128(sb + a.img_bytes);
       TilePos pos;
       pos.init(t_begin, a.nb);
       uint32_t epoch = 0;
-      Ring group, stage;  // plane-slot group and accumulator stage of tile i
+      Ring ent;  // TMEM entry of tile i
       bool need_b = true, ok = true;
-      for (uint32_t i = 0; ok && i < n_my; ++i, group.advance(1, SG), stage.advance(1, DS)) {
+      for (uint32_t i = 0; ok && i < n_my; ++i, ent.advance(1, R)) {
         if (i > 0) {
           const uint32_t g0 = pos.g;
           pos.advance(1, nb);
@@ -365,40 +431,30 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
             need_b = true;
           }
         }
-        for (int job = 0; job < NJ; ++job) {
-          // tile i's term jobs: warps 2 (i % 2) + job (the only waiters on its ring entries)
-          if ((uint32_t)(2 * (i & 1) + job) != (uint32_t)warp) continue;
-          if (need_b) {
-            if (!mbar_wait_suspend(bar(BAR_BFULL + (epoch & 1u)), (epoch >> 1) & 1u, abort)) {
-              ok = false;
-              break;
-            }
-            need_b = false;
-          }
-          if (!mbar_wait_suspend(bar(BAR_PFULL + group.idx), group.phase, abort) ||
-              !mbar_wait_suspend(bar(BAR_DEMPTY + stage.idx), stage.phase ^ 1u, abort)) {
+        // every issuer waits for every group's image, owning tiles there or
+        // not, so that it sees each phase of the image barriers in turn
+        if (need_b) {
+          if (!mbar_wait_suspend(bar(BAR_BFULL + (epoch & 1u)), (epoch >> 1) & 1u, abort)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t img = sb + (epoch & 1u) * a.img_bytes;
-          const uint32_t d = tmem + stage.idx * (uint32_t)(NJ * N) + (uint32_t)(job * N);
-          const uint32_t at = tmem + a.slot0 + group.idx * (uint32_t)(NP * kPlaneCols);
-          const int p0 = job == 0 ? 0 : NA, p1 = job == 0 ? NA : NP;
-#pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            if (p < p0 || p >= p1) continue;
-            // plane p of the image: N rows x 128 B (one swizzle atom column);
-            // K step kb starts 32 bytes further (2 in descriptor units)
-            const uint64_t b0 = sdesc_k_sw128(img + (uint32_t)p * (uint32_t)N * 128u);
-#pragma unroll
-            for (uint32_t kb = 0; kb < 4; ++kb)
-              mma_f8_ts(d, at + (uint32_t)(p * kPlaneCols) + 8u * kb, b0 + 2u * kb, idesc,
-                        (p > p0 || kb > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(BAR_PEMPTY + group.idx));
-          mma_commit(bar(BAR_DFULL + stage.idx));
+          need_b = false;
         }
+        if (i % I != (uint32_t)warp) continue;
+        // polled without a suspend hint: the issuer is the chain's critical
+        // step, and there are at most four of them
+        if (!mbar_wait(bar(BAR_PFULL + ent.idx), ent.phase, abort) ||
+            !mbar_wait(bar(BAR_DEMPTY + ent.idx), ent.phase ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + ent.idx * (uint32_t)(NJ * N);
+        const uint32_t at = tmem + kSlot0 + ent.idx * (uint32_t)(NP * kPlaneCols);
+        const uint64_t b = (epoch & 1u) ? bdesc1 : bdesc0;
+        issue_job<0, NA, N>(d, at, b, idesc);
+        if constexpr (PROD) issue_job<NA, NP, N>(d + (uint32_t)N, at, b, idesc);
+        mma_commit(bar(BAR_MDONE + ent.idx));
       }
       if (!ok) raise(a.err, abort);
       mma_commit(bar(BAR_DONE + warp));
@@ -407,19 +463,22 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ expansion
+    // Thread (warp w, lane l) owns key row 32 (w % 4) + l of the tiles i with
+    // i % WE == wg.  It reads the key's plane chunks from the staged block,
+    // frees the ring entry at once and writes the expanded planes to TMEM.
     const uint32_t wg = (uint32_t)(warp - kExpWarp0) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + a.slot0;
-    Ring group;
-    group.advance(wg, SG);
-    for (uint32_t i = wg; i < n_my; i += 2, group.advance(2, SG)) {
-      const uint32_t s = i & kStageMask;
-      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_FULL + s), (i / kStages) & 1u, abort))) {
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + kSlot0;
+    Ring ent, slot;
+    ent.advance(wg, R);
+    slot.advance(wg, n_stages);
+    for (uint32_t i = wg; i < n_my; i += WE, ent.advance(WE, R), slot.advance(WE, n_stages)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_FULL + slot.idx), slot.phase, abort))) {
         raise(a.err, abort);
         break;
       }
-      const uint8_t* blkp = smem + off_ring + s * blk_bytes;
+      const uint8_t* blkp = smem + off_ring + slot.idx * blk_bytes;
       uint4 w[NP];
 #pragma unroll
       for (int q = 0; q < K; ++q) w[q] = *reinterpret_cast<const uint4*>(blkp + ((q * kTokensPerBlock) + row) * 16);
@@ -428,13 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
                           w[0].w ^ w[1].w ^ w[2].w);
       }
       if constexpr (PROD) w[NA] = *reinterpret_cast<const uint4*>(blkp + ((K * kTokensPerBlock) + row) * 16);
-      mbar_arrive(bar(BAR_EMPTY + s));
-      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_PEMPTY + group.idx), group.phase ^ 1u, abort))) {
+      mbar_arrive(bar(BAR_EMPTY + slot.idx));
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_MDONE + ent.idx), ent.phase ^ 1u, abort))) {
         raise(a.err, abort);
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = lane_base + group.idx * (uint32_t)(NP * kPlaneCols);
+      const uint32_t taddr = lane_base + ent.idx * (uint32_t)(NP * kPlaneCols);
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
         uint32_t o[32];
@@ -446,11 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(BAR_PFULL + group.idx));
+      mbar_arrive(bar(BAR_PFULL + ent.idx));
     }
   } else {
     // ------------------------------------------------------------ epilogue
     grid_dependency_wait();  // the per-head constants come from the query preparation
+    // Thread (warp w, lane l) owns key row 32 (w % 4) + l of the tiles i with
+    // i % WP == eg.  The key's norms come straight from the packed block in
+    // global memory (one 8-byte load, issued before the accumulator wait; the
+    // block has just been streamed, so it is read from L2).
     const uint32_t eg = (uint32_t)(warp - kEpiWarp0) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
@@ -458,38 +521,39 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
     float4* wcst = s_cst[warp - kEpiWarp0];
     TilePos pos;
     pos.init(t_begin + eg, a.nb);
-    Ring stage;
-    stage.advance(eg, DS);
-    for (uint32_t i = eg; i < n_my; i += 2, stage.advance(2, DS)) {
-      if (i != eg) pos.advance(2, nb);
+    Ring ent;
+    ent.advance(eg, R);
+    uint32_t cst_g = 0xffffffffu;  // group whose per-head constants wcst holds
+    const uint8_t* norm_src = a.packed + (t_begin + eg) * a.lay.block_bytes + a.lay.norms_off + row * 8;
+    for (uint32_t i = eg; i < n_my; i += WP, ent.advance(WP, R), norm_src += WP * a.lay.block_bytes) {
+      if (i != eg) pos.advance(WP, nb);
+      const float2 nr = __ldg(reinterpret_cast<const float2*>(norm_src));
       const int64_t tok = (int64_t)pos.blk * kTokensPerBlock + row;
-      // this tile's per-head constants (each warp keeps its own copy) and norms
-      const float4 my_cst = lane < HP ? __ldg(a.consts + (int64_t)pos.g * a.Hp + lane) : make_float4(0, 0, 0, 0);
-      const uint32_t s = i & kStageMask;
-      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_FULL + s), (i / kStages) & 1u, abort))) {
-        raise(a.err, abort);
-        break;
+      if (pos.g != cst_g) {  // a new group: its per-head constants (each warp keeps its own copy)
+        __syncwarp();        // every lane has read the previous group's
+        if (lane < HP) wcst[lane] = __ldg(a.consts + (int64_t)pos.g * a.Hp + lane);
+        __syncwarp();
+        cst_g = pos.g;
       }
-      const float2 nr = *reinterpret_cast<const float2*>(smem + off_ring + s * blk_bytes + a.lay.norms_off + row * 8);
-      mbar_arrive(bar(BAR_EMPTY + s));
-      if (lane < HP) wcst[lane] = my_cst;
-      __syncwarp();
-
-      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_DFULL + stage.idx), stage.phase, abort))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_MDONE + ent.idx), ent.phase, abort))) {
         raise(a.err, abort);
         break;
       }
       tc_fence_after();
-      const uint32_t d = lane_base + stage.idx * (uint32_t)(NJ * N);
+      const uint32_t d = lane_base + ent.idx * (uint32_t)(NJ * N);
       float accA[HP], accB[HP];
-      if constexpr (NJ * N <= 64) {
+      // at most 32 accumulator registers in flight
+      if constexpr (NJ * N <= 32) {
         load_terms<HP, NJ>(d, accA, accB);
+      } else if constexpr (N <= 32) {
+        load_term_all<HP>(d, accA);
+        if constexpr (PROD) load_term_all<HP>(d + N, accB);
       } else {
         load_term<HP>(d, accA);
         if constexpr (PROD) load_term<HP>(d + N, accB);
       }
       tc_fence_before();
-      mbar_arrive(bar(BAR_DEMPTY + stage.idx));
+      mbar_arrive(bar(BAR_DEMPTY + ent.idx));
       if (tok < a.N) {
         const float rk = nr.y * a.kappa;
         float* out = a.logits + ((int64_t)pos.g * a.H) * a.N + tok;
@@ -503,7 +567,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(const ScoreTcArgs
           }
         }
       }
-      __syncwarp();  // every lane has read wcst before the next tile overwrites it
     }
   }
 
@@ -677,8 +740,8 @@ bool standard_masks(const ParityExpansion& px, int k) {
 }
 
 struct TcGeom {
-  int Hp, N, nA, nP, SG, DS;
-  uint32_t slot0, img, smem;
+  int Hp, N, nA, nP, R;
+  uint32_t img, smem, stages;
 };
 
 bool tc_geom(const tq_plan* p, int H, TcGeom* gm) {
@@ -689,28 +752,24 @@ bool tc_geom(const tq_plan* p, int H, TcGeom* gm) {
   gm->N = kSlices * gm->Hp;
   gm->nA = planes_of(k);
   gm->nP = gm->nA + p->lay.prod;
-  const int dcols = (1 + p->lay.prod) * gm->N;  // accumulator columns of one tile
-  const int gcols = gm->nP * kPlaneCols;        // plane columns of one tile
-  // even ring sizes (see the kernel's comment), the deepest that fit
-  const int cand[3][2] = {{4, 2}, {2, 4}, {2, 2}};
-  gm->SG = gm->DS = 0;
-  for (const auto& c : cand) {
-    if (c[0] * gcols + c[1] * dcols <= 512) {
-      gm->SG = c[0];
-      gm->DS = c[1];
-      break;
-    }
-  }
-  if (gm->SG < 2 || gm->DS < 2) return false;
-  gm->slot0 = (uint32_t)(gm->DS * dcols);
+  // TMEM tiles in flight, as the kernel's TcRoles computes them
+  gm->R = tiles_in_flight(gm->nP * kPlaneCols, (1 + p->lay.prod) * gm->N);
+  if (gm->R < 2) return false;
+  const uint32_t W = gm->R == 3 ? 3 : 2;  // expansion warpgroups (TcRoles::WE)
   gm->img = ((uint32_t)gm->nP * (uint32_t)gm->N * 128u + 1023u) & ~1023u;
-  const uint32_t ring = kStages * (uint32_t)p->lay.block_bytes;
-  gm->smem = 2 * gm->img + ring + BAR_COUNT * 8 + 16 + 1024;
-  return gm->smem <= 200 * 1024;
+  // the deepest packed-block ring (a multiple of the W warpgroups per role, at
+  // most 16 entries) that fits beside the two query images
+  for (uint32_t st = (kMaxStages / W) * W; st >= 2 * W; st -= W) {
+    gm->stages = st;
+    gm->smem = 2 * gm->img + st * (uint32_t)p->lay.block_bytes + BAR_COUNT * 8 + 16 + 1024;
+    if (gm->smem <= 190 * 1024) return true;
+  }
+  return false;
 }
 
 template <int HP, int K, int PROD>
 cudaError_t launch_kernel(const ScoreTcArgs& a, const TcGeom& gm, int64_t grid, cudaStream_t s) {
+  if (!TcRoles<HP, K, PROD>::fits) return cudaErrorInvalidValue;
   auto kern = score_tc_kernel<HP, K, PROD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gm.smem);
   if (e != cudaSuccess) return e;
@@ -718,7 +777,7 @@ cudaError_t launch_kernel(const ScoreTcArgs& a, const TcGeom& gm, int64_t grid, 
   // preparation runs; the roles that read its output wait for it
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(TcRoles<HP, K, PROD>::kThreads);
   cfg.dynamicSmemBytes = gm.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -779,9 +838,7 @@ cudaError_t launch_score_tc(const tq_plan* p, const float* queries, int64_t G, i
   a.lay = p->lay;
   a.H = H;
   a.Hp = gm.Hp;
-  a.SG = gm.SG;
-  a.DS = gm.DS;
-  a.slot0 = gm.slot0;
+  a.stages = gm.stages;
   a.img_bytes = gm.img;
   a.N = N;
   a.nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;

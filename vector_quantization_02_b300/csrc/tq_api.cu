@@ -110,9 +110,21 @@ cudaError_t build_tc_ops(tq_plan* p) {
   if (e == cudaSuccess && prod) e = cudaMemcpy(M.data(), p->M, M.size() * 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && prod) e = cudaMemcpy(S.data(), p->S, S.size() * 4, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return e;
-  split_images<__half>(Pi.data(), host.data(), host.data() + img);
-  split_images<__nv_bfloat16>(Pi.data(), host.data() + 2 * img, host.data() + 3 * img);
-  if (prod) split_images<__nv_bfloat16>(M.data(), host.data() + 4 * img, host.data() + 5 * img);
+  if (p->hadamard) {
+    // the encode's rotation operand is the +-1 matrix Pi / c (exact in fp16
+    // and bf16; the lo images stay zero), and its E5 operand c M: the encode
+    // then works on y / c, with the codebook divided by c (cp_enc, px_enc)
+    std::vector<float> U(128 * 128), cM(prod ? 128 * 128 : 0);
+    for (int i = 0; i < 128 * 128; ++i) U[i] = Pi[i] < 0.f ? -1.f : 1.f;
+    for (size_t i = 0; i < cM.size(); ++i) cM[i] = p->rot_scale * M[i];
+    split_images<__half>(U.data(), host.data(), host.data() + img);
+    split_images<__nv_bfloat16>(U.data(), host.data() + 2 * img, host.data() + 3 * img);
+    if (prod) split_images<__nv_bfloat16>(cM.data(), host.data() + 4 * img, host.data() + 5 * img);
+  } else {
+    split_images<__half>(Pi.data(), host.data(), host.data() + img);
+    split_images<__nv_bfloat16>(Pi.data(), host.data() + 2 * img, host.data() + 3 * img);
+    if (prod) split_images<__nv_bfloat16>(M.data(), host.data() + 4 * img, host.data() + 5 * img);
+  }
   // decode B operands: row j of the image holds column j of Pi (of S), scaled by 2^8
   std::vector<float> T(128 * 128);
   auto transposed_scaled = [&](const std::vector<float>& A) {
@@ -245,8 +257,14 @@ int tq_encode_path(const tq_plan* p, tq_dtype dt) {
   return TQ_EUNSUPPORTED;
 }
 
-tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
-                         void* stream, tq_plan** out) {
+}  // extern "C"
+
+namespace {
+
+// Plan creation shared by tq_plan_create and tq_plan_create_hadamard; a
+// Hadamard plan passes hadamard = 1 (Pi already holds c H diag(signs)).
+tq_status create_plan(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
+                      void* stream, int hadamard, tq_plan** out) {
   if (!out) return TQ_EINVAL;
   *out = nullptr;
   if (d < 128 || d > kMaxD || d % 128 != 0) return TQ_EINVAL;
@@ -273,6 +291,8 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
   L.norms_off = (int64_t)L.planes * L.C * kTokensPerBlock * 16;
   L.block_bytes = L.norms_off + kTokensPerBlock * 8;
   p->kappa = (float)(std::sqrt(M_PI / 2.0) / d);
+  p->hadamard = hadamard;
+  p->rot_scale = hadamard ? (float)(1.0 / std::sqrt((double)d)) : 1.f;
 
   const size_t mat = (size_t)d * d * sizeof(float);
   bool ok = cudaMalloc(&p->Pi, mat) == cudaSuccess && cudaMalloc(&p->PiT, mat) == cudaSuccess &&
@@ -326,6 +346,21 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
     p->px.c0 = (float)c0;
     p->px.mid = (float)mid;
   }
+  // the codebook as the d = 128 encode compares it: divided by the rotation's
+  // scale for a Hadamard plan (the encode works on y / c there)
+  p->cp_enc = p->cp;
+  p->px_enc = p->px;
+  if (hadamard) {
+    const float c = p->rot_scale;
+    for (int i = 0; i < kMaxLevels; ++i) p->cp_enc.c[i] = p->cp.c[i] / c;
+    for (int i = 0; i + 1 < kMaxLevels; ++i) p->cp_enc.t[i] = p->cp.t[i] / c;
+    for (int i = 0; i < kMaxTerms; ++i) {
+      p->px_enc.coef[i] = p->px.coef[i] / c;
+      p->px_enc.half[i] = p->px.half[i] / c;
+    }
+    p->px_enc.c0 = p->px.c0 / c;
+    p->px_enc.mid = p->px.mid / c;
+  }
   if (d == 128) {
     if (build_tc_ops(p) != cudaSuccess) {
       free_plan(p);
@@ -341,6 +376,45 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
   }
   *out = p;
   return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
+                         void* stream, tq_plan** out) {
+  return create_plan(d, bits, mode, Pi, S, codebook, stream, 0, out);
+}
+
+tq_status tq_plan_create_hadamard(int d, int bits, tq_mode mode, const float* signs, const float* S,
+                                  const float* codebook, void* stream, tq_plan** out) {
+  if (!out) return TQ_EINVAL;
+  *out = nullptr;
+  if (d < 128 || d > kMaxD || (d & (d - 1)) != 0 || !signs) return TQ_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<float> sg(d), Pi((size_t)d * d);
+  if (cudaMemcpyAsync(sg.data(), signs, d * sizeof(float), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return TQ_ECUDA;
+  for (int j = 0; j < d; ++j)
+    if (sg[j] != 1.f && sg[j] != -1.f) return TQ_EINVAL;
+  // Pi[i][j] = c (-1)^popcount(i & j) signs[j], c = 1/sqrt(d) rounded once to fp32
+  const float c = (float)(1.0 / std::sqrt((double)d));
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < d; ++j) Pi[(size_t)i * d + j] = (__builtin_popcount((unsigned)(i & j)) & 1 ? -c : c) * sg[j];
+  float* Pi_d = nullptr;
+  if (cudaMalloc(&Pi_d, Pi.size() * sizeof(float)) != cudaSuccess) {
+    cudaGetLastError();
+    return TQ_ENOMEM;
+  }
+  tq_status st = cudaMemcpyAsync(Pi_d, Pi.data(), Pi.size() * sizeof(float), cudaMemcpyHostToDevice, s) ==
+                         cudaSuccess
+                     ? create_plan(d, bits, mode, Pi_d, S, codebook, stream, 1, out)
+                     : TQ_ECUDA;
+  cudaStreamSynchronize(s);
+  cudaFree(Pi_d);
+  return st;
 }
 
 tq_status tq_plan_destroy(tq_plan* plan) {

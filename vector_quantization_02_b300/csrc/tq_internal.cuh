@@ -63,6 +63,10 @@ struct tq_plan {
   tq::CodeParams cp;
   tq::ParityExpansion px;  // codebook in parity form (tensor-core score)
   float kappa;        // sqrt(pi/2) / m
+  int hadamard;       // 1: Pi = c H diag(signs), c = 1/sqrt(d) (tq_plan_create_hadamard)
+  float rot_scale;    // c for a Hadamard plan, else 1
+  tq::CodeParams cp_enc;       // the codebook as the d = 128 encode uses it: divided by c (Hadamard)
+  tq::ParityExpansion px_enc;  // the same for the parity expansion
   float* Pi;          // [d][d] row-major, y = Pi u
   float* PiT;         // [d][d] = Pi^T (coalesced column access in SIMT kernels)
   float* S;           // [d][d] (PROD)
