@@ -262,6 +262,89 @@ def encode_only_leg(w, bits: int, mode: str, rotation: str, keys, flush, reps: i
     return out
 
 
+def attend_leg(w, kplan, packed_k, q, flush, reps: int, lead):
+    """tq_attend (one decode step of attention on the compressed cache) on the
+    workload's keys and values drawn by the same generator (seed offset 7),
+    values in a 3-bit TurboQuantMSE plan, scale 1/sqrt(d); cold L2."""
+    import vector_quantization_02_b300 as tq
+    G, N, H, d = w.G, w.N, w.H, w.d
+    vbits = 3
+    vplan = tq.Plan.from_seeds(d, vbits, tq_synth.rotation_gaussian(d, w.seeds["rotation"] + 1000), None, mode="mse")
+    vals = tq_synth.keys(w, device=q.device, seed_offset=7)
+    packed_v = tq.tq_encode_values(vplan, vals)
+    del vals
+    out = torch.empty(G, H, d, dtype=torch.float32, device=q.device)
+    ws = torch.empty(tq.attend_workspace_bytes(kplan, vplan, G, H, N), dtype=torch.uint8, device=q.device)
+    scale = 1.0 / d ** 0.5
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        tq.tq_attend(kplan, vplan, q, packed_k, packed_v, N, scale, out=out, workspace=ws)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        lead(300)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        tq.tq_attend(kplan, vplan, q, packed_k, packed_v, N, scale, out=out, workspace=ws)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    assert kplan.status() == 0 and vplan.status() == 0
+    ms = statistics.median(a.elapsed_time(b) for a, b in times)
+    # algorithmic bytes: the packed keys and values once, queries in, outputs out
+    nbytes = kplan.packed_bytes(G, N) + vplan.packed_bytes(G, N) + q.numel() * 4 + out.numel() * 4
+    r = {"value_bits": vbits, "ms_cold_l2": round(ms, 5), "tokens_per_s": G * N / (ms * 1e-3),
+         "roofline_cold_l2": roofline(nbytes, ms, "attend", "k_attend.cu", w.name),
+         "launches": 4, "reps": reps,
+         "note": "query preparation + score (logits to the workspace) + value contraction + split combine"}
+    vplan.close()
+    return r
+
+
+def fractional_leg(w, keys, q, half_bits: int, flush, reps: int, lead):
+    """Encode and score (cold L2) of the step's keys at a fractional width:
+    half_bits / 2 bits per channel, the first d/2 rotated coordinates with
+    one more Lloyd-Max bit (dense rotation of the workload's seed)."""
+    import vector_quantization_02_b300 as tq
+    G, N, H, d = w.G, w.N, w.H, w.d
+    k_hi = (half_bits + 1) // 2 - 1
+    Pi = tq.tq_haar_rotation(tq_synth.rotation_gaussian(d, w.seeds["rotation"]))
+    plan = tq.Plan.fractional(d, half_bits, Pi, tq_synth.projection(d, w.seeds["projection"]),
+                              tq.tq_lloyd_max_codebook(1 << k_hi, d), tq.tq_lloyd_max_codebook(1 << (k_hi - 1), d))
+    packed = torch.empty(plan.packed_bytes(G, N), dtype=torch.uint8, device=q.device)
+    logits = torch.empty(G, H, N, dtype=torch.float32, device=q.device)
+    ws = torch.empty(tq.score_workspace_bytes(plan, G, H, N), dtype=torch.uint8, device=q.device)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            lead(300)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+    enc_ms = timed(lambda: tq.tq_encode(plan, keys, packed=packed))
+    sc_ms = timed(lambda: tq.tq_score(plan, q, packed, N, logits=logits, workspace=ws))
+    assert plan.status() == 0
+    P = plan.packed_bytes(G, N)
+    out = {"bits_per_channel": half_bits / 2, "bytes_per_key": P // (G * (-(-N // 128)) * 128),
+           "encode_ms_cold_l2": round(enc_ms, 5), "score_ms_cold_l2": round(sc_ms, 5),
+           "encode_roofline_cold_l2": roofline(keys.numel() * keys.element_size() + P, enc_ms, "encode_tc",
+                                               "k_encode_tc.cu", w.name, flops=2 * 2 * d * d * G * N),
+           "score_roofline_cold_l2": roofline(P + G * H * N * 4 + q.numel() * 4, sc_ms, "score_tc", "k_score_tc.cu",
+                                              w.name, flops=2 * 2 * d * H * G * N), "reps": reps}
+    plan.close()
+    return out
+
+
 def score_only_leg(name: str, bits: int, flush, reps: int, dev, lead):
     """tq_score alone on a second workload, cold L2: the keys are encoded once,
     64 groups at a time (untimed), then one query per head is scored against
@@ -508,6 +591,19 @@ def run_ours(args, world, rank):
                                 flops=(2 if plan.mode == "prod" else 1) * 2 * d * d * G * N)}
         del xh
 
+    # one decode step of attention on the same compressed keys and values
+    att = None
+    if d == 128 and args.mode == "prod" and not mse:
+        try:
+            att = attend_leg(w, plan, packed, q, flush, max(5, args.steps), lead)
+        except tq.TQError:
+            att = None  # a shape tq_attend does not take
+
+    # the same keys at a fractional width (3.5 bits per channel)
+    frac = None
+    if d == 128 and args.mode == "prod" and w.key_dtype != torch.float32 and H <= 16:
+        frac = fractional_leg(w, keys, q, 7, flush, max(5, args.steps), lead)
+
     # the same encode with the randomised Walsh-Hadamard rotation (or, when the
     # step itself uses it, with the dense rotation)
     other = "dense" if args.rotation == "hadamard" else "hadamard"
@@ -543,6 +639,8 @@ def run_ours(args, world, rank):
             "fp32_key_baseline": base,
             "decode": dec,
             f"encode_{other}": enc_other,
+            "attend": att,
+            "fractional_3p5": frac,
         },
         "e2e": None if e2e_ms is None else {
             "value": keys_total / (e2e_ms * 1e-3), "unit": "keys/s", "h2d_bytes_per_step": key_bytes + q_bytes,

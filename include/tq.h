@@ -128,6 +128,28 @@ tq_status tq_plan_create(int d, int bits, tq_mode mode, const float* Pi, const f
  * for a sign that is not +-1), TQ_ENOMEM, TQ_ECUDA. */
 tq_status tq_plan_create_hadamard(int d, int bits, tq_mode mode, const float* signs, const float* S,
                                   const float* codebook, void* stream, tq_plan** out);
+/* Create a plan at a fractional width ([TAMBUR]: KV caches at 3.5 bits per
+ * channel are quality-neutral, at 2.5 bits slightly degraded).  The pages do
+ * not say how the channels are split; this library's reading: the first d/2
+ * coordinates of the rotated vector take one more Lloyd-Max bit than the
+ * last d/2 (after the random rotation every coordinate has the same
+ * distribution), so the average is b + 1/2 bits per channel:
+ *   TQ_PROD: half_bits 5 (2.5) or 7 (3.5): 1/2 or 2/3 code bits + 1 QJL bit;
+ *   TQ_MSE:  half_bits 3 (1.5) or 5 (2.5): 1/2 or 2/3 code bits.
+ *   codebook_hi  device fp32, 2^k_hi ascending centroids (coordinates < d/2);
+ *   codebook_lo  device fp32, 2^(k_hi-1) ascending centroids (the others);
+ *   Pi, S: as tq_plan_create.
+ * Packed layout: as tq_packed_bytes describes, except that code plane k_hi - 1
+ * holds the first d/2 coordinates only: per 128 coordinates 8 bytes per token
+ * (coordinate 64 c + 32 w + i at bit i of little-endian word w of half chunk
+ * c), the 128 tokens' 8-byte half chunks in token order; the sign plane and
+ * the norms follow.  Bytes per key: 48 (2.5, Prod), 64 (3.5, Prod).
+ * Supported: d = 128; encode of fp16/bf16 keys, score with H <= 16, decode,
+ * all on the d = 128 tensor-core kernels (other calls: TQ_EUNSUPPORTED).
+ * Errors: TQ_EINVAL, TQ_ENOMEM, TQ_ECUDA. */
+tq_status tq_plan_create_fractional(int d, int half_bits, tq_mode mode, const float* Pi, const float* S,
+                                    const float* codebook_hi, const float* codebook_lo, void* stream,
+                                    tq_plan** out);
 tq_status tq_plan_destroy(tq_plan* plan);
 
 /* Bytes of the packed buffer for G groups of N tokens.  Layout ([P5] §3):
@@ -203,6 +225,43 @@ tq_status tq_score(const tq_plan* plan, const float* queries, int64_t n_groups, 
 tq_status tq_score_noalloc(const tq_plan* plan, const float* queries, int64_t n_groups, int n_heads,
                            const void* packed, int64_t n_tokens, float* logits, int top_k,
                            float* top_scores, int64_t* top_idx, void* stream);
+
+/* Encode value vectors for attention: the TurboQuantMSE encode of tq_encode
+ * ([PT-KR] 1단계; the pages' 3-bit KV figure compresses values too) written in
+ * the coordinate-major value layout that tq_attend reads: per 128-token block,
+ * for each code plane p (LSB first) and coordinate j, 16 bytes hold bit p of
+ * coordinate j of the block's 128 tokens (token t = bit t % 32 of
+ * little-endian word t / 32); then the 128 pairs {float ||v||, float 0}.  The
+ * same bytes per vector as tq_encode (tq_packed_bytes); the same bits,
+ * transposed within each block.
+ *   plan  a TQ_MSE plan.  values: device [G][N][d] fp32/fp16/bf16.
+ * Errors: as tq_encode; TQ_EINVAL for a TQ_PROD plan. */
+tq_status tq_encode_values(const tq_plan* plan, const void* values, tq_dtype dtype, int64_t n_groups,
+                           int64_t n_tokens, void* packed, void* stream);
+
+/* One decode step of attention on the compressed cache ([TAMBUR]: attention
+ * logits computed directly on the compressed keys; [P5] section 3: a dedicated
+ * kernel for the packed format):
+ *   out[g][h] = sum_t softmax_t(scale * logit[g][h][t]) v_hat[g][t],
+ * logit as tq_score computes it from the keys (kplan, TQ_PROD, packed by
+ * tq_encode), v_hat = ||v|| Pi_v^T c_v[idx] from the values (vplan, TQ_MSE,
+ * packed by tq_encode_values).  The pages name no scale: pass 1/sqrt(d) for
+ * the usual scaled dot-product attention.
+ *   queries device fp32 [G][H][d]; out device fp32 [G][H][d];
+ *   workspace device, >= tq_attend_workspace_bytes(...), 256-byte aligned
+ *   (it holds the logits on their way to the softmax: G*H*N*4 bytes and the
+ *   per-split partial sums).
+ * Supported: d = 128 for both plans; the key plan as tq_score's tensor-core
+ * path takes it; a value codebook of 2, 4 or 8 levels, odd-symmetric; H <= 8,
+ * or H <= 16 with at most 4 value levels.  Otherwise TQ_EUNSUPPORTED.
+ * Device errors go to the key plan's (score) and the value plan's
+ * (value contraction) error words.  Errors: TQ_EINVAL, TQ_EALIGN,
+ * TQ_EUNSUPPORTED, TQ_ECUDA. */
+size_t tq_attend_workspace_bytes(const tq_plan* kplan, const tq_plan* vplan, int64_t n_groups, int n_heads,
+                                 int64_t n_tokens);
+tq_status tq_attend(const tq_plan* kplan, const tq_plan* vplan, const float* queries, int64_t n_groups,
+                    int n_heads, const void* kpacked, const void* vpacked, int64_t n_tokens, float scale,
+                    float* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Reconstruct keys ([PT-KR] usage listing: ``tq.decompress``):
  * x_hat = n Pi^T c[idx] + rho sqrt(pi/2)/m S^T (2z - 1)  (TQ_MSE: first term),

@@ -429,6 +429,174 @@ def score_mse_rotated(q, idx, n, Pi, c) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# Fractional bit widths (2.5 / 3.5 bits per channel)
+#
+# [TAMBUR] reports quality-neutral KV caches at 3.5 bits per channel and a
+# small degradation at 2.5.  READING (the pages do not say how the channels
+# are split): b + 1/2 bits per channel on average, with the first d/2
+# coordinates of the rotated vector quantised with one more Lloyd-Max bit
+# than the other d/2.  After the random rotation every coordinate has the same
+# distribution, so which half gets the extra bit does not matter; the first
+# half is taken.  For TurboQuantProd the MSE stage is the mixed quantiser and
+# the QJL stage is unchanged (b + 1/2 = (b - 1/2) MSE bits + 1 QJL bit).
+# Parity of this reading is unpinned: only what the mathematics fixes is
+# pinned (uniform special cases, nearest centroid per coordinate, the
+# distortion as the mean of the two codebooks', unbiasedness).
+# ----------------------------------------------------------------------------
+
+def mixed_split(d: int) -> int:
+    """Rotated coordinates [0, d_hi) take the larger codebook (READING: d/2)."""
+    return d // 2
+
+
+def centroids_mixed(idx, c_hi, c_lo, d_hi: int) -> np.ndarray:
+    """c[idx] per coordinate: c_hi for coordinates < d_hi, c_lo for the rest."""
+    idx = np.asarray(idx)
+    out = np.empty(idx.shape, dtype=np.float64)
+    out[..., :d_hi] = _as64(c_hi)[idx[..., :d_hi]]
+    out[..., d_hi:] = _as64(c_lo)[idx[..., d_hi:]]
+    return out
+
+
+def encode_mse_mixed(x, Pi, c_hi, c_lo, d_hi: int) -> dict:
+    """TurboQuantMSE with two codebooks: normalise, rotate, quantise
+    coordinate j < d_hi with c_hi and the others with c_lo (nearest centroid,
+    ties to the lower index).  Returns idx, n, y and the boundary-band mask."""
+    x = _as64(x)
+    n = np.sqrt(np.sum(x * x, axis=1))
+    u = np.zeros_like(x)
+    nz = n > 0
+    u[nz] = x[nz] / n[nz, None]
+    y = u @ _as64(Pi).T
+    t_hi, t_lo = boundaries(c_hi), boundaries(c_lo)
+    idx = np.empty(y.shape, dtype=np.int64)
+    idx[:, :d_hi] = quantize(y[:, :d_hi], t_hi)
+    idx[:, d_hi:] = quantize(y[:, d_hi:], t_lo)
+    near = np.zeros(y.shape, dtype=bool)
+    near[:, :d_hi] = np.any(np.abs(y[:, :d_hi, None] - t_hi) <= 1e-5, axis=-1)
+    near[:, d_hi:] = np.any(np.abs(y[:, d_hi:, None] - t_lo) <= 1e-5, axis=-1)
+    return dict(idx=idx, n=n, y=y, code_exempt=near)
+
+
+def mse_reconstruct_mixed(idx, n, Pi, c_hi, c_lo, d_hi: int) -> np.ndarray:
+    """x_mse = ||x|| Pi^T c[idx] with the per-coordinate codebooks."""
+    return _as64(n)[:, None] * (centroids_mixed(idx, c_hi, c_lo, d_hi) @ _as64(Pi))
+
+
+def encode_prod_mixed(x, Pi, S, c_hi, c_lo, d_hi: int) -> dict:
+    """TurboQuantProd at a fractional width: the mixed MSE stage, then the QJL
+    stage of ``qjl_stage`` on its residual."""
+    out = encode_mse_mixed(x, Pi, c_hi, c_lo, d_hi)
+    out.update(qjl_stage_mixed(x, out["idx"], out["n"], Pi, S, c_hi, c_lo, d_hi))
+    return out
+
+
+def qjl_stage_mixed(x, idx, n, Pi, S, c_hi, c_lo, d_hi: int) -> dict:
+    """``qjl_stage`` with the mixed reconstruction."""
+    x = _as64(x)
+    S = _as64(S)
+    n = _as64(n)
+    r = x - mse_reconstruct_mixed(idx, n, Pi, c_hi, c_lo, d_hi)
+    rho = np.sqrt(np.sum(r * r, axis=1))
+    p = r @ S.T
+    z = p >= 0.0
+    return dict(r=r, rho=rho, p=p, z=z, sign_exempt=np.abs(p) <= 1e-5 * n[:, None])
+
+
+def score_prod_mixed(q, idx, z, n, rho, Pi, S, c_hi, c_lo, d_hi: int) -> np.ndarray:
+    """``score_prod`` with the mixed reconstruction: [H][N]."""
+    q = _as64(q)
+    S = _as64(S)
+    m = S.shape[0]
+    xm = mse_reconstruct_mixed(idx, n, Pi, c_hi, c_lo, d_hi)
+    return q @ xm.T + (_as64(rho)[None, :] * (KAPPA_NUM / m)) * ((q @ S.T) @ qjl_vector(z).T)
+
+
+def frac_block_bytes(d: int, k_lo: int, prod: bool) -> int:
+    """Bytes of a 128-token block at a fractional width: k_lo full code planes
+    (16 bytes per 128 coordinates per token), the extra bit of the first d/2
+    coordinates (8 bytes per 128 coordinates per token), the sign plane
+    (Prod) and the norm pairs."""
+    return TOKENS_PER_BLOCK * ((k_lo + (1 if prod else 0)) * d // 8 + d // 16 + 8)
+
+
+def pack_mixed(idx, z, n, rho, d: int, k_lo: int, prod: bool, G: int, N: int) -> np.ndarray:
+    """Packed layout at a fractional width: per 128-token block, the k_lo full
+    code planes as ``pack`` writes them (bit p of every coordinate's code),
+    then the extra plane (bit k_lo of the codes of coordinates < d/2; 8 bytes
+    per 128 coordinates per token, token-major, coordinate 64 c' + 32 w + i at
+    bit i of word w of chunk c'), then the sign plane (Prod), then the norm
+    pairs {||x||, ||r||} (||r|| = 0 for MSE).  Padded tokens are zero."""
+    T = TOKENS_PER_BLOCK
+    nb = -(-N // T)
+    d_hi = mixed_split(d)
+    idx = np.asarray(idx).reshape(G, N, d)
+    full = [((idx >> p) & 1).astype(np.uint64) for p in range(k_lo)]
+    if prod:
+        full.append(np.asarray(z).reshape(G, N, d).astype(np.uint64))
+    extra = ((idx[:, :, :d_hi] >> k_lo) & 1).astype(np.uint64)
+
+    def words(bits, width):  # [G][N][width] bits -> [G][nb*T][width // 32] uint32
+        b = np.zeros((G, nb * T, width), dtype=np.uint64)
+        b[:, :N] = bits
+        b = b.reshape(G, nb * T, width // 32, 32)
+        return (b << np.arange(32, dtype=np.uint64)).sum(axis=-1).astype(np.uint32)
+
+    out = bytearray()
+    fw = [words(f, d) for f in full]
+    ew = words(extra, d_hi)
+    norms = np.zeros((G, nb * T, 2), dtype=np.float32)
+    norms[:, :N, 0] = np.asarray(n, dtype=np.float32).reshape(G, N)
+    if prod:
+        norms[:, :N, 1] = np.asarray(rho, dtype=np.float32).reshape(G, N)
+    C = d // CHUNK_COORDS
+    for g in range(G):
+        for blk in range(nb):
+            rows = slice(blk * T, (blk + 1) * T)
+            for p in range(k_lo):                       # full code planes: [C][T][4]
+                out += fw[p][g, rows].reshape(T, C, 4).transpose(1, 0, 2).astype("<u4").tobytes()
+            out += ew[g, rows].reshape(T, C, 2).transpose(1, 0, 2).astype("<u4").tobytes()
+            if prod:
+                out += fw[k_lo][g, rows].reshape(T, C, 4).transpose(1, 0, 2).astype("<u4").tobytes()
+            out += norms[g, rows].astype("<f4").tobytes()
+    return np.frombuffer(bytes(out), dtype=np.uint8)
+
+
+def unpack_mixed(buf, d: int, k_lo: int, prod: bool, G: int, N: int) -> dict:
+    """Inverse of ``pack_mixed``: idx [G*N][d], z (Prod), n, rho."""
+    T = TOKENS_PER_BLOCK
+    C = d // CHUNK_COORDS
+    nb = -(-N // T)
+    d_hi = mixed_split(d)
+    bb = frac_block_bytes(d, k_lo, prod)
+    buf = np.asarray(buf, dtype=np.uint8).reshape(G * nb, bb)
+    full_bytes = T * C * 16
+
+    def bits_of(section, width):  # [B][C'][T][w] words -> [B][T][width]
+        w = np.ascontiguousarray(section).view("<u4")
+        per = width // 32 // C
+        w = w.reshape(G * nb, C, T, per).transpose(0, 2, 1, 3).reshape(G * nb, T, width // 32)
+        return ((w[..., None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(G * nb, T, width)
+
+    off = 0
+    idx = np.zeros((G * nb, T, d), dtype=np.int64)
+    for p in range(k_lo):
+        idx |= bits_of(buf[:, off:off + full_bytes], d).astype(np.int64) << p
+        off += full_bytes
+    ext = bits_of(buf[:, off:off + full_bytes // 2], d_hi)
+    idx[:, :, :d_hi] |= ext.astype(np.int64) << k_lo
+    off += full_bytes // 2
+    z = np.zeros((G * nb, T, d), dtype=bool)
+    if prod:
+        z = bits_of(buf[:, off:off + full_bytes], d).astype(bool)
+        off += full_bytes
+    nr = np.ascontiguousarray(buf[:, off:off + T * 8]).view("<f4").reshape(G, nb * T, 2).astype(np.float64)
+    idx = idx.reshape(G, nb * T, d)[:, :N].reshape(G * N, d)
+    z = z.reshape(G, nb * T, d)[:, :N].reshape(G * N, d)
+    return dict(idx=idx, z=z, n=nr[:, :N, 0].reshape(G * N), rho=nr[:, :N, 1].reshape(G * N))
+
+
+# ----------------------------------------------------------------------------
 # Values and the attention output of one decode step
 #
 # The value cache holds TurboQuantMSE codes ([PT-KR] "1단계"; the pages' 58 MB

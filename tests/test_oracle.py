@@ -602,3 +602,104 @@ def test_attend_packed_matches_per_group_attend():
         want = o.attend(q[g], ke["idx"][r], ke["z"][r], ke["n"][r].astype(np.float32), ke["rho"][r].astype(np.float32),
                         Pi_k, S, c_k, ve["idx"][r], ve["n"][r].astype(np.float32), Pi_v, c_v, 1 / math.sqrt(d))
         assert np.allclose(out[g], want, rtol=0, atol=1e-12 * np.max(np.abs(want)))
+
+
+# ---------------------------------------------------------------- fractional bit widths (reading; parity unpinned)
+
+def test_mixed_quantiser_with_one_codebook_is_the_uniform_one():
+    d = 64
+    rng = _rng(60)
+    Pi = _haar(d, 61)
+    S = rng.standard_normal((d, d))
+    c = o.codebook_f32(4, d)
+    x = rng.standard_normal((30, d))
+    q = rng.standard_normal((3, d))
+    for d_hi in (0, 17, d):
+        m = o.encode_prod_mixed(x, Pi, S, c, c, d_hi)
+        u = o.encode_prod(x, Pi, S, c)
+        assert np.array_equal(m["idx"], u["idx"]) and np.array_equal(m["z"], u["z"])
+        assert np.allclose(m["rho"], u["rho"], rtol=0, atol=1e-13)
+        a = o.score_prod_mixed(q, m["idx"], m["z"], m["n"], m["rho"], Pi, S, c, c, d_hi)
+        b = o.score_prod(q, u["idx"], u["z"], u["n"], u["rho"], Pi, S, c)
+        assert np.allclose(a, b, rtol=0, atol=1e-12 * np.max(np.abs(b)))
+
+
+def test_mixed_quantiser_is_nearest_centroid_per_coordinate():
+    d = 8
+    rng = _rng(62)
+    Pi = _haar(d, 63)
+    c_hi, c_lo = o.codebook_f32(8, d), o.codebook_f32(4, d)
+    x = rng.standard_normal((200, d))
+    e = o.encode_mse_mixed(x, Pi, c_hi, c_lo, 4)
+    for j in range(d):
+        cb = c_hi if j < 4 else c_lo
+        want = np.argmin(np.abs(e["y"][:, j, None] - cb.astype(np.float64)[None, :]), axis=1)
+        assert np.array_equal(e["idx"][:, j], want)
+    assert e["idx"][:, :4].max() <= 7 and e["idx"][:, 4:].max() <= 3
+
+
+@pytest.mark.parametrize("k_lo", [1, 2, 3])
+def test_mixed_distortion_is_the_mean_of_the_two_codebooks(k_lo):
+    # rotated coordinates of random unit vectors are ~N(0, 1/d): the distortion
+    # of the split quantiser is the mean of the two Lloyd-Max distortions
+    # (Max's table values, not the oracle's)
+    d, n = 128, 20000
+    tab = _golden("lloyd_max_textbook.json")["levels"]
+    rng = _rng(64 + k_lo)
+    Pi = _haar(d, 70)
+    x = rng.standard_normal((n, d))
+    x /= np.linalg.norm(x, axis=1, keepdims=True)
+    c_hi, c_lo = o.codebook_f32(2 << k_lo, d), o.codebook_f32(1 << k_lo, d)
+    e = o.encode_mse_mixed(x, Pi, c_hi, c_lo, o.mixed_split(d))
+    D = np.mean(np.sum((x - o.mse_reconstruct_mixed(e["idx"], e["n"], Pi, c_hi, c_lo, d // 2)) ** 2, axis=1))
+    want = 0.5 * (tab[str(2 << k_lo)]["mse"] + tab[str(1 << k_lo)]["mse"])
+    assert abs(D - want) <= 0.03 * want
+
+
+def test_mixed_prod_estimator_is_unbiased():
+    d, T = 32, 3000
+    rng = _rng(66)
+    Pi = _haar(d, 67)
+    c_hi, c_lo = o.codebook_f32(4, d), o.codebook_f32(2, d)
+    x = rng.standard_normal((1, d))
+    q = rng.standard_normal((1, d))
+    truth = (q @ x.T).item()
+    est = np.empty(T)
+    for t in range(T):
+        S = _rng(1000 + t).standard_normal((d, d))
+        e = o.encode_prod_mixed(x, Pi, S, c_hi, c_lo, d // 2)
+        est[t] = o.score_prod_mixed(q, e["idx"], e["z"], e["n"], e["rho"], Pi, S, c_hi, c_lo, d // 2)[0, 0]
+    r = e["r"][0]
+    var = ((math.pi / 2) * (r @ r).item() * (q @ q.T).item() - (q[0] @ r).item() ** 2) / d
+    assert abs(est.mean() - truth) <= 4 * math.sqrt(var / T)
+    assert abs(est.var() / var - 1.0) <= 0.1
+
+
+@pytest.mark.parametrize("k_lo,prod", [(2, True), (1, True), (3, False)])
+def test_fractional_layout_roundtrip_and_bit_addresses(k_lo, prod):
+    G, N, d = 2, 300, 256
+    rng = _rng(68)
+    d_hi = o.mixed_split(d)
+    idx = rng.integers(0, 1 << k_lo, size=(G * N, d))
+    idx[:, :d_hi] = rng.integers(0, 2 << k_lo, size=(G * N, d_hi))
+    z = rng.integers(0, 2, size=(G * N, d)).astype(bool)
+    n = rng.random(G * N).astype(np.float32)
+    rho = rng.random(G * N).astype(np.float32)
+    buf = o.pack_mixed(idx, z, n, rho, d, k_lo, prod, G, N)
+    nb = 3
+    bb = o.frac_block_bytes(d, k_lo, prod)
+    assert buf.size == G * nb * bb
+    u = o.unpack_mixed(buf, d, k_lo, prod, G, N)
+    assert np.array_equal(u["idx"], idx) and np.array_equal(u["n"], n.astype(np.float64))
+    if prod:
+        assert np.array_equal(u["z"], z) and np.array_equal(u["rho"], rho.astype(np.float64))
+    # the extra plane: bit k_lo of coordinate j < d/2 of token t is bit i of
+    # word w of the 8 bytes at ((c' 128 + t) 8) after the full planes, j = 64 c' + 32 w + i
+    C = d // 128
+    for (g, tok, j) in [(0, 0, 0), (1, 299, d_hi - 1), (0, 130, 70), (1, 257, 33)]:
+        blk, t = divmod(tok, 128)
+        c2, rem = divmod(j, 64)
+        w, i = divmod(rem, 32)
+        off = (g * nb + blk) * bb + k_lo * C * 128 * 16 + (c2 * 128 + t) * 8 + 4 * w
+        word = int.from_bytes(bytes(buf[off:off + 4]), "little")
+        assert (word >> i) & 1 == (idx[g * N + tok, j] >> k_lo) & 1

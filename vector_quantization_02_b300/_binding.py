@@ -32,6 +32,7 @@ def _load() -> ctypes.CDLL:
         "tq_haar_rotation": (c_int, [c_int, vp, vp]),
         "tq_plan_create": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, ctypes.POINTER(vp)]),
         "tq_plan_create_hadamard": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, ctypes.POINTER(vp)]),
+        "tq_plan_create_fractional": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, vp, ctypes.POINTER(vp)]),
         "tq_plan_destroy": (c_int, [vp]),
         "tq_packed_bytes": (c_sz, [vp, c_i64, c_i64]),
         "tq_encode": (c_int, [vp, vp, c_int, c_i64, c_i64, vp, vp]),
@@ -48,6 +49,9 @@ def _load() -> ctypes.CDLL:
         "tq_encode_path": (c_int, [vp, c_int]),
         "tq_decode_path": (c_int, [vp]),
         "tq_selftest_wait_expiry": (c_int, [vp, vp]),
+        "tq_encode_values": (c_int, [vp, vp, c_int, c_i64, c_i64, vp, vp]),
+        "tq_attend_workspace_bytes": (c_sz, [vp, vp, c_i64, c_int, c_i64]),
+        "tq_attend": (c_int, [vp, vp, vp, c_i64, c_int, vp, vp, c_i64, ctypes.c_float, vp, vp, c_sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -58,11 +62,12 @@ def _load() -> ctypes.CDLL:
 
 lib = _load()
 EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_plan_create_hadamard",
+            "tq_plan_create_fractional",
             "tq_plan_destroy",
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
             "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
             "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path", "tq_decode_path",
-            "tq_selftest_wait_expiry")
+            "tq_selftest_wait_expiry", "tq_encode_values", "tq_attend_workspace_bytes", "tq_attend")
 PATHS = {0: "tensor_d128", 1: "tensor_wide", 2: "cuda_core"}
 TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
 
@@ -171,6 +176,33 @@ class Plan:
         """Build Pi and the codebook with the library's host helpers."""
         k = bits - 1 if mode == "prod" else bits
         return cls(d, bits, tq_haar_rotation(rotation_gaussian), S, tq_lloyd_max_codebook(1 << k, d), mode)
+
+    @classmethod
+    def fractional(cls, d: int, half_bits: int, Pi: torch.Tensor, S: torch.Tensor | None, codebook_hi: torch.Tensor,
+                   codebook_lo: torch.Tensor, mode: str = "prod", stream=None):
+        """A plan at b + 1/2 bits per channel (half_bits = 2b + 1): the first
+        d/2 rotated coordinates take codebook_hi, the others codebook_lo
+        (tq_plan_create_fractional)."""
+        self = cls.__new__(cls)
+        self.d, self.mode, self.hadamard, self.half_bits = d, mode, False, half_bits
+        dev = torch.device("cuda", torch.cuda.current_device())
+        Pi_d = Pi.to(dev, torch.float32).contiguous()
+        S_d = S.to(dev, torch.float32).contiguous() if S is not None else None
+        hi = codebook_hi.to(dev, torch.float32).contiguous()
+        lo = codebook_lo.to(dev, torch.float32).contiguous()
+        k_hi = (half_bits + 1) // 2 - (1 if mode == "prod" else 0)
+        self.bits = k_hi + 1 if mode == "prod" else k_hi
+        if hi.numel() != 1 << k_hi or lo.numel() != 1 << (k_hi - 1):
+            raise ValueError(f"codebooks must have {1 << k_hi} and {1 << (k_hi - 1)} centroids")
+        h = ctypes.c_void_p()
+        st = lib.tq_plan_create_fractional(d, half_bits, _MODES[mode], _dev(Pi_d, "Pi", shape=(d, d)),
+                                           _dev(S_d, "S", shape=(d, d)) if S_d is not None else None,
+                                           _dev(hi, "codebook_hi"), _dev(lo, "codebook_lo"),
+                                           ctypes.c_void_p(_stream(stream)), ctypes.byref(h))
+        _check(st, "tq_plan_create_fractional")
+        self.handle = h
+        self.levels = hi.numel()
+        return self
 
     @classmethod
     def hadamard(cls, d: int, bits: int, signs: torch.Tensor, S: torch.Tensor | None, codebook: torch.Tensor,
@@ -315,3 +347,48 @@ def tq_score_noalloc(plan: Plan, queries: torch.Tensor, packed: torch.Tensor, N:
                               ctypes.c_void_p(_stream(stream)))
     _check(st, "tq_score_noalloc")
     return (logits, top_scores, top_idx) if top_k else logits
+
+
+def tq_encode_values(plan: Plan, values: torch.Tensor, packed: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """values [G][N][d] (CUDA) -> packed uint8 buffer in the coordinate-major
+    value layout (an MSE plan)."""
+    G, N, d = values.shape
+    if d != plan.d:
+        raise ValueError("values' last dimension must equal the plan's d")
+    nbytes = plan.packed_bytes(G, N)
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=values.device)
+    elif packed.numel() < nbytes or packed.dtype != torch.uint8:
+        raise ValueError("packed buffer too small")
+    if values.dtype not in _DTYPES:
+        raise ValueError(f"unsupported value dtype {values.dtype}")
+    _check(lib.tq_encode_values(plan.handle, _dev(values, "values"), _DTYPES[values.dtype], G, N,
+                                _dev(packed, "packed"), ctypes.c_void_p(_stream(stream))), "tq_encode_values")
+    return packed
+
+
+def attend_workspace_bytes(kplan: Plan, vplan: Plan, G: int, H: int, N: int) -> int:
+    return int(lib.tq_attend_workspace_bytes(kplan.handle, vplan.handle, G, H, N))
+
+
+def tq_attend(kplan: Plan, vplan: Plan, queries: torch.Tensor, kpacked: torch.Tensor, vpacked: torch.Tensor, N: int,
+              scale: float, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """One decode step of attention on the compressed cache: queries [G][H][d]
+    -> out [G][H][d] (softmax of scale * logits over the N tokens, times the
+    reconstructed values)."""
+    G, H, d = queries.shape
+    dev = queries.device
+    if kpacked.numel() < kplan.packed_bytes(G, N) or vpacked.numel() < vplan.packed_bytes(G, N):
+        raise ValueError("packed buffers too small for (G, N)")
+    if out is None:
+        out = torch.empty(G, H, d, dtype=torch.float32, device=dev)
+    wsb = attend_workspace_bytes(kplan, vplan, G, H, N)
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    st = lib.tq_attend(kplan.handle, vplan.handle, _dev(queries, "queries", torch.float32), G, H,
+                       _dev(kpacked, "kpacked"), _dev(vpacked, "vpacked"), N, ctypes.c_float(scale),
+                       _dev(out, "out", torch.float32, (G, H, d)), _dev(workspace, "workspace"), workspace.numel(),
+                       ctypes.c_void_p(_stream(stream)))
+    _check(st, "tq_attend")
+    return out

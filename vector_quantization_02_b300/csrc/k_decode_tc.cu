@@ -60,6 +60,7 @@ struct DecTcArgs {
   Layout lay;
   int64_t N, nb, n_tiles;
   uint32_t ctab[16];  // level i: fp16 bits of hi (low half) and lo (high half) of 2^8 c_i
+  uint32_t ctab_lo[16];  // the same for the lower codebook of a fractional width (coordinates 64..127)
   float kappa;
   const uint8_t* packed;
   const uint8_t* pit;  // 2^8 Pi^T images: hi, lo
@@ -84,11 +85,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
   const uint32_t sb = smem_u32(smem);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ uint32_t s_ctab[16];
+  __shared__ uint32_t s_ctab[32];  // [0, 16): coordinates 0..63; [16, 32): 64..127
   auto bar = [&](int i) { return sb + kOffDecBar + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x < 16) s_ctab[threadIdx.x] = a.ctab[threadIdx.x];
+  if (threadIdx.x < 16) {
+    s_ctab[threadIdx.x] = a.ctab[threadIdx.x];
+    s_ctab[16 + threadIdx.x] = a.lay.frac ? a.ctab_lo[threadIdx.x] : a.ctab[threadIdx.x];
+  }
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar(DB_OPS), 1);
@@ -200,9 +204,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
       const uint8_t* blk = smem + kOffBlk + s * kBlkMax;
       uint4 pw[K];
 #pragma unroll
-      for (int p = 0; p < K; ++p) pw[p] = *reinterpret_cast<const uint4*>(blk + ((int64_t)p * kTokensPerBlock + row) * 16);
+      for (int p = 0; p < K; ++p) {
+        if (p == K - 1 && a.lay.frac) {  // a fractional width's half plane: coordinates 0..63
+          const uint2 h = *reinterpret_cast<const uint2*>(blk + a.lay.top_off + row * 8);
+          pw[p] = make_uint4(h.x, h.y, 0u, 0u);
+        } else {
+          pw[p] = *reinterpret_cast<const uint4*>(blk + ((int64_t)p * kTokensPerBlock + row) * 16);
+        }
+      }
       uint4 zw = make_uint4(0u, 0u, 0u, 0u);
-      if constexpr (PROD) zw = *reinterpret_cast<const uint4*>(blk + ((int64_t)K * kTokensPerBlock + row) * 16);
+      if constexpr (PROD) zw = *reinterpret_cast<const uint4*>(blk + a.lay.sign_off + row * 16);
       mbar_arrive(bar(DB_SEMPTY + s));
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
@@ -219,7 +230,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
             i0 |= ((wp[p] >> (2 * m)) & 1u) << p;
             i1 |= ((wp[p] >> (2 * m + 1)) & 1u) << p;
           }
-          const uint32_t c0 = s_ctab[i0], c1 = s_ctab[i1];
+          const uint32_t c0 = s_ctab[(w >> 1) * 16 + i0], c1 = s_ctab[(w >> 1) * 16 + i1];
           hi[m] = __byte_perm(c0, c1, 0x5410);  // (hi of coordinate 2m, hi of 2m + 1)
           lo[m] = __byte_perm(c0, c1, 0x7632);
         }
@@ -307,6 +318,7 @@ cudaError_t launch_dec(const tq_plan* p, const uint8_t* packed, int64_t G, int64
   a.nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
   a.n_tiles = G * a.nb;
   for (int i = 0; i < 16; ++i) a.ctab[i] = i < p->cp.L ? p->dec_ctab[i] : 0u;
+  for (int i = 0; i < 16; ++i) a.ctab_lo[i] = p->lay.frac && i < p->cp_lo.L ? p->dec_ctab_lo[i] : 0u;
   a.kappa = p->kappa;
   a.packed = packed;
   a.pit = p->tc_ops + tc_dec_image(p, 0) * kDecImg;

@@ -75,6 +75,12 @@ struct EncTcArgs {
   // +-1 matrix (pi_hi), whose scale c is folded into cp, px and M; rho = c ||r'||
   int e2_single;
   float rho_scale;
+  // fractional width: coordinates 64..127 use the lower codebook (padded to
+  // the same number of code bits; its top bit is never set), and code plane
+  // K - 1 is stored as a half plane (coordinates 0..63, 8 bytes per token)
+  int frac;
+  CodeParams cp_lo;
+  ParityExpansion px_lo;
 };
 
 __device__ __forceinline__ void raise(int* err, volatile int* abort) {
@@ -286,17 +292,23 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       // boundaries: idx = #{t_i < 0}); centroids scaled by n
       const float sc = n > 0.f ? n : 1.f;
       float nt[L - 1], nc[L];
-#pragma unroll
-      for (int q = 0; q < L - 1; ++q) nt[q] = sc * a.cp.t[q];
-#pragma unroll
-      for (int q = 0; q < L; ++q) nc[q] = n * a.cp.c[q];
       // signed-form terms: -n half[t] as bits (the sign flips where the term's
       // parity is 1), and n mid
       constexpr int NT = K == 1 ? 1 : K == 2 ? 2 : 4;
       uint32_t nhalf[NT];
+      float nmid;
+      // the constants of one codebook (the lower one for coordinates 64..127
+      // of a fractional width)
+      auto set_codebook = [&](const CodeParams& cp, const ParityExpansion& px) {
 #pragma unroll
-      for (int t = 0; t < NT; ++t) nhalf[t] = __float_as_uint(-(n * a.px.half[t]));
-      const float nmid = n * a.px.mid;
+        for (int q = 0; q < L - 1; ++q) nt[q] = sc * cp.t[q];
+#pragma unroll
+        for (int q = 0; q < L; ++q) nc[q] = n * cp.c[q];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) nhalf[t] = __float_as_uint(-(n * px.half[t]));
+        nmid = n * px.mid;
+      };
+      set_codebook(a.cp, a.px);
 
       // E2 result -> E3 codes, E4 residual; the residual's bf16 split goes back
       // into the same TMEM columns as the A operand of E5
@@ -390,6 +402,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       tmem_ld_wait();
 #pragma unroll 1
       for (int cc = 0; cc < 4; cc += 2) {
+        if (cc == 2 && a.frac) set_codebook(a.cp_lo, a.px_lo);
         tmem_ld32(t_lane + 32 * (cc + 1), vb);
         chunk(va, cc);
         tmem_ld_wait();
@@ -436,12 +449,17 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       uint8_t* out = a.packed + tile * a.lay.block_bytes;
 #pragma unroll
       for (int p = 0; p < K; ++p) {
+        if (p == K - 1 && a.frac) {  // the half plane: coordinates 0..63
+          *reinterpret_cast<uint2*>(out + a.lay.top_off + row * 8) =
+              live ? make_uint2(pl[p][0], pl[p][1]) : make_uint2(0, 0);
+          continue;
+        }
         const uint4 val = live ? make_uint4(pl[p][0], pl[p][1], pl[p][2], pl[p][3])
                                : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(out + ((int64_t)p * kTokensPerBlock + row) * 16) = val;
       }
       if constexpr (PROD)
-        *reinterpret_cast<uint4*>(out + ((int64_t)K * kTokensPerBlock + row) * 16) =
+        *reinterpret_cast<uint4*>(out + a.lay.sign_off + row * 16) =
             live ? make_uint4(zs[0], zs[1], zs[2], zs[3]) : make_uint4(0, 0, 0, 0);
       *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, rho) : make_float2(0.f, 0.f);
     }
@@ -475,6 +493,9 @@ cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, 
   a.px = p->px_enc;
   a.e2_single = p->hadamard;
   a.rho_scale = p->rot_scale;
+  a.frac = p->lay.frac;
+  a.cp_lo = p->cp_enc_lo;
+  a.px_lo = p->px_enc_lo;
   a.G = G;
   a.N = N;
   a.nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;

@@ -690,7 +690,7 @@ int query_nsmid() {
 bool encode_wide_supported(const tq_plan* p, tq_dtype dt) {
   (void)dt;
   const bool prod = p->lay.prod != 0;
-  return p->wide_ops && (!prod || p->wide_scratch) && p->d % 128 == 0 && p->cp.L >= 2 &&
+  return !p->lay.frac && p->wide_ops && (!prod || p->wide_scratch) && p->d % 128 == 0 && p->cp.L >= 2 &&
          p->cp.L <= (prod ? 8 : 16) && enc_wide_smem(enc_wide_nc(p->d)) <= 227 * 1024;
 }
 

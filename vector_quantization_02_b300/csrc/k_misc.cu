@@ -410,6 +410,7 @@ cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s) {
 cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
                                cudaStream_t s) {
   if (G * N == 0) return cudaSuccess;
+  if (p->lay.frac) return cudaErrorNotSupported;  // fractional widths decode on the d = 128 tensor-core path
   if (p->d <= 128) return launch_decode_kb<16>(p, packed, G, N, out, s);
   return launch_decode_kb<8>(p, packed, G, N, out, s);
 }

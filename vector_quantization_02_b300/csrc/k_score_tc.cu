@@ -57,6 +57,7 @@
 #include <algorithm>
 
 #include "ptx_sm100.cuh"
+#include "tc_planes.cuh"
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -67,8 +68,6 @@ using namespace ptx;
 constexpr int kMaxStages = 16;      // packed-block ring entries (a multiple of the warpgroups per role)
 constexpr int kMaxR = 4;            // TMEM tiles in flight: plane-slot groups = accumulator stages = R
 constexpr int kMaxIssuers = kMaxR;
-constexpr int kSlices = 4;          // e4m3 slices of the query operand
-constexpr int kPlaneCols = 32;      // TMEM columns of one expanded plane (128 e4m3)
 
 // MMA-term planes of an odd-symmetric codebook with k code bits.
 __host__ __device__ constexpr int planes_of(int k) { return k == 3 ? 4 : k; }
@@ -113,10 +112,6 @@ enum {
   BAR_COUNT = BAR_DONE + kMaxIssuers
 };
 
-// reciprocal of the e4m3 value of bit 3 + i of a byte (2^-6, 2^-5, 2^-3, 2)
-__constant__ float c_comp[4] = {64.f, 32.f, 8.f, 0.5f};
-// source bit (within each byte of the plane word) of expanded word o
-__constant__ int c_src[8] = {3, 4, 5, 6, 0, 1, 2, 7};
 
 struct ScoreTcArgs {
   Layout lay;
@@ -137,85 +132,6 @@ __device__ __forceinline__ void raise(int* err, volatile int* abort) {
   atomicExch(err, 1);
 }
 
-// Eight TMEM words (32 e4m3 values) from one 32-coordinate plane word.
-__device__ __forceinline__ void expand_word(uint32_t W, uint32_t* o) {
-  const uint32_t b = W << 3, c = W >> 1;
-  o[0] = W & 0x08080808u;
-  o[1] = W & 0x10101010u;
-  o[2] = W & 0x20202020u;
-  o[3] = W & 0x40404040u;
-  o[4] = b & 0x08080808u;
-  o[5] = b & 0x10101010u;
-  o[6] = b & 0x20202020u;
-  o[7] = c & 0x40404040u;
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr));
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate)
-__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Instruction descriptor, kind::f8f6f4: e4m3 A and B, fp32 accumulate, K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
-  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
-}
-
-// Position in a ring of n entries: index and the parity of the pass over it.
-struct Ring {
-  uint32_t idx = 0, phase = 0;
-  __device__ __forceinline__ void advance(uint32_t by, uint32_t n) {
-    idx += by;
-    while (idx >= n) {
-      idx -= n;
-      phase ^= 1u;
-    }
-  }
-};
-
-// (group, block) of a tile, advanced without divisions.
-struct TilePos {
-  uint32_t g = 0, blk = 0;
-  __device__ __forceinline__ void init(int64_t tile, int64_t nb) {
-    g = (uint32_t)(tile / nb);
-    blk = (uint32_t)(tile - (int64_t)g * nb);
-  }
-  __device__ __forceinline__ void advance(uint32_t by, uint32_t nb) {
-    blk += by;
-    while (blk >= nb) {
-      blk -= nb;
-      ++g;
-    }
-  }
-};
-
-__device__ __forceinline__ float slice_weight(int sl) {
-  return sl == 0 ? 1.f : sl == 1 ? 0.0625f : sl == 2 ? 0.00390625f : 0.000244140625f;
-}
 
 // Both terms' accumulators of a tile (NJ x N <= 64 columns): every TMEM load is
 // issued before a single wait.
@@ -238,46 +154,6 @@ __device__ __forceinline__ void load_terms(uint32_t taddr, float (&accA)[HP], fl
     }
 }
 
-// One term's accumulators (N <= 32 columns), every TMEM load issued before a
-// single wait: acc[h] = sum over slices of D[slice * HP + h] / 16^slice.
-template <int HP>
-__device__ __forceinline__ void load_term_all(uint32_t taddr, float (&acc)[HP]) {
-  constexpr int N = kSlices * HP;
-  static_assert(N <= 32, "at most 32 columns in flight");
-  uint32_t v[N / 16][16];
-#pragma unroll
-  for (int c = 0; c < N / 16; ++c) tmem_ld16(taddr + 16 * c, v[c]);
-  tmem_ld_wait();
-#pragma unroll
-  for (int h = 0; h < HP; ++h) acc[h] = 0.f;
-#pragma unroll
-  for (int c = 0; c < N / 16; ++c)
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int col = 16 * c + e, sl = col / HP, h = col % HP;
-      acc[h] = fmaf(__uint_as_float(v[c][e]), slice_weight(sl), acc[h]);
-    }
-}
-
-// Tokens' accumulators of one term: sum over slices of D[slice * HP + h] / 16^slice.
-template <int HP>
-__device__ __forceinline__ void load_term(uint32_t taddr, float (&acc)[HP]) {
-  constexpr int N = kSlices * HP;
-#pragma unroll
-  for (int h = 0; h < HP; ++h) acc[h] = 0.f;
-#pragma unroll
-  for (int c0 = 0; c0 < N; c0 += 16) {
-    uint32_t v[16];
-    tmem_ld16(taddr + c0, v);
-    tmem_ld_wait();
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int col = c0 + e, sl = col / HP, h = col % HP;
-      const float w = sl == 0 ? 1.f : sl == 1 ? 0.0625f : sl == 2 ? 0.00390625f : 0.000244140625f;
-      acc[h] = fmaf(__uint_as_float(v[e]), w, acc[h]);
-    }
-  }
-}
 
 // One job's MMAs for one tile: planes [P0, P1) x 4 K steps into one
 // accumulator.  Every operand is a per-tile base plus a compile-time offset,
@@ -481,12 +357,19 @@ __global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_ke
       const uint8_t* blkp = smem + off_ring + slot.idx * blk_bytes;
       uint4 w[NP];
 #pragma unroll
-      for (int q = 0; q < K; ++q) w[q] = *reinterpret_cast<const uint4*>(blkp + ((q * kTokensPerBlock) + row) * 16);
+      for (int q = 0; q < K; ++q) {
+        if (q == K - 1 && a.lay.frac) {  // a fractional width's half plane: coordinates 0..63
+          const uint2 h = *reinterpret_cast<const uint2*>(blkp + a.lay.top_off + row * 8);
+          w[q] = make_uint4(h.x, h.y, 0u, 0u);
+        } else {
+          w[q] = *reinterpret_cast<const uint4*>(blkp + ((q * kTokensPerBlock) + row) * 16);
+        }
+      }
       if constexpr (K == 3) {  // the triple-product plane x0 ^ x1 ^ x2
         w[3] = make_uint4(w[0].x ^ w[1].x ^ w[2].x, w[0].y ^ w[1].y ^ w[2].y, w[0].z ^ w[1].z ^ w[2].z,
                           w[0].w ^ w[1].w ^ w[2].w);
       }
-      if constexpr (PROD) w[NA] = *reinterpret_cast<const uint4*>(blkp + ((K * kTokensPerBlock) + row) * 16);
+      if constexpr (PROD) w[NA] = *reinterpret_cast<const uint4*>(blkp + a.lay.sign_off + row * 16);
       mbar_arrive(bar(BAR_EMPTY + slot.idx));
       if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_MDONE + ent.idx), ent.phase ^ 1u, abort))) {
         raise(a.err, abort);
@@ -577,16 +460,6 @@ __global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_ke
 }
 
 // ---------------------------------------------------------------- query operand images
-// Byte offset of element (row n, K index k) of an image of rows x 128 e4m3
-// (one 128-byte swizzle atom column), as the tensor cores read a K-major operand.
-__device__ __forceinline__ uint32_t img_offset(int n, int k) {
-  return (uint32_t)(n >> 3) * 1024u + (uint32_t)(n & 7) * 128u + (uint32_t)(((k >> 4) ^ (n & 7)) << 4) +
-         (uint32_t)(k & 15);
-}
-
-__device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t x) {
-  return __half2float(__half(__nv_cvt_fp8_to_halfraw(x, __NV_E4M3)));
-}
 
 constexpr int kPrepHeads = 4;      // heads per prep CTA
 constexpr int kPrepThreads = 256;  // two threads per output coordinate (halves of the sum)
@@ -596,8 +469,8 @@ constexpr int kPrepThreads = 256;  // two threads per output coordinate (halves 
 // rows (4 slices x head) and the heads' constants are written.
 __global__ void __launch_bounds__(kPrepThreads)
 score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int prod, ParityExpansion px,
-                     const float* __restrict__ PiT, const float* __restrict__ ST, uint32_t img_bytes,
-                     uint8_t* __restrict__ images, float4* __restrict__ consts, int* err) {
+                     ParityExpansion px_lo, int frac, const float* __restrict__ PiT, const float* __restrict__ ST,
+                     uint32_t img_bytes, uint8_t* __restrict__ images, float4* __restrict__ consts, int* err) {
   constexpr int d = 128;
   grid_dependents_launch();  // the score kernel may start streaming packed blocks now
   extern __shared__ float prep_sm[];
@@ -605,7 +478,7 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
   float* sS = prep_sm + d * d;          // [d][d] S^T
   __shared__ float s_q[kPrepHeads][d], s_part[2][2][kPrepHeads][d];
   __shared__ float red[4 * kPrepHeads][4];
-  __shared__ float s_coef[kMaxTerms];
+  __shared__ float s_coef[kMaxTerms], s_coef_lo[kMaxTerms];  // coordinates 0..63 and 64..127
   const int quads = (H + kPrepHeads - 1) / kPrepHeads;
   const int64_t g = blockIdx.x / quads;
   const int h0 = (blockIdx.x % quads) * kPrepHeads;
@@ -625,7 +498,12 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
   if (t < d)
 #pragma unroll
     for (int hh = 0; hh < kPrepHeads; ++hh) s_q[hh][t] = hh < nh ? q[(g * H + h0 + hh) * d + t] : 0.f;
-  if (t < kMaxTerms) s_coef[t] = t < px.n ? px.coef[t] : 0.f;
+  if (t < kMaxTerms) {
+    s_coef[t] = t < px.n ? px.coef[t] : 0.f;
+    // a fractional width's lower codebook (coordinates 64..127), its terms on
+    // the same masks (zero where the top code bit is involved)
+    s_coef_lo[t] = t < px.n ? (frac ? px_lo.coef[t] : px.coef[t]) : 0.f;
+  }
   __syncthreads();
   {
     int no_abort = 0;
@@ -653,11 +531,13 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
   __syncthreads();
   // full values; per head sum and max |.| (warp shuffles in the first 4 warps)
   float v[4 * kPrepHeads];
+  // the c0 term: c0 of coordinate j's codebook times (Pi q)_j, summed below
+  const float c0j = (frac && j >= 64) ? px_lo.c0 : px.c0;
 #pragma unroll
   for (int hh = 0; hh < kPrepHeads; ++hh) {
     qr[hh] = s_part[0][0][hh][j] + s_part[1][0][hh][j];
     sq[hh] = s_part[0][1][hh][j] + s_part[1][1][hh][j];
-    v[4 * hh + 0] = qr[hh];
+    v[4 * hh + 0] = c0j * qr[hh];
     v[4 * hh + 1] = sq[hh];
     v[4 * hh + 2] = fabsf(qr[hh]);
     v[4 * hh + 3] = fabsf(sq[hh]);
@@ -683,7 +563,7 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
     for (int r = 0; r < 4 * kPrepHeads; ++r) red[r][t >> 5] = v[r];
   __syncthreads();
   float gmax = 0.f;
-  for (int p = 0; p < nA; ++p) gmax = fmaxf(gmax, fabsf(s_coef[p]));
+  for (int p = 0; p < nA; ++p) gmax = fmaxf(gmax, fmaxf(fabsf(s_coef[p]), fabsf(s_coef_lo[p])));
   const int nP = nA + prod;
   uint8_t* img = images + g * img_bytes;
   // K index kk of a plane: TMEM column c = kk / 4 = 8 w + o, byte b = kk % 4,
@@ -706,7 +586,8 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
     const float sA = ldexpf(1.f, 2 - eA), sB = ldexpf(1.f, 2 - eB);
     // the two thread halves split the planes
     for (int p = half; p < nP; p += 2) {
-      float val = p < nA ? s_coef[p] * s_part[0][0][hh][jc] * comp * sA : 2.f * s_part[0][1][hh][jc] * comp * sB;
+      const float coef = jc < 64 ? s_coef[p] : s_coef_lo[p];
+      float val = p < nA ? coef * s_part[0][0][hh][jc] * comp * sA : 2.f * s_part[0][1][hh][jc] * comp * sB;
       uint8_t* base = img + (uint32_t)p * (uint32_t)N * 128u;
       float scale = 1.f;
 #pragma unroll
@@ -717,7 +598,7 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
         scale *= 16.f;
       }
     }
-    if (t == 0) consts[g * Hp + h] = make_float4(1.f / sA, px.c0 * sum_qr, 1.f / sB, -sum_sq);
+    if (t == 0) consts[g * Hp + h] = make_float4(1.f / sA, sum_qr, 1.f / sB, -sum_sq);
   }
   if (h0 == 0) {  // zero rows of the padding heads
     for (int p = half; p < nP; p += 2) {
@@ -829,8 +710,8 @@ cudaError_t launch_score_tc(const tq_plan* p, const float* queries, int64_t G, i
   if (e != cudaSuccess) return e;
   const int64_t prep_blocks = G * ((H + kPrepHeads - 1) / kPrepHeads);
   score_tc_prep_kernel<<<(unsigned)prep_blocks, kPrepThreads, prep_smem, s>>>(
-      queries, H, gm.Hp, gm.nA, p->lay.prod, p->px, p->PiT, p->lay.prod ? p->ST : p->PiT, gm.img, images, consts,
-      p->err);
+      queries, H, gm.Hp, gm.nA, p->lay.prod, p->px, p->px_enc_lo, p->lay.frac, p->PiT, p->lay.prod ? p->ST : p->PiT,
+      gm.img, images, consts, p->err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

@@ -383,7 +383,7 @@ cudaError_t launch_wide_kernel(const CUtensorMap& tm, const WideArgs& a, size_t 
 }  // namespace
 
 bool score_wide_supported(const tq_plan* p, int H) {
-  return p->d % 128 == 0 && H >= 1 && H <= 256 && p->lay.k >= 1 && p->lay.k <= 4 &&
+  return !p->lay.frac && p->d % 128 == 0 && H >= 1 && H <= 256 && p->lay.k >= 1 && p->lay.k <= 4 &&
          wide_smem_bytes(p, H) <= 227 * 1024;
 }
 

@@ -138,15 +138,19 @@ cudaError_t build_tc_ops(tq_plan* p) {
     split_images<__half>(T.data(), host.data() + tq::tc_dec_image(p, 2) * img,
                          host.data() + tq::tc_dec_image(p, 3) * img);
   }
-  for (int i = 0; i < 16; ++i) {
-    const float v = i < p->cp.L ? 256.f * p->cp.c[i] : 0.f;
-    const __half h = __float2half_rn(v);
-    const __half l = __float2half_rn(v - __half2float(h));
-    uint16_t hb, lb;
-    std::memcpy(&hb, &h, 2);
-    std::memcpy(&lb, &l, 2);
-    p->dec_ctab[i] = (uint32_t)hb | ((uint32_t)lb << 16);
-  }
+  auto ctab = [](const CodeParams& cp, uint32_t* tab) {
+    for (int i = 0; i < 16; ++i) {
+      const float v = i < cp.L ? 256.f * cp.c[i] : 0.f;
+      const __half h = __float2half_rn(v);
+      const __half l = __float2half_rn(v - __half2float(h));
+      uint16_t hb, lb;
+      std::memcpy(&hb, &h, 2);
+      std::memcpy(&lb, &l, 2);
+      tab[i] = (uint32_t)hb | ((uint32_t)lb << 16);
+    }
+  };
+  ctab(p->cp, p->dec_ctab);
+  if (p->lay.frac) ctab(p->cp_lo, p->dec_ctab_lo);
   e = cudaMalloc(&p->tc_ops, host.size());
   if (e == cudaSuccess) e = cudaMemcpy(p->tc_ops, host.data(), host.size(), cudaMemcpyHostToDevice);
   return e;
@@ -263,8 +267,54 @@ namespace {
 
 // Plan creation shared by tq_plan_create and tq_plan_create_hadamard; a
 // Hadamard plan passes hadamard = 1 (Pi already holds c H diag(signs)).
+// Parity expansion of an ascending codebook of `levels` entries (host, fp64
+// coefficients rounded to fp32), as tq_codebook_parity_expansion computes it.
+bool expansion_of(int levels, const float* hc, ParityExpansion* px) {
+  unsigned masks[kMaxTerms];
+  double coefs[kMaxTerms], c0 = 0.0;
+  int n = 0;
+  if (tq_codebook_parity_expansion(levels, hc, &n, masks, coefs, &c0) != TQ_OK) return false;
+  px->n = n;
+  double mid = c0;
+  for (int i = 0; i < kMaxTerms; ++i) {
+    px->mask[i] = i < n ? masks[i] : 0u;
+    px->coef[i] = i < n ? (float)coefs[i] : 0.f;
+    px->half[i] = i < n ? (float)(0.5 * coefs[i]) : 0.f;
+    if (i < n) mid += 0.5 * coefs[i];
+  }
+  px->c0 = (float)c0;
+  px->mid = (float)mid;
+  return true;
+}
+
+// A codebook of 2^(k-1) levels in the form of the k-bit one (fractional
+// widths: the encode quantises both halves of the coordinates with k code
+// bits): thresholds past the last at +inf, so the top bit is never set, and
+// the parity terms of the k-bit masks with the lower codebook's coefficients
+// (zero on the masks that involve the top bit).
+void pad_lower_codebook(const CodeParams& lo, const ParityExpansion& pxlo, const ParityExpansion& pxhi,
+                        CodeParams* cp, ParityExpansion* px) {
+  *cp = lo;
+  const int L = 2 * lo.L;
+  cp->L = L;
+  for (int i = lo.L; i < L && i < kMaxLevels; ++i) cp->c[i] = lo.c[lo.L - 1];
+  for (int i = lo.L - 1; i + 1 < L && i < kMaxLevels - 1; ++i) cp->t[i] = INFINITY;
+  *px = pxhi;
+  double mid = pxlo.c0;
+  for (int t = 0; t < pxhi.n; ++t) {
+    float c = 0.f;
+    for (int u = 0; u < pxlo.n; ++u)
+      if (pxlo.mask[u] == pxhi.mask[t]) c = pxlo.coef[u];
+    px->coef[t] = c;
+    px->half[t] = 0.5f * c;
+    mid += 0.5 * (double)c;
+  }
+  px->c0 = pxlo.c0;
+  px->mid = (float)mid;
+}
+
 tq_status create_plan(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
-                      void* stream, int hadamard, tq_plan** out) {
+                      void* stream, int hadamard, tq_plan** out, const float* codebook_lo = nullptr) {
   if (!out) return TQ_EINVAL;
   *out = nullptr;
   if (d < 128 || d > kMaxD || d % 128 != 0) return TQ_EINVAL;
@@ -288,7 +338,11 @@ tq_status create_plan(int d, int bits, tq_mode mode, const float* Pi, const floa
   L.prod = mode == TQ_PROD;
   L.planes = k + L.prod;
   L.C = d / kChunk;
-  L.norms_off = (int64_t)L.planes * L.C * kTokensPerBlock * 16;
+  L.frac = codebook_lo != nullptr;
+  L.top_off = (int64_t)(k - 1) * L.C * kTokensPerBlock * 16;
+  // a fractional width's top code plane holds the first d/2 coordinates only
+  L.sign_off = L.top_off + (int64_t)L.C * kTokensPerBlock * (L.frac ? 8 : 16);
+  L.norms_off = L.sign_off + (L.prod ? (int64_t)L.C * kTokensPerBlock * 16 : 0);
   L.block_bytes = L.norms_off + kTokensPerBlock * 8;
   p->kappa = (float)(std::sqrt(M_PI / 2.0) / d);
   p->hadamard = hadamard;
@@ -348,6 +402,30 @@ tq_status create_plan(int d, int bits, tq_mode mode, const float* Pi, const floa
   }
   // the codebook as the d = 128 encode compares it: divided by the rotation's
   // scale for a Hadamard plan (the encode works on y / c there)
+  if (L.frac) {
+    // the codebook of the last d/2 coordinates: 2^(k-1) levels, ascending
+    const int lv = levels / 2;
+    float hl[kMaxLevels];
+    if (cudaMemcpyAsync(hl, codebook_lo, lv * sizeof(float), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+      free_plan(p);
+      return TQ_ECUDA;
+    }
+    CodeParams& lo = p->cp_lo;
+    lo.L = lv;
+    for (int i = 0; i < kMaxLevels; ++i) lo.c[i] = i < lv ? hl[i] : 0.f;
+    for (int i = 0; i + 1 < kMaxLevels; ++i) lo.t[i] = i + 1 < lv ? 0.5f * (hl[i] + hl[i + 1]) : 0.f;
+    for (int i = 0; i + 1 < lv; ++i)
+      if (!(hl[i] < hl[i + 1])) {
+        free_plan(p);
+        return TQ_EINVAL;
+      }
+    if (!expansion_of(lv, hl, &p->px_lo)) {
+      free_plan(p);
+      return TQ_EINVAL;
+    }
+    pad_lower_codebook(p->cp_lo, p->px_lo, p->px, &p->cp_enc_lo, &p->px_enc_lo);
+  }
   p->cp_enc = p->cp;
   p->px_enc = p->px;
   if (hadamard) {
@@ -417,6 +495,18 @@ tq_status tq_plan_create_hadamard(int d, int bits, tq_mode mode, const float* si
   return st;
 }
 
+tq_status tq_plan_create_fractional(int d, int half_bits, tq_mode mode, const float* Pi, const float* S,
+                                    const float* codebook_hi, const float* codebook_lo, void* stream,
+                                    tq_plan** out) {
+  if (!out) return TQ_EINVAL;
+  *out = nullptr;
+  if (d != 128 || !codebook_lo) return TQ_EINVAL;
+  if (mode == TQ_PROD && half_bits != 5 && half_bits != 7) return TQ_EINVAL;
+  if (mode == TQ_MSE && half_bits != 3 && half_bits != 5) return TQ_EINVAL;
+  const int k_hi = (half_bits + 1) / 2 - (mode == TQ_PROD ? 1 : 0);
+  return create_plan(d, mode == TQ_PROD ? k_hi + 1 : k_hi, mode, Pi, S, codebook_hi, stream, 0, out, codebook_lo);
+}
+
 tq_status tq_plan_destroy(tq_plan* plan) {
   if (!plan) return TQ_EINVAL;
   free_plan(plan);
@@ -465,6 +555,36 @@ tq_status tq_score(const tq_plan* p, const float* queries, int64_t G, int H, con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return from_cuda(score_run(p, queries, G, H, static_cast<const uint8_t*>(packed), N, logits, top_k, top_scores,
                              top_idx, workspace, s));
+}
+
+tq_status tq_encode_values(const tq_plan* p, const void* values, tq_dtype dtype, int64_t G, int64_t N, void* packed,
+                           void* stream) {
+  if (!p || p->lay.prod) return TQ_EINVAL;
+  if (p->lay.frac) return TQ_EUNSUPPORTED;
+  const tq_status st = tq_encode(p, values, dtype, G, N, packed, stream);
+  if (st != TQ_OK || G == 0 || N == 0) return st;
+  const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
+  return from_cuda(launch_values_layout(p, static_cast<uint8_t*>(packed), G * nb, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t tq_attend_workspace_bytes(const tq_plan* kplan, const tq_plan* vplan, int64_t G, int H, int64_t N) {
+  if (!kplan || !vplan || G < 0 || H < 1 || N < 0) return 0;
+  return attend_workspace_bytes(kplan, vplan, G, H, N);
+}
+
+tq_status tq_attend(const tq_plan* kplan, const tq_plan* vplan, const float* queries, int64_t G, int H,
+                    const void* kpacked, const void* vpacked, int64_t N, float scale, float* out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (!kplan || !vplan || G < 0 || N < 0 || H < 1 || !std::isfinite(scale)) return TQ_EINVAL;
+  if (!attend_supported(kplan, vplan, H)) return TQ_EUNSUPPORTED;
+  if (G == 0 || N == 0) return TQ_OK;
+  if (!queries || !kpacked || !vpacked || !out || !workspace) return TQ_EINVAL;
+  if (workspace_bytes < attend_workspace_bytes(kplan, vplan, G, H, N)) return TQ_EINVAL;
+  if (!aligned16(queries) || !aligned16(kpacked) || !aligned16(vpacked) || !aligned16(out)) return TQ_EALIGN;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_EALIGN;
+  return from_cuda(launch_attend(kplan, vplan, queries, G, H, static_cast<const uint8_t*>(kpacked),
+                                 static_cast<const uint8_t*>(vpacked), N, scale, out, workspace,
+                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 tq_status tq_decode(const tq_plan* p, const void* packed, int64_t G, int64_t N, float* out, void* stream) {

@@ -42,10 +42,15 @@ struct ParityExpansion {
 // Geometry of the packed layout for one plan.
 struct Layout {
   int d;            // head dimension
-  int k;            // code planes
+  int k;            // code planes (code bits of the coordinates with the most)
   int planes;       // k (+1 sign plane in PROD)
   int C;            // 128-coordinate chunks per plane
   int prod;         // 1 for TurboQuantProd
+  int frac;         // 1 for a fractional width: the first d/2 coordinates have k code
+                    // bits, the others k - 1; code plane k - 1 is then a half plane
+                    // of 8 bytes per 128 coordinates per token
+  int64_t top_off;      // offset of code plane k - 1 inside a block
+  int64_t sign_off;     // offset of the sign plane (PROD)
   int64_t block_bytes;  // bytes per 128-token block
   int64_t norms_off;    // offset of the norm pairs inside a block
 
@@ -67,6 +72,12 @@ struct tq_plan {
   float rot_scale;    // c for a Hadamard plan, else 1
   tq::CodeParams cp_enc;       // the codebook as the d = 128 encode uses it: divided by c (Hadamard)
   tq::ParityExpansion px_enc;  // the same for the parity expansion
+  // fractional width (lay.frac): the codebook of the last d/2 coordinates, with
+  // 2^(k-1) levels (cp_lo, px_lo); padded to 2^k levels for the encode (never
+  // reached thresholds at +inf, zero weights on the extra parity terms)
+  tq::CodeParams cp_lo, cp_enc_lo;
+  tq::ParityExpansion px_lo, px_enc_lo;
+  uint32_t dec_ctab_lo[16];
   float* Pi;          // [d][d] row-major, y = Pi u
   float* PiT;         // [d][d] = Pi^T (coalesced column access in SIMT kernels)
   float* S;           // [d][d] (PROD)
@@ -120,6 +131,15 @@ bool score_wide_supported(const tq_plan* p, int H);
 size_t score_wide_workspace_bytes(const tq_plan* p, int64_t G, int H);
 cudaError_t launch_score_wide(const tq_plan* p, const float* queries, int64_t G, int H, const uint8_t* packed,
                               int64_t N, float* logits, void* ws, cudaStream_t s);
+
+// Attention of a decode step (k_attend.cu): keys of a Prod plan, values of an
+// MSE plan in the coordinate-major value layout.
+cudaError_t launch_values_layout(const tq_plan* p, uint8_t* packed, int64_t n_blocks, cudaStream_t s);
+bool attend_supported(const tq_plan* kp, const tq_plan* vp, int H);
+size_t attend_workspace_bytes(const tq_plan* kp, const tq_plan* vp, int64_t G, int H, int64_t N);
+cudaError_t launch_attend(const tq_plan* kp, const tq_plan* vp, const float* q, int64_t G, int H,
+                          const uint8_t* kpacked, const uint8_t* vpacked, int64_t N, float scale, float* out,
+                          void* ws, cudaStream_t s);
 
 // Scoring as tq_score performs it (query preparation, score kernel, optional
 // top-k) on a caller-provided workspace of at least score_workspace_bytes().
