@@ -31,8 +31,8 @@
 //     codebook, sum_t x_T[j][t] w[t] over every tile of the split in TMEM;
 //     at the end the same warpgroup combines planes and slices into
 //     o[h][j] = sum_t w_t c[idx_{t,j}] in the rotated frame;
-//  3. attend_combine_kernel merges the splits of a group (max-rescaled sums)
-//     and rotates back, out = Pi_v^T o / sum_t exp(scale (l - m)).
+//  3. attend_combine_kernel (one CTA per group, every head) merges the splits
+//     (max-rescaled sums) and rotates back, out = Pi_v^T o / sum_t exp(scale (l - m)).
 // The packed keys and values are each read once; the logits make one round
 // trip through memory (the workspace), which at decode-step sizes stays in L2.
 #include <cuda_fp8.h>
@@ -88,11 +88,11 @@ __global__ void __launch_bounds__(128) values_to_coordinate_major_kernel(uint8_t
 
 // ------------------------------------------------------------------ attention
 constexpr int kAttStages = 16;          // value-block ring
-constexpr int kAttThreads = 480;        // 15 warps: producer, 2 issuers, value WG, 2 weight WGs
-constexpr int kAttProducer = 0, kAttIssuer0 = 1, kAttValWarp0 = 3, kAttWgtWarp0 = 7;
+constexpr int kAttThreads = 608;        // 19 warps: producer, 2 issuers, 2 value WGs, 2 weight WGs
+constexpr int kAttProducer = 0, kAttIssuer0 = 1, kAttValWarp0 = 3, kAttWgtWarp0 = 11;
 enum {
   AB_FULL = 0,
-  AB_EMPTY = AB_FULL + kAttStages,   // value warpgroup (128) + the tile's weight warpgroup (128)
+  AB_EMPTY = AB_FULL + kAttStages,   // the tile's value warpgroup (128) + its weight warpgroup (128)
   AB_PFULL = AB_EMPTY + kAttStages,  // [2] value planes of entry e in TMEM
   AB_WFULL = AB_PFULL + 2,           // [2] weight image of entry e in shared memory
   AB_MDONE = AB_WFULL + 2,           // [2] MMAs of entry e's tile complete
@@ -224,14 +224,17 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
     }
   } else if (warp < kAttWgtWarp0) {
     // ------------------------------------------------------------ value planes
+    // value warpgroup e takes the tiles i with i % 2 == e (TMEM entry e);
     // thread (warp w, lane l) owns coordinate j = 32 (w % 4) + l: its 16-byte
     // chunk of each code plane holds the block's 128 tokens
+    const uint32_t e = (uint32_t)(warp - kAttValWarp0) >> 2;
     const int quad = warp & 3;
     const int j = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + kSlot0;
     Ring slot;
-    for (uint32_t i = 0; i < n_t; ++i, slot.advance(1, kAttStages)) {
-      const uint32_t e = i & 1u, use = i >> 1;
+    slot.advance(e, kAttStages);
+    uint32_t use = 0;
+    for (uint32_t i = e; i < n_t; i += 2, ++use, slot.advance(2, kAttStages)) {
       if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(AB_FULL + slot.idx), slot.phase, abort))) {
         *abort = 1;
         atomicExch(a.err, 1);
@@ -458,32 +461,57 @@ done:
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// One CTA of 128 threads per (group, head): merge the splits' partial sums
-// (max-rescaled), divide by the softmax denominator and rotate back:
-// out = Pi_v^T o.  Thread j owns coordinate j.
-__global__ void __launch_bounds__(128) attend_combine_kernel(const float* __restrict__ part_o,
-                                                             const float* __restrict__ part_ml, int splits, int H,
-                                                             int Hp, const float* __restrict__ Pi_v,
-                                                             float* __restrict__ out) {
-  __shared__ float s_o[128];
-  const int64_t g = blockIdx.x / H;
-  const int h = blockIdx.x % H, j = threadIdx.x;
-  float M = -INFINITY;
-  for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, part_ml[((g * splits + sp) * Hp + h) * 2]);
-  float num = 0.f, den = 0.f;
-  for (int sp = 0; sp < splits; ++sp) {
-    const int64_t r = (g * splits + sp) * Hp + h;
-    const float f = __expf(part_ml[r * 2] - M);
-    num = fmaf(f, part_o[r * 128 + j], num);
-    den = fmaf(f, part_ml[r * 2 + 1], den);
+// One CTA of 512 threads per group: merge the splits' partial sums of every
+// head (max-rescaled), divide by the softmax denominator and rotate back,
+// out = Pi_v^T o, reading Pi_v once for all heads of the group.  Thread
+// (quarter r, coordinate j) sums rows i in [32 r, 32 r + 32) of Pi_v with its
+// 32 loads in flight together; the four quarters are added in shared memory.
+constexpr int kCombThreads = 512;
+template <int HP>
+__global__ void __launch_bounds__(kCombThreads) attend_combine_kernel(const float* __restrict__ part_o,
+                                                                      const float* __restrict__ part_ml, int splits,
+                                                                      int H, int Hp, const float* __restrict__ Pi_v,
+                                                                      float* __restrict__ out) {
+  __shared__ float s_o[HP][128];
+  __shared__ float s_q[4][HP][128];
+  const int64_t g = blockIdx.x;
+  for (int p = threadIdx.x; p < HP * 128; p += kCombThreads) {
+    const int h = p >> 7, j = p & 127;
+    float o = 0.f;
+    if (h < H) {
+      float M = -INFINITY;
+      for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, part_ml[((g * splits + sp) * Hp + h) * 2]);
+      float num = 0.f, den = 0.f;
+      for (int sp = 0; sp < splits; ++sp) {
+        const int64_t r = (g * splits + sp) * Hp + h;
+        const float f = __expf(part_ml[r * 2] - M);
+        num = fmaf(f, part_o[r * 128 + j], num);
+        den = fmaf(f, part_ml[r * 2 + 1], den);
+      }
+      o = num / den;
+    }
+    s_o[h][j] = o;
   }
-  s_o[j] = num / den;
-  __syncthreads();
   // out_j = sum_i Pi_v[i][j] o_i  (Pi_v row-major, y = Pi_v u)
-  float acc = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < 128; ++i) acc = fmaf(Pi_v[i * 128 + j], s_o[i], acc);
-  out[(g * H + h) * 128 + j] = acc;
+  const int r = threadIdx.x >> 7, j = threadIdx.x & 127;
+  float pv[32];
+#pragma unroll
+  for (int ii = 0; ii < 32; ++ii) pv[ii] = __ldg(Pi_v + (32 * r + ii) * 128 + j);
+  __syncthreads();
+  float acc[HP];
+#pragma unroll
+  for (int h = 0; h < HP; ++h) acc[h] = 0.f;
+#pragma unroll
+  for (int ii = 0; ii < 32; ++ii)
+#pragma unroll
+    for (int h = 0; h < HP; ++h) acc[h] = fmaf(pv[ii], s_o[h][32 * r + ii], acc[h]);
+#pragma unroll
+  for (int h = 0; h < HP; ++h) s_q[r][h][j] = acc[h];
+  __syncthreads();
+  for (int p = threadIdx.x; p < H * 128; p += kCombThreads) {
+    const int h = p >> 7, jj = p & 127;
+    out[(g * H + h) * 128 + jj] = (s_q[0][h][jj] + s_q[1][h][jj]) + (s_q[2][h][jj] + s_q[3][h][jj]);
+  }
 }
 
 }  // namespace
@@ -581,7 +609,11 @@ cudaError_t launch_attend(const tq_plan* kp, const tq_plan* vp, const float* q, 
     default: return cudaErrorNotSupported;
   }
   if (e != cudaSuccess) return e;
-  attend_combine_kernel<<<(unsigned)(G * H), 128, 0, s>>>(part_o, part_ml, S, H, Hp, vp->Pi, out);
+  switch (Hp) {
+    case 4: attend_combine_kernel<4><<<(unsigned)G, kCombThreads, 0, s>>>(part_o, part_ml, S, H, Hp, vp->Pi, out); break;
+    case 8: attend_combine_kernel<8><<<(unsigned)G, kCombThreads, 0, s>>>(part_o, part_ml, S, H, Hp, vp->Pi, out); break;
+    default: attend_combine_kernel<16><<<(unsigned)G, kCombThreads, 0, s>>>(part_o, part_ml, S, H, Hp, vp->Pi, out); break;
+  }
   return cudaGetLastError();
 }
 
