@@ -17,8 +17,13 @@
 //  warp 0     bulk copies: once the B images, then each tile's packed block
 //             into a 2-stage ring;
 //  warp 1     TMEM owner (512 columns) and MMA issuer (one thread);
-//  warps 2-5  expansion: thread = key row; code bits -> A operands in TMEM;
-//  warps 6-9  epilogue: thread = key row; accumulators -> fp32 rows of out.
+//  warps 2-5  expansion: thread = key row; code bits -> A operands in TMEM,
+//             through lookup tables built once per CTA that map the code bits
+//             of four coordinates (two for k >= 3) straight to their fp16 hi
+//             and lo operand words;
+//  warps 6-9  epilogue: thread = key row; accumulators -> fp32 rows, staged in
+//             shared memory (128-byte swizzle, conflict-free) and written by
+//             TMA tensor stores that clip the rows past N of a ragged block.
 // TMEM columns: D1 [0, 128), D2 [128, 256), A hi [256, 320), A lo [320, 384),
 // signs [384, 448); A columns hold fp16 pairs, k step kb at column 8 kb.
 // Every wait is bounded: on expiry the kernel raises the plan's error word,
@@ -35,25 +40,32 @@ namespace {
 using namespace ptx;
 
 constexpr int kDecThreads = 320;
+constexpr int kDecEpi0 = 192;                 // first epilogue thread (warp 6)
 constexpr int kDecStages = 2;
 constexpr uint32_t kDecImg = 128 * 128 * 2;   // one 128 x 128 fp16 operand image
 constexpr uint32_t kDecAtom = 128 * 128;      // 128 rows x 64 elements (128 B) per swizzle atom
 constexpr uint32_t kOffPtHi = 0, kOffPtLo = kDecImg, kOffStHi = 2 * kDecImg, kOffStLo = 3 * kDecImg;
 constexpr uint32_t kBlkMax = 4 * 2048 + 1024;  // largest d = 128 block: four planes + norms
 constexpr uint32_t kOffBlk = 4 * kDecImg;
-constexpr uint32_t kOffDecBar = kOffBlk + kDecStages * kBlkMax;
+// output staging: four boxes of 128 rows x 32 fp32 (128 B rows, 128-byte swizzle)
+constexpr uint32_t kStageBox = 128 * 128;
+constexpr uint32_t kOffStage = kOffBlk + kDecStages * kBlkMax;  // a multiple of 1024
+constexpr uint32_t kOffTab = kOffStage + 4 * kStageBox;        // lookup tables: 2 x 256 x 16 B
+constexpr uint32_t kOffDecBar = kOffTab + 2 * 256 * 16;
 enum {
   DB_OPS = 0,
   DB_SFULL = 1,
   DB_SEMPTY = DB_SFULL + kDecStages,  // expansion (128) + epilogue (128) arrivals
   DB_AFULL = DB_SEMPTY + kDecStages,
-  DB_AEMPTY,
-  DB_DFULL,
+  DB_MDONE,   // a tile's MMAs complete: A may be rewritten, D1 and D2 are full
   DB_DEMPTY,
+  DB_SFREE,   // the staging buffer may be written (previous tile's stores have read it)
+  DB_STAGED,  // the tile's rows are in the staging buffer (128 epilogue arrivals)
   DB_DONE,
   DB_COUNT
 };
 constexpr uint32_t kDecSmem = kOffDecBar + DB_COUNT * 8 + 1024;  // + alignment slack
+static_assert(kOffStage % 1024 == 0, "128-byte swizzled boxes start on 1024-byte boundaries");
 constexpr uint32_t kColD1 = 0, kColD2 = 128, kColAHi = 256, kColALo = 320, kColSg = 384;
 
 struct DecTcArgs {
@@ -78,20 +90,56 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
   return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
+// Lookup tables of the expansion, built per CTA from the codebook's split
+// levels ctab (coordinates 0..63) and ctab_lo (64..127, the lower codebook of
+// a fractional width, else ctab again).  For k <= 2 an entry covers four
+// coordinates: key = sum_p nibble_p << 4p (bit u of plane p's nibble belongs
+// to coordinate u), value = {hi pair 0-1, hi pair 2-3, lo pair 0-1, lo pair
+// 2-3}.  For k >= 3 an entry covers two: key = sum_p (2 bits of plane p) << 2p,
+// value = {hi pair, lo pair} (the first half of a uint4).
+template <int K>
+__device__ __forceinline__ void build_dec_tables(const DecTcArgs& a, uint4* tab) {
+  constexpr int U = K <= 2 ? 4 : 2, kEnt = 1 << (U * K);
+  static_assert(kEnt <= 256, "table");
+  for (int e = threadIdx.x; e < 2 * kEnt; e += blockDim.x) {
+    const int t = e / kEnt, key = e % kEnt;
+    const uint32_t* ct = (t == 1 && a.lay.frac) ? a.ctab_lo : a.ctab;
+    uint32_t c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      uint32_t idx = 0;
+#pragma unroll
+      for (int p = 0; p < K; ++p) idx |= (uint32_t)((key >> (U * p + u)) & 1) << p;
+      c[u] = ct[idx];
+    }
+    if constexpr (U == 4)
+      tab[t * 256 + key] = make_uint4(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410),
+                                      __byte_perm(c[0], c[1], 0x7632), __byte_perm(c[2], c[3], 0x7632));
+    else
+      tab[t * 256 + key] = make_uint4(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[0], c[1], 0x7632), 0u, 0u);
+  }
+}
+
 template <int K, bool PROD>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmOut, const DecTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ uint32_t s_ctab[32];  // [0, 16): coordinates 0..63; [16, 32): 64..127
+  __shared__ uint2 s_sgn[16];  // 2 z - 1 of four coordinates as two fp16 pairs, by their four sign bits
+  uint4* tab = reinterpret_cast<uint4*>(smem + kOffTab);
   auto bar = [&](int i) { return sb + kOffDecBar + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  build_dec_tables<K>(a, tab);
   if (threadIdx.x < 16) {
-    s_ctab[threadIdx.x] = a.ctab[threadIdx.x];
-    s_ctab[16 + threadIdx.x] = a.lay.frac ? a.ctab_lo[threadIdx.x] : a.ctab[threadIdx.x];
+    // +1 = 0x3C00, -1 = 0xBC00 in fp16; sign bit u of the index is z of coordinate u
+    uint32_t h[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) h[u] = 0x3C00u | ((~(threadIdx.x >> u) & 1u) << 15);
+    s_sgn[threadIdx.x] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
   }
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -101,9 +149,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
       mbar_init(bar(DB_SEMPTY + s), 256);
     }
     mbar_init(bar(DB_AFULL), 128);
-    mbar_init(bar(DB_AEMPTY), 1);
-    mbar_init(bar(DB_DFULL), 1);
+    mbar_init(bar(DB_MDONE), 1);
     mbar_init(bar(DB_DEMPTY), 128);
+    mbar_init(bar(DB_SFREE), 1);
+    mbar_init(bar(DB_STAGED), 128);
     mbar_init(bar(DB_DONE), 1);
     fence_mbar_init();
   }
@@ -150,8 +199,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The operand descriptors are built once; every MMA adds a compile-time
+    // offset.  One commit per tile: the expansion (A free) and the epilogue
+    // (D full) both wait on it, each for every phase in turn.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(0u, 128, 128);
+      const uint64_t dph = sdesc_k_sw128(sb + kOffPtHi), dpl = sdesc_k_sw128(sb + kOffPtLo);
+      const uint64_t dsh = sdesc_k_sw128(sb + kOffStHi), dsl = sdesc_k_sw128(sb + kOffStLo);
+      const uint32_t d1 = tmem + kColD1, d2 = tmem + kColD2;
+      const uint32_t ahi = tmem + kColAHi, alo = tmem + kColALo, sg = tmem + kColSg;
       bool ok = mbar_wait(bar(DB_OPS), 0, abort);
       for (int64_t i = 0; ok && i < n_my; ++i) {
         const uint32_t ph = (uint32_t)i & 1u;
@@ -161,22 +217,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
         }
         tc_fence_after();
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const uint32_t off = (kb >> 2) * kDecAtom + (kb & 3) * 32;
-          const uint64_t bh = sdesc_k_sw128(sb + kOffPtHi + off), bl = sdesc_k_sw128(sb + kOffPtLo + off);
-          const uint32_t ahi = tmem + kColAHi + 8 * kb, alo = tmem + kColALo + 8 * kb;
-          mma_f16_ts(tmem + kColD1, ahi, bh, idesc, kb > 0);
-          mma_f16_ts(tmem + kColD1, ahi, bl, idesc, 1u);
-          mma_f16_ts(tmem + kColD1, alo, bh, idesc, 1u);
+        for (uint32_t kb = 0; kb < 8; ++kb) {
+          // k step kb: swizzle atom kb / 4 of the image, 32 bytes per step within it
+          // (descriptor address units of 16 bytes); A columns 8 kb
+          const uint64_t off = (uint64_t)(((kb >> 2) * kDecAtom + (kb & 3) * 32) >> 4);
+          mma_f16_ts(d1, ahi + 8 * kb, dph + off, idesc, kb > 0 ? 1u : 0u);
+          mma_f16_ts(d1, ahi + 8 * kb, dpl + off, idesc, 1u);
+          mma_f16_ts(d1, alo + 8 * kb, dph + off, idesc, 1u);
           if constexpr (PROD) {
-            const uint64_t sh = sdesc_k_sw128(sb + kOffStHi + off), sl = sdesc_k_sw128(sb + kOffStLo + off);
-            const uint32_t sg = tmem + kColSg + 8 * kb;
-            mma_f16_ts(tmem + kColD2, sg, sh, idesc, kb > 0);
-            mma_f16_ts(tmem + kColD2, sg, sl, idesc, 1u);
+            mma_f16_ts(d2, sg + 8 * kb, dsh + off, idesc, kb > 0 ? 1u : 0u);
+            mma_f16_ts(d2, sg + 8 * kb, dsl + off, idesc, 1u);
           }
         }
-        mma_commit(bar(DB_DFULL));
-        mma_commit(bar(DB_AEMPTY));
+        mma_commit(bar(DB_MDONE));
       }
       if (!ok) raise_dec(a.err, abort);
       // all issued MMAs complete before TMEM is freed
@@ -195,7 +248,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
       // every lane polls; the warp proceeds (or gives up) as one, because the
       // tcgen05 stores below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(bar(DB_SFULL + s), (uint32_t)(i / kDecStages) & 1u, abort)) ||
-          !__all_sync(0xffffffffu, mbar_wait(bar(DB_AEMPTY), ((uint32_t)i & 1u) ^ 1u, abort))) {
+          !__all_sync(0xffffffffu, mbar_wait(bar(DB_MDONE), ((uint32_t)i & 1u) ^ 1u, abort))) {
         ok = false;
         break;
       }
@@ -217,32 +270,46 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
       mbar_arrive(bar(DB_SEMPTY + s));
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        // coordinates 32 w + e, e = 0..31: bit e of word w of each plane
+        // coordinates 32 w + e, e = 0..31: bit e of word w of each plane;
+        // table 1 for coordinates 64..127
         uint32_t wp[K];
 #pragma unroll
         for (int p = 0; p < K; ++p) wp[p] = word_of(pw[p], w);
+        const uint4* tw = tab + (w >> 1) * 256;
         uint32_t hi[16], lo[16];
+        if constexpr (K <= 2) {
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          uint32_t i0 = 0, i1 = 0;
-#pragma unroll
-          for (int p = 0; p < K; ++p) {
-            i0 |= ((wp[p] >> (2 * m)) & 1u) << p;
-            i1 |= ((wp[p] >> (2 * m + 1)) & 1u) << p;
+          for (int q = 0; q < 8; ++q) {
+            uint32_t key = (wp[0] >> (4 * q)) & 0xFu;
+            if constexpr (K == 2) key |= ((wp[1] >> (4 * q)) & 0xFu) << 4;
+            const uint4 e = tw[key];
+            hi[2 * q] = e.x;
+            hi[2 * q + 1] = e.y;
+            lo[2 * q] = e.z;
+            lo[2 * q + 1] = e.w;
           }
-          const uint32_t c0 = s_ctab[(w >> 1) * 16 + i0], c1 = s_ctab[(w >> 1) * 16 + i1];
-          hi[m] = __byte_perm(c0, c1, 0x5410);  // (hi of coordinate 2m, hi of 2m + 1)
-          lo[m] = __byte_perm(c0, c1, 0x7632);
+        } else {
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            uint32_t key = 0;
+#pragma unroll
+            for (int p = 0; p < K; ++p) key |= ((wp[p] >> (2 * m)) & 3u) << (2 * p);
+            const uint2 e = *reinterpret_cast<const uint2*>(tw + key);
+            hi[m] = e.x;
+            lo[m] = e.y;
+          }
         }
         tmem_st16(t_lane + kColAHi + 16 * w, hi);
         tmem_st16(t_lane + kColALo + 16 * w, lo);
         if constexpr (PROD) {
-          // 2 z - 1 as fp16 (+1 = 0x3C00, -1 = 0xBC00)
           const uint32_t z = word_of(zw, w);
           uint32_t sg[16];
 #pragma unroll
-          for (int m = 0; m < 16; ++m)
-            sg[m] = 0x3C003C00u | ((~(z >> (2 * m)) & 1u) << 15) | ((~(z >> (2 * m + 1)) & 1u) << 31);
+          for (int q = 0; q < 8; ++q) {
+            const uint2 e = s_sgn[(z >> (4 * q)) & 0xFu];
+            sg[2 * q] = e.x;
+            sg[2 * q + 1] = e.y;
+          }
           tmem_st16(t_lane + kColSg + 16 * w, sg);
         }
       }
@@ -253,14 +320,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
     if (!ok) raise_dec(a.err, abort);
   } else {
     // ------------------------------------------------------------ epilogue
+    // Thread = key row.  Rows go to the staging buffer (box q = fp32 columns
+    // 32 q .. 32 q + 31, 128-byte rows whose 16-byte chunks are XOR-swizzled
+    // by row % 8), then thread kDecEpi0 writes the tile with four TMA stores.
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const bool leader = threadIdx.x == kDecEpi0;
+    const uint32_t stage_row = sb + kOffStage + (uint32_t)row * 128u;
+    if (leader) prefetch_tmap(&tmOut);
     bool ok = true;
     for (int64_t i = 0; ok && i < n_my; ++i) {
       const int s = (int)(i % kDecStages);
+      const uint32_t ph = (uint32_t)i & 1u;
       const int64_t tile = blockIdx.x + i * gridDim.x;
-      const int64_t g = tile / a.nb, tok = (tile - g * a.nb) * kTokensPerBlock + row;
+      const int64_t g = tile / a.nb, tok0 = (tile - g * a.nb) * kTokensPerBlock;
       // the key's norms, read from the staged block (this role waits on the
       // stage itself, so the block cannot be refilled before it is read)
       if (!__all_sync(0xffffffffu, mbar_wait(bar(DB_SFULL + s), (uint32_t)(i / kDecStages) & 1u, abort))) {
@@ -271,12 +345,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
           *reinterpret_cast<const float2*>(smem + kOffBlk + s * kBlkMax + a.lay.norms_off + row * 8);
       mbar_arrive(bar(DB_SEMPTY + s));
       const float s1 = nr.x * (1.f / 65536.f), s2 = nr.y * a.kappa * (1.f / 256.f);
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(DB_DFULL), (uint32_t)i & 1u, abort))) {
+      if (leader) {
+        // the previous tile's stores have read the staging buffer
+        bulk_wait_read_all();
+        mbar_arrive(bar(DB_SFREE));
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(DB_MDONE), ph, abort)) ||
+          !__all_sync(0xffffffffu, mbar_wait(bar(DB_SFREE), ph, abort))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float4* dst = reinterpret_cast<float4*>(a.out + (g * a.N + tok) * 128);
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         uint32_t v1[32], v2[32];
@@ -287,21 +366,35 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_tc_kernel(const DecTcAr
           tc_fence_before();
           mbar_arrive(bar(DB_DEMPTY));
         }
-        if (tok < a.N) {
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            float o[4];
+        for (int j = 0; j < 8; ++j) {
+          float o[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              o[u] = s1 * __uint_as_float(v1[4 * t + u]);
-              if constexpr (PROD) o[u] = fmaf(s2, __uint_as_float(v2[4 * t + u]), o[u]);
-            }
-            dst[8 * q + t] = make_float4(o[0], o[1], o[2], o[3]);
+          for (int u = 0; u < 4; ++u) {
+            o[u] = s1 * __uint_as_float(v1[4 * j + u]);
+            if constexpr (PROD) o[u] = fmaf(s2, __uint_as_float(v2[4 * j + u]), o[u]);
           }
+          sts128(stage_row + (uint32_t)q * kStageBox + (uint32_t)((j ^ (row & 7)) << 4), __float_as_uint(o[0]),
+                 __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+        }
+      }
+      // the rows are visible to the TMA unit, then the leader stores the tile
+      // (rows past N, in a ragged last block of a group, are clipped)
+      fence_proxy_async_smem();
+      mbar_arrive(bar(DB_STAGED));
+      if (leader) {
+        if (!mbar_wait(bar(DB_STAGED), ph, abort)) {
+          ok = false;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            tma_store_3d(&tmOut, sb + kOffStage + (uint32_t)q * kStageBox, 32 * q, (int32_t)tok0, (int32_t)g);
+          bulk_commit_group();
         }
       }
     }
     if (!ok) raise_dec(a.err, abort);
+    if (leader) bulk_wait_all();  // the output is written before the CTA exits
   }
 
   tc_fence_before();
@@ -325,14 +418,23 @@ cudaError_t launch_dec(const tq_plan* p, const uint8_t* packed, int64_t G, int64
   a.st = PROD ? p->tc_ops + tc_dec_image(p, 2) * kDecImg : nullptr;
   a.out = out;
   a.err = p->err;
+  // the output as [G][N][128] fp32, written in boxes of 128 rows x 32 values
+  CUtensorMap tm;
+  const uint64_t dims[3] = {128, (uint64_t)N, (uint64_t)G};
+  const uint64_t strides[2] = {128 * sizeof(float), (uint64_t)N * 128 * sizeof(float)};
+  // (a box no taller than the tensor; the staging rows keep their places)
+  const uint32_t box[3] = {32, N < 128 ? (uint32_t)N : 128u, 1};
+  cudaError_t e = make_tmap_3d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
   auto kern = decode_tc_kernel<K, PROD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmem);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t grid = a.n_tiles < sms ? a.n_tiles : sms;
-  kern<<<(unsigned)grid, kDecThreads, kDecSmem, s>>>(a);
+  kern<<<(unsigned)grid, kDecThreads, kDecSmem, s>>>(tm, a);
   return cudaGetLastError();
 }
 

@@ -462,105 +462,92 @@ __global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_ke
 // ---------------------------------------------------------------- query operand images
 
 constexpr int kPrepHeads = 4;      // heads per prep CTA
-constexpr int kPrepThreads = 256;  // two threads per output coordinate (halves of the sum)
+constexpr int kPrepThreads = 512;  // four threads per output coordinate (quarters of the sum)
 
-// One CTA per (group, up to 4 heads).  Pi^T and S^T are staged in shared memory
-// (one round trip), Pi q and S q are formed in fp32, then every plane's image
-// rows (4 slices x head) and the heads' constants are written.
-__global__ void __launch_bounds__(kPrepThreads)
+// One CTA per (group, up to 4 heads).  Pi^T and S^T are read from global
+// memory, where every CTA reads the same 128 KB (L2-resident): thread
+// (quarter r, coordinate j) sums rows [32 r, 32 r + 32) with sixteen rows of
+// each matrix in flight at a time.  Pi q and S q are formed in fp32, then every
+// plane's image rows (4 slices x head) and the heads' constants are written.
+// No shared-memory staging of the matrices: two CTAs fit on an SM.
+__global__ void __launch_bounds__(kPrepThreads, 2)
 score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int prod, ParityExpansion px,
                      ParityExpansion px_lo, int frac, const float* __restrict__ PiT, const float* __restrict__ ST,
-                     uint32_t img_bytes, uint8_t* __restrict__ images, float4* __restrict__ consts, int* err) {
+                     uint32_t img_bytes, uint8_t* __restrict__ images, float4* __restrict__ consts) {
   constexpr int d = 128;
   grid_dependents_launch();  // the score kernel may start streaming packed blocks now
-  extern __shared__ float prep_sm[];
-  float* sPi = prep_sm;                 // [d][d] Pi^T
-  float* sS = prep_sm + d * d;          // [d][d] S^T
-  __shared__ float s_q[kPrepHeads][d], s_part[2][2][kPrepHeads][d];
-  __shared__ float red[4 * kPrepHeads][4];
+  __shared__ float4 s_q[d];                          // the CTA's heads' queries, one float4 per coordinate
+  __shared__ float s_part[4][2][kPrepHeads][d];      // quarter sums of Pi q and S q
+  __shared__ float s_full[kPrepHeads][2][d];         // Pi q and S q
+  __shared__ float red[kPrepHeads][4][4];            // [head][warp][sum c0 Pi q, sum S q, max |Pi q|, max |S q|]
   __shared__ float s_coef[kMaxTerms], s_coef_lo[kMaxTerms];  // coordinates 0..63 and 64..127
   const int quads = (H + kPrepHeads - 1) / kPrepHeads;
   const int64_t g = blockIdx.x / quads;
   const int h0 = (blockIdx.x % quads) * kPrepHeads;
   const int nh = min(kPrepHeads, H - h0);
-  const int t = threadIdx.x, j = t & (d - 1), half = t >> 7;
+  const int t = threadIdx.x, r = t >> 7, j = t & (d - 1), lane = t & 31;
   const int N = kSlices * Hp;
-  __shared__ __align__(8) uint64_t s_bar;
-  const uint32_t bar = smem_u32(&s_bar);
-  if (t == 0) {  // Pi^T and S^T (64 KB each) in one round trip
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    const uint32_t bytes = d * d * sizeof(float);
-    mbar_arrive_expect_tx(bar, prod ? 2 * bytes : bytes);
-    bulk_load(smem_u32(sPi), PiT, bytes, bar);
-    if (prod) bulk_load(smem_u32(sS), ST, bytes, bar);
+  if (t < d) {
+    const float* qg = q + (g * H + h0) * d + t;
+    s_q[t] = make_float4(qg[0], nh > 1 ? qg[d] : 0.f, nh > 2 ? qg[2 * d] : 0.f, nh > 3 ? qg[3 * d] : 0.f);
   }
-  if (t < d)
-#pragma unroll
-    for (int hh = 0; hh < kPrepHeads; ++hh) s_q[hh][t] = hh < nh ? q[(g * H + h0 + hh) * d + t] : 0.f;
   if (t < kMaxTerms) {
     s_coef[t] = t < px.n ? px.coef[t] : 0.f;
     // a fractional width's lower codebook (coordinates 64..127), its terms on
     // the same masks (zero where the top code bit is involved)
     s_coef_lo[t] = t < px.n ? (frac ? px_lo.coef[t] : px.coef[t]) : 0.f;
   }
-  __syncthreads();
-  {
-    int no_abort = 0;
-    if (!mbar_wait(bar, 0, &no_abort) && t == 0) atomicExch(err, 1);
-  }
-  // partial sums over i in [64 half, 64 half + 64) for output coordinate j
   float qr[kPrepHeads], sq[kPrepHeads];
 #pragma unroll
   for (int hh = 0; hh < kPrepHeads; ++hh) qr[hh] = sq[hh] = 0.f;
-#pragma unroll 8
-  for (int i = 64 * half; i < 64 * half + 64; ++i) {
-    const float pv = sPi[i * d + j];
-    const float sv = prod ? sS[i * d + j] : 0.f;
 #pragma unroll
-    for (int hh = 0; hh < kPrepHeads; ++hh) {
-      qr[hh] = fmaf(pv, s_q[hh][i], qr[hh]);
-      sq[hh] = fmaf(sv, s_q[hh][i], sq[hh]);
+  for (int b = 0; b < 2; ++b) {
+    const int i0 = 32 * r + 16 * b;
+    float pv[16], sv[16];
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+      pv[ii] = __ldg(PiT + (i0 + ii) * d + j);
+      sv[ii] = __ldg(ST + (i0 + ii) * d + j);
+    }
+    if (b == 0) __syncthreads();  // the queries are in shared memory
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+      const float4 qq = s_q[i0 + ii];
+      qr[0] = fmaf(pv[ii], qq.x, qr[0]);
+      qr[1] = fmaf(pv[ii], qq.y, qr[1]);
+      qr[2] = fmaf(pv[ii], qq.z, qr[2]);
+      qr[3] = fmaf(pv[ii], qq.w, qr[3]);
+      sq[0] = fmaf(sv[ii], qq.x, sq[0]);
+      sq[1] = fmaf(sv[ii], qq.y, sq[1]);
+      sq[2] = fmaf(sv[ii], qq.z, sq[2]);
+      sq[3] = fmaf(sv[ii], qq.w, sq[3]);
     }
   }
 #pragma unroll
   for (int hh = 0; hh < kPrepHeads; ++hh) {
-    s_part[half][0][hh][j] = qr[hh];
-    s_part[half][1][hh][j] = sq[hh];
+    s_part[r][0][hh][j] = qr[hh];
+    s_part[r][1][hh][j] = sq[hh];
   }
   __syncthreads();
-  // full values; per head sum and max |.| (warp shuffles in the first 4 warps)
-  float v[4 * kPrepHeads];
+  // thread (head hh = r, coordinate j) from here on: the full values, and per
+  // head the sum and max |.| over the coordinates (the head's four warps)
+  const int hh = r;
+  const float vqr = (s_part[0][0][hh][j] + s_part[1][0][hh][j]) + (s_part[2][0][hh][j] + s_part[3][0][hh][j]);
+  const float vsq = (s_part[0][1][hh][j] + s_part[1][1][hh][j]) + (s_part[2][1][hh][j] + s_part[3][1][hh][j]);
+  s_full[hh][0][j] = vqr;
+  s_full[hh][1][j] = vsq;
   // the c0 term: c0 of coordinate j's codebook times (Pi q)_j, summed below
-  const float c0j = (frac && j >= 64) ? px_lo.c0 : px.c0;
+  float v[4] = {((frac && j >= 64) ? px_lo.c0 : px.c0) * vqr, vsq, fabsf(vqr), fabsf(vsq)};
 #pragma unroll
-  for (int hh = 0; hh < kPrepHeads; ++hh) {
-    qr[hh] = s_part[0][0][hh][j] + s_part[1][0][hh][j];
-    sq[hh] = s_part[0][1][hh][j] + s_part[1][1][hh][j];
-    v[4 * hh + 0] = c0j * qr[hh];
-    v[4 * hh + 1] = sq[hh];
-    v[4 * hh + 2] = fabsf(qr[hh]);
-    v[4 * hh + 3] = fabsf(sq[hh]);
-  }
-  __syncthreads();
-  if (half == 0) {
+  for (int o = 16; o; o >>= 1)
 #pragma unroll
-    for (int hh = 0; hh < kPrepHeads; ++hh) {
-      s_part[0][0][hh][j] = qr[hh];
-      s_part[0][1][hh][j] = sq[hh];
+    for (int c = 0; c < 4; ++c) {
+      const float x = __shfl_xor_sync(0xffffffffu, v[c], o);
+      v[c] = (c & 2) ? fmaxf(v[c], x) : v[c] + x;
     }
-  }
+  if (lane == 0)
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-#pragma unroll
-    for (int r = 0; r < 4 * kPrepHeads; ++r) {
-      const float x = __shfl_xor_sync(0xffffffffu, v[r], o);
-      v[r] = (r & 2) ? fmaxf(v[r], x) : v[r] + x;
-    }
-  }
-  if (half == 0 && (t & 31) == 0)
-#pragma unroll
-    for (int r = 0; r < 4 * kPrepHeads; ++r) red[r][t >> 5] = v[r];
+    for (int c = 0; c < 4; ++c) red[hh][(t >> 5) & 3][c] = v[c];
   __syncthreads();
   float gmax = 0.f;
   for (int p = 0; p < nA; ++p) gmax = fmaxf(gmax, fmaxf(fabsf(s_coef[p]), fabsf(s_coef_lo[p])));
@@ -571,12 +558,12 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
   const int kk = j, col = kk >> 2, bte = kk & 3;
   const int jc = 32 * (col >> 3) + 8 * bte + c_src[col & 7];
   const float comp = c_comp[col & 3];
-  for (int hh = 0; hh < nh; ++hh) {
+  if (hh < nh) {
     const int h = h0 + hh;
-    const float sum_qr = (red[4 * hh][0] + red[4 * hh][1]) + (red[4 * hh][2] + red[4 * hh][3]);
-    const float sum_sq = (red[4 * hh + 1][0] + red[4 * hh + 1][1]) + (red[4 * hh + 1][2] + red[4 * hh + 1][3]);
-    const float max_qr = fmaxf(fmaxf(red[4 * hh + 2][0], red[4 * hh + 2][1]), fmaxf(red[4 * hh + 2][2], red[4 * hh + 2][3]));
-    const float max_sq = fmaxf(fmaxf(red[4 * hh + 3][0], red[4 * hh + 3][1]), fmaxf(red[4 * hh + 3][2], red[4 * hh + 3][3]));
+    const float sum_qr = (red[hh][0][0] + red[hh][1][0]) + (red[hh][2][0] + red[hh][3][0]);
+    const float sum_sq = (red[hh][0][1] + red[hh][1][1]) + (red[hh][2][1] + red[hh][3][1]);
+    const float max_qr = fmaxf(fmaxf(red[hh][0][2], red[hh][1][2]), fmaxf(red[hh][2][2], red[hh][3][2]));
+    const float max_sq = fmaxf(fmaxf(red[hh][0][3], red[hh][1][3]), fmaxf(red[hh][2][3], red[hh][3][3]));
     // sigma = 2^(2 - e) with max |value| < 2^e: normalised values below 4, so
     // with the compensation (at most 64) every slice stays below 256
     int eA = 0, eB = 0;
@@ -584,10 +571,9 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
     if (mA > 0.f) frexpf(mA, &eA);
     if (mB > 0.f) frexpf(mB, &eB);
     const float sA = ldexpf(1.f, 2 - eA), sB = ldexpf(1.f, 2 - eB);
-    // the two thread halves split the planes
-    for (int p = half; p < nP; p += 2) {
+    for (int p = 0; p < nP; ++p) {
       const float coef = jc < 64 ? s_coef[p] : s_coef_lo[p];
-      float val = p < nA ? coef * s_part[0][0][hh][jc] * comp * sA : 2.f * s_part[0][1][hh][jc] * comp * sB;
+      float val = p < nA ? coef * s_full[hh][0][jc] * comp * sA : 2.f * s_full[hh][1][jc] * comp * sB;
       uint8_t* base = img + (uint32_t)p * (uint32_t)N * 128u;
       float scale = 1.f;
 #pragma unroll
@@ -598,12 +584,12 @@ score_tc_prep_kernel(const float* __restrict__ q, int H, int Hp, int nA, int pro
         scale *= 16.f;
       }
     }
-    if (t == 0) consts[g * Hp + h] = make_float4(1.f / sA, sum_qr, 1.f / sB, -sum_sq);
+    if (j == 0) consts[g * Hp + h] = make_float4(1.f / sA, sum_qr, 1.f / sB, -sum_sq);
   }
   if (h0 == 0) {  // zero rows of the padding heads
-    for (int p = half; p < nP; p += 2) {
+    for (int p = 0; p < nP; ++p) {
       uint8_t* base = img + (uint32_t)p * (uint32_t)N * 128u;
-      for (int hz = H; hz < Hp; ++hz)
+      for (int hz = H + r; hz < Hp; hz += 4)
         for (int sl = 0; sl < kSlices; ++sl) base[img_offset(sl * Hp + hz, kk)] = 0;
     }
   }
@@ -704,15 +690,11 @@ cudaError_t launch_score_tc(const tq_plan* p, const float* queries, int64_t G, i
   if (G * N == 0) return cudaSuccess;
   uint8_t* images = static_cast<uint8_t*>(ws);
   float4* consts = reinterpret_cast<float4*>(images + (((size_t)G * gm.img + 255) & ~(size_t)255));
-  const size_t prep_smem = 2 * 128 * 128 * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(score_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)prep_smem);
-  if (e != cudaSuccess) return e;
   const int64_t prep_blocks = G * ((H + kPrepHeads - 1) / kPrepHeads);
-  score_tc_prep_kernel<<<(unsigned)prep_blocks, kPrepThreads, prep_smem, s>>>(
+  score_tc_prep_kernel<<<(unsigned)prep_blocks, kPrepThreads, 0, s>>>(
       queries, H, gm.Hp, gm.nA, p->lay.prod, p->px, p->px_enc_lo, p->lay.frac, p->PiT, p->lay.prod ? p->ST : p->PiT,
-      gm.img, images, consts, p->err);
-  e = cudaGetLastError();
+      gm.img, images, consts);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   ScoreTcArgs a;

@@ -103,6 +103,28 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// 3-D tiled tensor store shared -> global, tracked in the issuing thread's bulk
+// group.  Box elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk group of this thread has finished reading
+// its shared-memory source (the source may then be rewritten).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until every committed bulk group of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA, tensor core) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -192,5 +214,9 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_type, uint32_t M, u
 // box is box_cols x box_rows elements.
 cudaError_t make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
                          uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+// Host: a 3-D tiled tensor map (dims[0] innermost; strides in bytes of dims 1
+// and 2) with box box[0] x box[1] x box[2] elements.
+cudaError_t make_tmap_3d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, const uint64_t dims[3],
+                         const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle sw);
 
 }  // namespace tq

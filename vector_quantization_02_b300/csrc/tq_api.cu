@@ -192,6 +192,19 @@ cudaError_t make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ba
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_3d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, const uint64_t dims[3],
+                         const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle sw) {
+  EncodeTmapFn enc = tmap_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides[0], strides[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(tm, dt, 3, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Workspace: [tensor-core query images and constants | Pi q, S q] [top-k candidates]
 size_t score_workspace_bytes(const tq_plan* p, int64_t G, int H, int64_t N, int top_k) {
   const size_t prep = score_tc_supported(p, H)     ? score_tc_workspace_bytes(p, G, H)
