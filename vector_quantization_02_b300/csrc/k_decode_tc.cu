@@ -17,13 +17,18 @@
 //  warp 0     bulk copies: once the B images, then each tile's packed block
 //             into a 2-stage ring;
 //  warp 1     TMEM owner (512 columns) and MMA issuer (one thread);
-//  warps 2-5  expansion: thread = key row; code bits -> A operands in TMEM,
-//             through lookup tables built once per CTA that map the code bits
-//             of four coordinates (two for k >= 3) straight to their fp16 hi
-//             and lo operand words;
-//  warps 6-9  epilogue: thread = key row; accumulators -> fp32 rows, staged in
-//             shared memory (128-byte swizzle, conflict-free) and written by
-//             TMA tensor stores that clip the rows past N of a ragged block.
+//  warps 2-9  expansion: thread = (key row, half of the coordinates); code
+//             bits -> A operands in TMEM: for k <= 2 the levels' fp16 bytes sit
+//             in registers and byte permutes pick them for four coordinates at
+//             a time; for k >= 3 a table built once per CTA maps the code bits
+//             of two coordinates to their fp16 hi and lo words;
+//  warps 10-17 epilogue: thread = (key row, half of the coordinates);
+//             accumulators -> fp32 rows, staged in shared memory (128-byte
+//             swizzle, conflict-free) and written by TMA tensor stores that
+//             clip the rows past N of a ragged block.
+// Two warps per TMEM lane quarter in each of these roles: one warp moves only
+// about 32 bytes per cycle between its registers and TMEM, and the rate grows
+// with the number of warps.
 // TMEM columns: D1 [0, 128), D2 [128, 256), A hi [256, 320), A lo [320, 384),
 // signs [384, 448); A columns hold fp16 pairs, k step kb at column 8 kb.
 // Every wait is bounded: on expiry the kernel raises the plan's error word,
@@ -39,8 +44,10 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kDecThreads = 320;
-constexpr int kDecEpi0 = 192;                 // first epilogue thread (warp 6)
+constexpr int kDecSplit = 2;                  // warps per TMEM lane quarter in the expansion and the epilogue
+constexpr int kDecThreads = 64 + 256 * kDecSplit;
+constexpr int kDecExpWarp0 = 2, kDecEpiWarp0 = 2 + 4 * kDecSplit;
+constexpr int kDecEpi0 = 32 * kDecEpiWarp0;   // first epilogue thread
 constexpr int kDecStages = 2;
 constexpr uint32_t kDecImg = 128 * 128 * 2;   // one 128 x 128 fp16 operand image
 constexpr uint32_t kDecAtom = 128 * 128;      // 128 rows x 64 elements (128 B) per swizzle atom
@@ -55,12 +62,14 @@ constexpr uint32_t kOffDecBar = kOffTab + 2 * 256 * 16;
 enum {
   DB_OPS = 0,
   DB_SFULL = 1,
-  DB_SEMPTY = DB_SFULL + kDecStages,  // expansion (128) + epilogue (128) arrivals
-  DB_AFULL = DB_SEMPTY + kDecStages,
-  DB_MDONE,   // a tile's MMAs complete: A may be rewritten, D1 and D2 are full
+  DB_SEMPTY = DB_SFULL + kDecStages,  // expansion + epilogue arrivals (every thread of both)
+  DB_AFULL0 = DB_SEMPTY + kDecStages,  // A columns of k steps 0..3 written
+  DB_AFULL1,  // A columns of k steps 4..7 written
+  DB_H0DONE,  // the MMAs of k steps 0..3 complete: their A columns may be rewritten
+  DB_MDONE,   // all of a tile's MMAs complete: A may be rewritten, D1 and D2 are full
   DB_DEMPTY,
   DB_SFREE,   // the staging buffer may be written (previous tile's stores have read it)
-  DB_STAGED,  // the tile's rows are in the staging buffer (128 epilogue arrivals)
+  DB_STAGED,  // the tile's rows are in the staging buffer (every epilogue thread)
   DB_DONE,
   DB_COUNT
 };
@@ -90,33 +99,27 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
   return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
-// Lookup tables of the expansion, built per CTA from the codebook's split
-// levels ctab (coordinates 0..63) and ctab_lo (64..127, the lower codebook of
-// a fractional width, else ctab again).  For k <= 2 an entry covers four
-// coordinates: key = sum_p nibble_p << 4p (bit u of plane p's nibble belongs
-// to coordinate u), value = {hi pair 0-1, hi pair 2-3, lo pair 0-1, lo pair
-// 2-3}.  For k >= 3 an entry covers two: key = sum_p (2 bits of plane p) << 2p,
-// value = {hi pair, lo pair} (the first half of a uint4).
+// Lookup table of the expansion for k >= 3, built per CTA from the codebook's
+// split levels ctab (coordinates 0..63) and ctab_lo (64..127, the lower
+// codebook of a fractional width, else ctab again).  An entry covers two
+// coordinates: key = sum_p (2 bits of plane p) << 2p, value = {hi pair, lo
+// pair} in the first half of a uint4.  (k <= 2 keeps its levels in registers.)
 template <int K>
 __device__ __forceinline__ void build_dec_tables(const DecTcArgs& a, uint4* tab) {
-  constexpr int U = K <= 2 ? 4 : 2, kEnt = 1 << (U * K);
+  constexpr int kEnt = 1 << (2 * K);
   static_assert(kEnt <= 256, "table");
   for (int e = threadIdx.x; e < 2 * kEnt; e += blockDim.x) {
     const int t = e / kEnt, key = e % kEnt;
     const uint32_t* ct = (t == 1 && a.lay.frac) ? a.ctab_lo : a.ctab;
-    uint32_t c[U];
+    uint32_t c[2];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < 2; ++u) {
       uint32_t idx = 0;
 #pragma unroll
-      for (int p = 0; p < K; ++p) idx |= (uint32_t)((key >> (U * p + u)) & 1) << p;
+      for (int p = 0; p < K; ++p) idx |= (uint32_t)((key >> (2 * p + u)) & 1) << p;
       c[u] = ct[idx];
     }
-    if constexpr (U == 4)
-      tab[t * 256 + key] = make_uint4(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410),
-                                      __byte_perm(c[0], c[1], 0x7632), __byte_perm(c[2], c[3], 0x7632));
-    else
-      tab[t * 256 + key] = make_uint4(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[0], c[1], 0x7632), 0u, 0u);
+    tab[t * 256 + key] = make_uint4(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[0], c[1], 0x7632), 0u, 0u);
   }
 }
 
@@ -128,31 +131,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint32_t sb = smem_u32(smem);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ uint2 s_sgn[16];  // 2 z - 1 of four coordinates as two fp16 pairs, by their four sign bits
   uint4* tab = reinterpret_cast<uint4*>(smem + kOffTab);
   auto bar = [&](int i) { return sb + kOffDecBar + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  build_dec_tables<K>(a, tab);
-  if (threadIdx.x < 16) {
-    // +1 = 0x3C00, -1 = 0xBC00 in fp16; sign bit u of the index is z of coordinate u
-    uint32_t h[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) h[u] = 0x3C00u | ((~(threadIdx.x >> u) & 1u) << 15);
-    s_sgn[threadIdx.x] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-  }
+  if constexpr (K >= 3) build_dec_tables<K>(a, tab);
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar(DB_OPS), 1);
     for (int s = 0; s < kDecStages; ++s) {
       mbar_init(bar(DB_SFULL + s), 1);
-      mbar_init(bar(DB_SEMPTY + s), 256);
+      mbar_init(bar(DB_SEMPTY + s), 256 * kDecSplit);
     }
-    mbar_init(bar(DB_AFULL), 128);
+    mbar_init(bar(DB_AFULL0), 128);
+    mbar_init(bar(DB_AFULL1), 128);
+    mbar_init(bar(DB_H0DONE), 1);
     mbar_init(bar(DB_MDONE), 1);
-    mbar_init(bar(DB_DEMPTY), 128);
+    mbar_init(bar(DB_DEMPTY), 128 * kDecSplit);
     mbar_init(bar(DB_SFREE), 1);
-    mbar_init(bar(DB_STAGED), 128);
+    mbar_init(bar(DB_STAGED), 128 * kDecSplit);
     mbar_init(bar(DB_DONE), 1);
     fence_mbar_init();
   }
@@ -200,8 +197,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // The operand descriptors are built once; every MMA adds a compile-time
-    // offset.  One commit per tile: the expansion (A free) and the epilogue
-    // (D full) both wait on it, each for every phase in turn.
+    // offset.  Two commits per tile, one per half of K: the expansion waits
+    // on each (that half of A free), the epilogue on the second (D full).
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(0u, 128, 128);
       const uint64_t dph = sdesc_k_sw128(sb + kOffPtHi), dpl = sdesc_k_sw128(sb + kOffPtLo);
@@ -211,25 +208,31 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       bool ok = mbar_wait(bar(DB_OPS), 0, abort);
       for (int64_t i = 0; ok && i < n_my; ++i) {
         const uint32_t ph = (uint32_t)i & 1u;
-        if (!mbar_wait(bar(DB_AFULL), ph, abort) || !mbar_wait(bar(DB_DEMPTY), ph ^ 1u, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        // two halves of K: the expansion rewrites the first half of A for the
+        // next tile while the second half's MMAs run
 #pragma unroll
-        for (uint32_t kb = 0; kb < 8; ++kb) {
-          // k step kb: swizzle atom kb / 4 of the image, 32 bytes per step within it
-          // (descriptor address units of 16 bytes); A columns 8 kb
-          const uint64_t off = (uint64_t)(((kb >> 2) * kDecAtom + (kb & 3) * 32) >> 4);
-          mma_f16_ts(d1, ahi + 8 * kb, dph + off, idesc, kb > 0 ? 1u : 0u);
-          mma_f16_ts(d1, ahi + 8 * kb, dpl + off, idesc, 1u);
-          mma_f16_ts(d1, alo + 8 * kb, dph + off, idesc, 1u);
-          if constexpr (PROD) {
-            mma_f16_ts(d2, sg + 8 * kb, dsh + off, idesc, kb > 0 ? 1u : 0u);
-            mma_f16_ts(d2, sg + 8 * kb, dsl + off, idesc, 1u);
+        for (uint32_t h = 0; h < 2; ++h) {
+          if (!mbar_wait(bar(h == 0 ? DB_AFULL0 : DB_AFULL1), ph, abort) ||
+              (h == 0 && !mbar_wait(bar(DB_DEMPTY), ph ^ 1u, abort))) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t kb = 4 * h; kb < 4 * h + 4; ++kb) {
+            // k step kb: swizzle atom kb / 4 of the image, 32 bytes per step within it
+            // (descriptor address units of 16 bytes); A columns 8 kb
+            const uint64_t off = (uint64_t)(((kb >> 2) * kDecAtom + (kb & 3) * 32) >> 4);
+            mma_f16_ts(d1, ahi + 8 * kb, dph + off, idesc, kb > 0 ? 1u : 0u);
+            mma_f16_ts(d1, ahi + 8 * kb, dpl + off, idesc, 1u);
+            mma_f16_ts(d1, alo + 8 * kb, dph + off, idesc, 1u);
+            if constexpr (PROD) {
+              mma_f16_ts(d2, sg + 8 * kb, dsh + off, idesc, kb > 0 ? 1u : 0u);
+              mma_f16_ts(d2, sg + 8 * kb, dsl + off, idesc, 1u);
+            }
+          }
+          mma_commit(bar(h == 0 ? DB_H0DONE : DB_MDONE));
         }
-        mma_commit(bar(DB_MDONE));
       }
       if (!ok) raise_dec(a.err, abort);
       // all issued MMAs complete before TMEM is freed
@@ -237,9 +240,26 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       int dummy = 0;
       mbar_wait(bar(DB_DONE), 0, &dummy);
     }
-  } else if (warp < 6) {
+  } else if (warp < kDecEpiWarp0) {
     // ------------------------------------------------------------ expansion
-    const int quad = warp & 3;
+    // half hh of the coordinates: words 2 hh and 2 hh + 1 of each plane
+    const int quad = warp & 3, hh = (warp - kDecExpWarp0) >> 2;
+    // levels 0..3 of each codebook (k <= 2): fp16 hi (h) and lo (l) parts,
+    // levels 0, 1 in x and 2, 3 in y
+    struct {
+      uint32_t hx0, hy0, lx0, ly0, hx1, hy1, lx1, ly1;
+    } lv;
+    {
+      const uint32_t* c1 = a.lay.frac ? a.ctab_lo : a.ctab;
+      lv.hx0 = __byte_perm(a.ctab[0], a.ctab[1], 0x5410);
+      lv.hy0 = __byte_perm(a.ctab[2], a.ctab[3], 0x5410);
+      lv.lx0 = __byte_perm(a.ctab[0], a.ctab[1], 0x7632);
+      lv.ly0 = __byte_perm(a.ctab[2], a.ctab[3], 0x7632);
+      lv.hx1 = __byte_perm(c1[0], c1[1], 0x5410);
+      lv.hy1 = __byte_perm(c1[2], c1[3], 0x5410);
+      lv.lx1 = __byte_perm(c1[0], c1[1], 0x7632);
+      lv.ly1 = __byte_perm(c1[2], c1[3], 0x7632);
+    }
     const int row = quad * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
@@ -247,12 +267,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int s = (int)(i % kDecStages);
       // every lane polls; the warp proceeds (or gives up) as one, because the
       // tcgen05 stores below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(DB_SFULL + s), (uint32_t)(i / kDecStages) & 1u, abort)) ||
-          !__all_sync(0xffffffffu, mbar_wait(bar(DB_MDONE), ((uint32_t)i & 1u) ^ 1u, abort))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(DB_SFULL + s), (uint32_t)(i / kDecStages) & 1u, abort))) {
         ok = false;
         break;
       }
-      tc_fence_after();
       // this key's 16-byte chunk of every plane (d = 128: one chunk per plane)
       const uint8_t* blk = smem + kOffBlk + s * kBlkMax;
       uint4 pw[K];
@@ -268,27 +286,47 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       uint4 zw = make_uint4(0u, 0u, 0u, 0u);
       if constexpr (PROD) zw = *reinterpret_cast<const uint4*>(blk + a.lay.sign_off + row * 16);
       mbar_arrive(bar(DB_SEMPTY + s));
+      // half h of A (words 2 h, 2 h + 1: k steps 4 h .. 4 h + 3) once the
+      // previous tile's MMAs on it are complete
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
+      for (int hx = 0; hx < 2 / kDecSplit; ++hx) {
+      const int h = (2 / kDecSplit) * hh + hx;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(h == 0 ? DB_H0DONE : DB_MDONE), ((uint32_t)i & 1u) ^ 1u, abort))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ww = 0; ww < 2; ++ww) {
         // coordinates 32 w + e, e = 0..31: bit e of word w of each plane;
-        // table 1 for coordinates 64..127
+        // the lower codebook's levels for coordinates 64..127
+        const int w = 2 * h + ww;
         uint32_t wp[K];
 #pragma unroll
         for (int p = 0; p < K; ++p) wp[p] = word_of(pw[p], w);
-        const uint4* tw = tab + (w >> 1) * 256;
         uint32_t hi[16], lo[16];
         if constexpr (K <= 2) {
+          // Levels in registers: the fp16 bytes of levels 0..3 (hi and lo
+          // parts), picked by byte permutes.  For four coordinates, byte u of
+          // S is coordinate u's level index, and byte u of T = 0x22 S +
+          // 0x10101010 holds the selectors (2 idx, 2 idx + 1) of that level's
+          // two bytes; T's low half selects coordinates 0, 1, its high half 2, 3.
+          const uint32_t thx = w < 2 ? lv.hx0 : lv.hx1, thy = w < 2 ? lv.hy0 : lv.hy1;
+          const uint32_t tlx = w < 2 ? lv.lx0 : lv.lx1, tly = w < 2 ? lv.ly0 : lv.ly1;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            uint32_t key = (wp[0] >> (4 * q)) & 0xFu;
-            if constexpr (K == 2) key |= ((wp[1] >> (4 * q)) & 0xFu) << 4;
-            const uint4 e = tw[key];
-            hi[2 * q] = e.x;
-            hi[2 * q + 1] = e.y;
-            lo[2 * q] = e.z;
-            lo[2 * q + 1] = e.w;
+            // bit u of a nibble to bit 8 u: x * 0x204081 places the four
+            // shifted copies without overlap
+            uint32_t S = (((wp[0] >> (4 * q)) & 0xFu) * 0x00204081u) & 0x01010101u;
+            if constexpr (K == 2) S |= (((wp[1] >> (4 * q)) & 0xFu) * 0x00408102u) & 0x02020202u;
+            const uint32_t T = S * 0x22u + 0x10101010u;
+            hi[2 * q] = __byte_perm(thx, thy, T);
+            hi[2 * q + 1] = __byte_perm(thx, thy, T >> 16);
+            lo[2 * q] = __byte_perm(tlx, tly, T);
+            lo[2 * q + 1] = __byte_perm(tlx, tly, T >> 16);
           }
         } else {
+          const uint4* tw = tab + (w >> 1) * 256;
 #pragma unroll
           for (int m = 0; m < 16; ++m) {
             uint32_t key = 0;
@@ -302,28 +340,34 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         tmem_st16(t_lane + kColAHi + 16 * w, hi);
         tmem_st16(t_lane + kColALo + 16 * w, lo);
         if constexpr (PROD) {
-          const uint32_t z = word_of(zw, w);
+          // 2 z - 1 as fp16 (+1 = 0x3C00, -1 = 0xBC00): byte u of S is 1 - z of
+          // coordinate u; the selectors pick 0x00 for the low byte and 0x3C or
+          // 0xBC for the high byte of each value
+          const uint32_t nz = ~word_of(zw, w);
           uint32_t sg[16];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const uint2 e = s_sgn[(z >> (4 * q)) & 0xFu];
-            sg[2 * q] = e.x;
-            sg[2 * q + 1] = e.y;
+            const uint32_t S = (((nz >> (4 * q)) & 0xFu) * 0x00204081u) & 0x01010101u;
+            const uint32_t T = (S << 4) | 0x02020202u;
+            sg[2 * q] = __byte_perm(0x0000BC3Cu, 0u, T);
+            sg[2 * q + 1] = __byte_perm(0x0000BC3Cu, 0u, T >> 16);
           }
           tmem_st16(t_lane + kColSg + 16 * w, sg);
         }
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(DB_AFULL));
+      mbar_arrive(bar(h == 0 ? DB_AFULL0 : DB_AFULL1));
+      }
     }
     if (!ok) raise_dec(a.err, abort);
   } else {
     // ------------------------------------------------------------ epilogue
-    // Thread = key row.  Rows go to the staging buffer (box q = fp32 columns
-    // 32 q .. 32 q + 31, 128-byte rows whose 16-byte chunks are XOR-swizzled
-    // by row % 8), then thread kDecEpi0 writes the tile with four TMA stores.
-    const int quad = warp & 3;
+    // Thread = (key row, half hh of the coordinates).  Rows go to the staging
+    // buffer (box q = fp32 columns 32 q .. 32 q + 31, 128-byte rows whose
+    // 16-byte chunks are XOR-swizzled by row % 8), then thread kDecEpi0 writes
+    // the tile with four TMA stores.
+    const int quad = warp & 3, hh = (warp - kDecEpiWarp0) >> 2;
     const int row = quad * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     const bool leader = threadIdx.x == kDecEpi0;
@@ -357,12 +401,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
+      for (int q = (4 / kDecSplit) * hh; q < (4 / kDecSplit) * (hh + 1); ++q) {
         uint32_t v1[32], v2[32];
         tmem_ld32(t_lane + kColD1 + 32 * q, v1);
         if constexpr (PROD) tmem_ld32(t_lane + kColD2 + 32 * q, v2);
         tmem_ld_wait();
-        if (q == 3) {  // both accumulators read: the next tile's MMAs may write them
+        if (q == (4 / kDecSplit) * (hh + 1) - 1) {  // accumulators read: the next tile's MMAs may write them
           tc_fence_before();
           mbar_arrive(bar(DB_DEMPTY));
         }
