@@ -291,6 +291,21 @@ const char* tq_status_string(tq_status status);
  * context and the plan stay usable.  Errors: TQ_EINVAL (null plan), TQ_ECUDA. */
 tq_status tq_selftest_wait_expiry(tq_plan* plan, void* stream);
 
+/* Self-test of the error path of a real kernel (no GPU fault is involved):
+ * runs tq_encode's tensor-core encode (d = 128, fp16/bf16 keys) on the given
+ * keys, except that the producer of CTA 0 withholds the copy of its first key
+ * tile.  The waits on that tile give up after their poll limit (about a
+ * second) and raise the plan's error word; every role of that CTA then stops,
+ * waits for the copies and MMAs it issued and frees its TMEM; the other CTAs
+ * finish normally.  After the caller synchronises, tq_plan_status reports
+ * TQ_ETIMEOUT (and clears the word); `packed` holds no usable result, and the
+ * context and the plan stay usable.  Arguments and layout as tq_encode.
+ * Errors: TQ_EINVAL (null plan or pointer, G or N < 1, other dtypes),
+ * TQ_EALIGN, TQ_EUNSUPPORTED (a plan or size the d = 128 encode does not
+ * take), TQ_ECUDA. */
+tq_status tq_selftest_encode_drain(tq_plan* plan, const void* keys, tq_dtype dtype, int64_t n_groups,
+                                   int64_t n_tokens, void* packed, void* stream);
+
 /* Version of the packed layout described above (bumped on any change). */
 int tq_format_version(void);
 

@@ -268,6 +268,26 @@ def test_dispatch_paths(cuda, d, bits, mode, H, dtype, score_path, encode_path):
     assert plan.encode_path(dtype) == encode_path
 
 
+@pytest.mark.parametrize("G,N", [(1, 300), (8, 12000)])
+def test_encode_drain_is_reported(cuda, G, N):
+    """A real kernel's error path: the d = 128 encode runs with one key tile's
+    copy withheld; the waits on it give up, the CTA drains what it issued and
+    frees its TMEM, the plan's error word reads TQ_ETIMEOUT once, and the next
+    encode on the same context and plan matches the oracle."""
+    d = 128
+    w, inp = _case_inputs(d, G, N, torch.float16, 3, "prod", True)
+    plan = inp.plan()
+    keys = tq_synth.keys(w).to(cuda)
+    plan.selftest_encode_drain(keys)
+    torch.cuda.synchronize()
+    assert plan.status() == -5
+    assert plan.status() == 0
+    packed = tq.tq_encode(plan, keys)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    compare_encode(inp, packed.cpu().numpy(), keys.cpu())
+
+
 def test_bounded_wait_expiry_is_reported(cuda):
     """A device wait that nothing satisfies gives up after its poll limit and
     raises the plan's error word (TQ_ETIMEOUT once); nothing faults, and the

@@ -49,6 +49,7 @@ def _load() -> ctypes.CDLL:
         "tq_encode_path": (c_int, [vp, c_int]),
         "tq_decode_path": (c_int, [vp]),
         "tq_selftest_wait_expiry": (c_int, [vp, vp]),
+        "tq_selftest_encode_drain": (c_int, [vp, vp, c_int, c_i64, c_i64, vp, vp]),
         "tq_encode_values": (c_int, [vp, vp, c_int, c_i64, c_i64, vp, vp]),
         "tq_attend_workspace_bytes": (c_sz, [vp, vp, c_i64, c_int, c_i64]),
         "tq_attend": (c_int, [vp, vp, vp, c_i64, c_int, vp, vp, c_i64, ctypes.c_float, vp, vp, c_sz, vp]),
@@ -67,7 +68,8 @@ EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_p
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
             "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
             "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path", "tq_decode_path",
-            "tq_selftest_wait_expiry", "tq_encode_values", "tq_attend_workspace_bytes", "tq_attend")
+            "tq_selftest_wait_expiry", "tq_selftest_encode_drain", "tq_encode_values", "tq_attend_workspace_bytes",
+            "tq_attend")
 PATHS = {0: "tensor_d128", 1: "tensor_wide", 2: "cuda_core"}
 TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
 
@@ -230,6 +232,18 @@ class Plan:
     def selftest_wait_expiry(self, stream=None) -> None:
         """Enqueue the bounded-wait self-test; after a sync, status() reports TQ_ETIMEOUT once."""
         _check(lib.tq_selftest_wait_expiry(self.handle, ctypes.c_void_p(_stream(stream))), "tq_selftest_wait_expiry")
+
+    def selftest_encode_drain(self, keys: torch.Tensor, stream=None) -> None:
+        """Enqueue the d = 128 encode of keys [G][N][128] (fp16/bf16) with CTA 0's
+        first key tile withheld; after a sync, status() reports TQ_ETIMEOUT once."""
+        G, N, d = keys.shape
+        if d != self.d or keys.dtype not in (torch.float16, torch.bfloat16):
+            raise ValueError("the self-test takes fp16/bf16 keys of the plan's d")
+        packed = torch.empty(self.packed_bytes(G, N), dtype=torch.uint8, device=keys.device)
+        _check(lib.tq_selftest_encode_drain(self.handle, _dev(keys, "keys"), _DTYPES[keys.dtype], G, N,
+                                            _dev(packed, "packed"), ctypes.c_void_p(_stream(stream))),
+               "tq_selftest_encode_drain")
+        self._drain_buffers = (keys, packed)  # alive until the caller synchronises
 
     def score_path(self, H: int) -> str:
         """Kernel family tq_score takes for H heads: tensor_d128 or tensor_wide."""

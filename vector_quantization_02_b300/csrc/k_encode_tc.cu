@@ -81,6 +81,9 @@ struct EncTcArgs {
   int frac;
   CodeParams cp_lo;
   ParityExpansion px_lo;
+  // error-path self-test only (tq_selftest_encode_drain): CTA 0's producer
+  // withholds the copy of its first key tile, so the waits on it run out
+  int drop_first;
 };
 
 __device__ __forceinline__ void raise(int* err, volatile int* abort) {
@@ -154,13 +157,18 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
         bulk_load(sb + kOffMHi, a.m_hi, kOpBytes, bar(BAR_OPS));
         bulk_load(sb + kOffMLo, a.m_lo, kOpBytes, bar(BAR_OPS));
       }
-      int64_t issued = 0;
+      int64_t issued = 0, withheld = -1;
       for (int64_t i = 0; i < n_my; ++i) {
         const int s = (int)(i % kStages);
         const uint32_t use = (uint32_t)(i / kStages);
         if (!mbar_wait(bar(BAR_XEMPTY + s), (use & 1) ^ 1, abort)) {
           raise(a.err, abort);
           break;
+        }
+        if (i == 0 && a.drop_first && blockIdx.x == 0) {  // self-test: no copy, no arrival
+          withheld = 0;
+          issued = 1;
+          continue;
         }
         const int64_t tile = blockIdx.x + i * gridDim.x;
         const int64_t g = tile / a.nb, blk = tile % a.nb;
@@ -173,7 +181,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       // no copy may still be landing when the CTA exits: wait for the last loads
       int dummy = 0;
       for (int64_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        mbar_wait(bar(BAR_XFULL + (int)(i % kStages)), (uint32_t)(i / kStages) & 1, &dummy);
+        if (i != withheld) mbar_wait(bar(BAR_XFULL + (int)(i % kStages)), (uint32_t)(i / kStages) & 1, &dummy);
       mbar_wait(bar(BAR_OPS), 0, &dummy);
     }
   } else if (warp == 1 || warp == kE5Warp) {
@@ -482,7 +490,8 @@ bool odd_masks(const ParityExpansion& px, int k) {
 }
 
 template <int L, bool kBF16, bool PX, bool PROD>
-cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, uint8_t* packed, cudaStream_t s) {
+cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, uint8_t* packed, cudaStream_t s,
+                      bool drop_first) {
   CUtensorMap tm;
   const cudaError_t te = make_tmap_2d(&tm, kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                                       keys, 128, (uint64_t)(G * N), 256, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -507,6 +516,7 @@ cudaError_t launch_tc(const tq_plan* p, const void* keys, int64_t G, int64_t N, 
   a.m_lo = PROD ? ops + 5 * kOpBytes : nullptr;
   a.packed = packed;
   a.err = p->err;
+  a.drop_first = drop_first ? 1 : 0;
   auto kern = encode_tc_kernel<L, kBF16, PX, PROD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -526,16 +536,16 @@ bool encode_tc_supported(const tq_plan* p, tq_dtype dt) {
 }
 
 cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N, uint8_t* packed,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool drop_first) {
   const bool bf = dt == TQ_BF16;
   const int k = p->cp.L == 2 ? 1 : p->cp.L == 4 ? 2 : p->cp.L == 8 ? 3 : 4;
   const bool px = odd_masks(p->px, k);
   const bool prod = p->lay.prod != 0;
 #define TQ_ENC_CASE(LV, PR)                                                                                    \
-  if (px) return bf ? launch_tc<LV, true, true, PR>(p, keys, G, N, packed, s)                                  \
-                    : launch_tc<LV, false, true, PR>(p, keys, G, N, packed, s);                                \
-  return bf ? launch_tc<LV, true, false, PR>(p, keys, G, N, packed, s)                                         \
-            : launch_tc<LV, false, false, PR>(p, keys, G, N, packed, s);
+  if (px) return bf ? launch_tc<LV, true, true, PR>(p, keys, G, N, packed, s, drop_first)                                  \
+                    : launch_tc<LV, false, true, PR>(p, keys, G, N, packed, s, drop_first);                                \
+  return bf ? launch_tc<LV, true, false, PR>(p, keys, G, N, packed, s, drop_first)                                         \
+            : launch_tc<LV, false, false, PR>(p, keys, G, N, packed, s, drop_first);
   switch (p->cp.L) {
     case 2:
       if (prod) { TQ_ENC_CASE(2, true) }
@@ -547,8 +557,8 @@ cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, in
       if (prod) { TQ_ENC_CASE(8, true) }
       TQ_ENC_CASE(8, false)
     case 16:  // 4-bit MSE codebooks: no parity expansion of that size
-      if (!prod) return bf ? launch_tc<16, true, false, false>(p, keys, G, N, packed, s)
-                           : launch_tc<16, false, false, false>(p, keys, G, N, packed, s);
+      if (!prod) return bf ? launch_tc<16, true, false, false>(p, keys, G, N, packed, s, drop_first)
+                           : launch_tc<16, false, false, false>(p, keys, G, N, packed, s, drop_first);
       break;
   }
 #undef TQ_ENC_CASE

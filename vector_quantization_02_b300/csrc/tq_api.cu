@@ -255,6 +255,16 @@ tq_status tq_selftest_wait_expiry(tq_plan* p, void* stream) {
   return from_cuda(tq::launch_wait_expiry(p->err, static_cast<cudaStream_t>(stream)));
 }
 
+tq_status tq_selftest_encode_drain(tq_plan* p, const void* keys, tq_dtype dtype, int64_t G, int64_t N,
+                                   void* packed, void* stream) {
+  if (!p || G < 1 || N < 1 || !keys || !packed) return TQ_EINVAL;
+  if (dtype != TQ_F16 && dtype != TQ_BF16) return TQ_EINVAL;
+  if (!aligned16(keys) || !aligned16(packed)) return TQ_EALIGN;
+  if (G * N >= (int64_t)INT32_MAX - 2 * kTokensPerBlock || !encode_tc_supported(p, dtype)) return TQ_EUNSUPPORTED;
+  return from_cuda(launch_encode_tc(p, keys, dtype, G, N, static_cast<uint8_t*>(packed),
+                                    static_cast<cudaStream_t>(stream), true));
+}
+
 int tq_score_path(const tq_plan* p, int H) {
   if (!p || H < 1 || H > 256) return TQ_EINVAL;
   if (tq::score_tc_supported(p, H)) return TQ_PATH_TENSOR_D128;

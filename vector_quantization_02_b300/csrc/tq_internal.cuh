@@ -99,8 +99,9 @@ namespace tq {
 // ---- launchers (one per kernel family); all return cudaGetLastError()
 cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s);
 bool encode_tc_supported(const tq_plan* p, tq_dtype dt);
+// drop_first: error-path self-test only (CTA 0 withholds its first key tile)
 cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, int64_t G, int64_t N, uint8_t* packed,
-                             cudaStream_t s);
+                             cudaStream_t s, bool drop_first = false);
 cudaError_t launch_topk(const float* logits, int64_t rows, int64_t N, int k, float* top_scores,
                         int64_t* top_idx, void* ws, cudaStream_t s);
 cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
