@@ -162,6 +162,23 @@ tq_status tq_plan_destroy(tq_plan* plan);
  * Returns 0 for a null plan or negative sizes. */
 size_t tq_packed_bytes(const tq_plan* plan, int64_t n_groups, int64_t n_tokens);
 
+/* Packed-cache header, so that a packed buffer can be stored and reloaded as
+ * plain bytes.  64 bytes, little-endian: uint32 magic "TQPK", uint32
+ * tq_format_version(), uint32 d, bits, mode, kind flags (1: Walsh-Hadamard
+ * plan, 2: fractional width), int64 n_groups, n_tokens, uint64 bytes per
+ * 128-token block, uint64 plan fingerprint (a hash of d, bits, mode, kind and
+ * the bytes of Pi, S and the codebooks given at plan creation), uint64
+ * checksum of the preceding 56 bytes.  The header is HOST memory owned by the
+ * caller; no GPU work.  tq_packed_header_write fills `header`
+ * (TQ_EINVAL for a null plan or pointer, negative sizes).
+ * tq_packed_header_read checks `header` against `plan` and returns the sizes
+ * it describes: TQ_EINVAL for a null plan or pointer, a wrong magic or a
+ * damaged header; TQ_EUNSUPPORTED for a header written for another format
+ * version, layout or plan (the bytes would decode to other keys). */
+#define TQ_PACKED_HEADER_BYTES 64
+tq_status tq_packed_header_write(const tq_plan* plan, int64_t n_groups, int64_t n_tokens, void* header);
+tq_status tq_packed_header_read(const tq_plan* plan, const void* header, int64_t* n_groups, int64_t* n_tokens);
+
 /* ---------------------------------------------------------------- the path */
 
 /* Encode keys ([PT-KR] 1단계 + 2단계; usage listing: ``tq.compress``):

@@ -77,6 +77,8 @@ def test_argument_errors_need_no_gpu():
     assert lib.tq_decode_path(None) == -1
     assert lib.tq_selftest_wait_expiry(None, None) == -1
     assert lib.tq_selftest_encode_drain(None, None, 1, 1, 1, None, None) == -1
+    assert lib.tq_packed_header_write(None, 1, 1, None) == -1
+    assert lib.tq_packed_header_read(None, None, None, None) == -1
 
 
 @pytest.mark.parametrize("levels", [2, 4, 8, 16])

@@ -288,6 +288,39 @@ def test_encode_drain_is_reported(cuda, G, N):
     compare_encode(inp, packed.cpu().numpy(), keys.cpu())
 
 
+def test_packed_header_round_trip(cuda):
+    """A packed cache stored as header + bytes reloads under the plan that wrote
+    it and is refused under any other: another rotation, bit width, mode or
+    format, or a damaged header."""
+    d, G, N = 128, 2, 300
+    w, inp = _case_inputs(d, G, N, torch.float16, 3, "prod", False)
+    plan = inp.plan()
+    keys = tq_synth.keys(w).to(cuda)
+    packed = tq.tq_encode(plan, keys)
+    header = plan.packed_header(G, N)
+    assert len(header) == 64 and header[:4] == b"TQPK"
+    stored = header + packed.cpu().numpy().tobytes()
+    # reload: the header gives the sizes, the bytes decode to the same keys
+    g2, n2 = plan.read_packed_header(stored[:64])
+    assert (g2, n2) == (G, N)
+    again = torch.frombuffer(bytearray(stored[64:]), dtype=torch.uint8).to(cuda)
+    torch.cuda.synchronize()
+    assert torch.equal(tq.tq_decode(plan, again, g2, n2), tq.tq_decode(plan, packed, G, N))
+    # a damaged header
+    bad = bytearray(header)
+    bad[33] ^= 1
+    with pytest.raises(tq.TQError):
+        plan.read_packed_header(bytes(bad))
+    # the same shape under other plans
+    others = [Inputs(d, 3, "prod", 99, 98).plan(), Inputs(d, 4, "prod", 11, 12).plan(),
+              Inputs(d, 3, "mse", 11, 12).plan()]
+    for other in others:
+        with pytest.raises(tq.TQError):
+            other.read_packed_header(header)
+    # the plan's own fingerprint does not depend on when it was built
+    assert inp.plan().read_packed_header(header) == (G, N)
+
+
 def test_bounded_wait_expiry_is_reported(cuda):
     """A device wait that nothing satisfies gives up after its poll limit and
     raises the plan's error word (TQ_ETIMEOUT once); nothing faults, and the

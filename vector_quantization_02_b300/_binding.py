@@ -49,6 +49,8 @@ def _load() -> ctypes.CDLL:
         "tq_encode_path": (c_int, [vp, c_int]),
         "tq_decode_path": (c_int, [vp]),
         "tq_selftest_wait_expiry": (c_int, [vp, vp]),
+        "tq_packed_header_write": (c_int, [vp, c_i64, c_i64, vp]),
+        "tq_packed_header_read": (c_int, [vp, vp, vp, vp]),
         "tq_selftest_encode_drain": (c_int, [vp, vp, c_int, c_i64, c_i64, vp, vp]),
         "tq_encode_values": (c_int, [vp, vp, c_int, c_i64, c_i64, vp, vp]),
         "tq_attend_workspace_bytes": (c_sz, [vp, vp, c_i64, c_int, c_i64]),
@@ -68,10 +70,12 @@ EXPORTED = ("tq_lloyd_max_codebook", "tq_haar_rotation", "tq_plan_create", "tq_p
             "tq_packed_bytes", "tq_encode", "tq_score_workspace_bytes", "tq_score", "tq_decode",
             "tq_score_fp32", "tq_plan_status", "tq_status_string", "tq_format_version", "tq_score_noalloc",
             "tq_codebook_parity_expansion", "tq_score_path", "tq_encode_path", "tq_decode_path",
-            "tq_selftest_wait_expiry", "tq_selftest_encode_drain", "tq_encode_values", "tq_attend_workspace_bytes",
+            "tq_selftest_wait_expiry", "tq_selftest_encode_drain", "tq_packed_header_write",
+            "tq_packed_header_read", "tq_encode_values", "tq_attend_workspace_bytes",
             "tq_attend")
 PATHS = {0: "tensor_d128", 1: "tensor_wide", 2: "cuda_core"}
 TQ_SCORE_NOALLOC_MAX_BYTES = 32 << 20
+TQ_PACKED_HEADER_BYTES = 64
 
 
 class TQError(RuntimeError):
@@ -244,6 +248,21 @@ class Plan:
                                             _dev(packed, "packed"), ctypes.c_void_p(_stream(stream))),
                "tq_selftest_encode_drain")
         self._drain_buffers = (keys, packed)  # alive until the caller synchronises
+
+    def packed_header(self, G: int, N: int) -> bytes:
+        """The 64-byte header describing a packed buffer of G x N keys of this plan."""
+        buf = ctypes.create_string_buffer(TQ_PACKED_HEADER_BYTES)
+        _check(lib.tq_packed_header_write(self.handle, G, N, buf), "tq_packed_header_write")
+        return buf.raw
+
+    def read_packed_header(self, header: bytes) -> tuple[int, int]:
+        """(G, N) of a header written for this plan; raises TQError otherwise."""
+        if len(header) != TQ_PACKED_HEADER_BYTES:
+            raise ValueError("a packed header is 64 bytes")
+        G, N = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib.tq_packed_header_read(self.handle, header, ctypes.byref(G), ctypes.byref(N)),
+               "tq_packed_header_read")
+        return G.value, N.value
 
     def score_path(self, H: int) -> str:
         """Kernel family tq_score takes for H heads: tensor_d128 or tensor_wide."""

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <new>
 #include <type_traits>
+#include <cstddef>
 #include <vector>
 
 #include "ptx_sm100.cuh"
@@ -336,6 +337,59 @@ void pad_lower_codebook(const CodeParams& lo, const ParityExpansion& pxlo, const
   px->mid = (float)mid;
 }
 
+// 64-bit hash of bytes, eight at a time (a multiply-xorshift mix per word,
+// then a final avalanche); identifies a plan's inputs in packed-cache headers
+struct Hash64 {
+  uint64_t h = 0x9E3779B97F4A7C15ull;
+  void word(uint64_t w) {
+    h ^= w + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+    h *= 0xBF58476D1CE4E5B9ull;
+    h ^= h >> 31;
+  }
+  void bytes(const void* p, size_t n) {
+    const unsigned char* b = static_cast<const unsigned char*>(p);
+    size_t i = 0;
+    for (; i + 8 <= n; i += 8) {
+      uint64_t w;
+      std::memcpy(&w, b + i, 8);
+      word(w);
+    }
+    uint64_t t = 0;
+    std::memcpy(&t, b + i, n - i);
+    word(t ^ ((uint64_t)n << 56));
+  }
+  uint64_t done() const {
+    uint64_t z = h;
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ull;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+  }
+};
+
+cudaError_t plan_fingerprint(tq_plan* p, const float* codebook_host, const float* codebook_lo_host, cudaStream_t s) {
+  Hash64 h;
+  const int32_t head[5] = {p->d, p->bits, p->mode, p->hadamard, p->lay.frac};
+  h.bytes(head, sizeof(head));
+  const size_t mat = (size_t)p->d * p->d;
+  std::vector<float> m(mat);
+  cudaError_t e = cudaMemcpyAsync(m.data(), p->Pi, mat * sizeof(float), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  h.bytes(m.data(), mat * sizeof(float));
+  if (p->lay.prod) {
+    e = cudaMemcpyAsync(m.data(), p->S, mat * sizeof(float), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    h.bytes(m.data(), mat * sizeof(float));
+  }
+  h.bytes(codebook_host, (size_t)p->cp.L * sizeof(float));
+  if (codebook_lo_host) h.bytes(codebook_lo_host, (size_t)p->cp_lo.L * sizeof(float));
+  p->fingerprint = h.done();
+  return cudaSuccess;
+}
+
 tq_status create_plan(int d, int bits, tq_mode mode, const float* Pi, const float* S, const float* codebook,
                       void* stream, int hadamard, tq_plan** out, const float* codebook_lo = nullptr) {
   if (!out) return TQ_EINVAL;
@@ -475,6 +529,10 @@ tq_status create_plan(int d, int bits, tq_mode mode, const float* Pi, const floa
       return we == cudaErrorMemoryAllocation ? TQ_ENOMEM : TQ_ECUDA;
     }
   }
+  if (plan_fingerprint(p, hc, codebook_lo ? p->cp_lo.c : nullptr, s) != cudaSuccess) {
+    free_plan(p);
+    return TQ_ECUDA;
+  }
   *out = p;
   return TQ_OK;
 }
@@ -540,6 +598,57 @@ size_t tq_packed_bytes(const tq_plan* p, int64_t G, int64_t N) {
   if (!p || G < 0 || N < 0) return 0;
   const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
   return (size_t)(G * nb) * (size_t)p->lay.block_bytes;
+}
+
+// Packed-cache header (64 bytes, little-endian): magic, format version, d,
+// bits, mode, kind flags, G, N, block bytes, plan fingerprint, checksum of the
+// first 56 bytes.
+namespace {
+constexpr uint32_t kHeaderMagic = 0x4B505154u;  // "TQPK"
+struct PackedHeader {
+  uint32_t magic, version, d, bits, mode, flags;
+  int64_t G, N;
+  uint64_t block_bytes, fingerprint, check;
+};
+static_assert(sizeof(PackedHeader) == TQ_PACKED_HEADER_BYTES, "header size");
+uint64_t header_check(const PackedHeader& h) {
+  Hash64 x;
+  x.bytes(&h, offsetof(PackedHeader, check));
+  return x.done();
+}
+}  // namespace
+
+tq_status tq_packed_header_write(const tq_plan* p, int64_t G, int64_t N, void* header) {
+  if (!p || G < 0 || N < 0 || !header) return TQ_EINVAL;
+  PackedHeader h;
+  std::memset(&h, 0, sizeof(h));
+  h.magic = kHeaderMagic;
+  h.version = (uint32_t)tq_format_version();
+  h.d = (uint32_t)p->d;
+  h.bits = (uint32_t)p->bits;
+  h.mode = (uint32_t)p->mode;
+  h.flags = (p->hadamard ? 1u : 0u) | (p->lay.frac ? 2u : 0u);
+  h.G = G;
+  h.N = N;
+  h.block_bytes = (uint64_t)p->lay.block_bytes;
+  h.fingerprint = p->fingerprint;
+  h.check = header_check(h);
+  std::memcpy(header, &h, sizeof(h));
+  return TQ_OK;
+}
+
+tq_status tq_packed_header_read(const tq_plan* p, const void* header, int64_t* G, int64_t* N) {
+  if (!p || !header) return TQ_EINVAL;
+  PackedHeader h;
+  std::memcpy(&h, header, sizeof(h));
+  if (h.magic != kHeaderMagic || h.check != header_check(h)) return TQ_EINVAL;
+  if (h.version != (uint32_t)tq_format_version() || h.d != (uint32_t)p->d || h.bits != (uint32_t)p->bits ||
+      h.mode != (uint32_t)p->mode || h.flags != ((p->hadamard ? 1u : 0u) | (p->lay.frac ? 2u : 0u)) ||
+      h.block_bytes != (uint64_t)p->lay.block_bytes || h.fingerprint != p->fingerprint || h.G < 0 || h.N < 0)
+    return TQ_EUNSUPPORTED;
+  if (G) *G = h.G;
+  if (N) *N = h.N;
+  return TQ_OK;
 }
 
 tq_status tq_encode(const tq_plan* p, const void* keys, tq_dtype dtype, int64_t G, int64_t N, void* packed,

@@ -92,6 +92,7 @@ struct tq_plan {
                       // bf16; then for decode 2^8 Pi^T hi/lo and (PROD) 2^8 S^T hi/lo, fp16
   uint32_t dec_ctab[16];  // decode: fp16 bits of hi (low half) and lo (high half) of 2^8 c_i
   int* err;           // device error word
+  uint64_t fingerprint;  // hash of d, bits, mode, kind and the bytes of Pi, S and the codebooks (packed-cache headers)
 };
 
 namespace tq {
