@@ -92,11 +92,11 @@ constexpr int kAttThreads = 608;        // 19 warps: producer, 2 issuers, 2 valu
 constexpr int kAttProducer = 0, kAttIssuer0 = 1, kAttValWarp0 = 3, kAttWgtWarp0 = 11;
 enum {
   AB_FULL = 0,
-  AB_EMPTY = AB_FULL + kAttStages,   // the tile's value warpgroup (128) + its weight warpgroup (128)
-  AB_PFULL = AB_EMPTY + kAttStages,  // [2] value planes of entry e in TMEM
-  AB_WFULL = AB_PFULL + 2,           // [2] weight image of entry e in shared memory
-  AB_MDONE = AB_WFULL + 2,           // [2] MMAs of entry e's tile complete
-  AB_DONE = AB_MDONE + 2,            // [2] all MMAs of issuer e complete
+  AB_EMPTY = AB_FULL + kAttStages,   // both value warpgroups (256) + the tile's weight warpgroup (128)
+  AB_PFULL = AB_EMPTY + kAttStages,  // [2] value planes of TMEM entry e (tile i: e = i % 2)
+  AB_WFULL = AB_PFULL + 2,           // [4] weight image slot i % 4 in shared memory
+  AB_MDONE = AB_WFULL + 4,           // [4] MMAs of tile i complete (slot i % 4)
+  AB_DONE = AB_MDONE + 4,            // [2] all MMAs of issuer e complete
   AB_COUNT = AB_DONE + 2
 };
 
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
   const uint32_t blk_bytes = (uint32_t)a.lay.block_bytes;
-  const uint32_t off_ring = 2 * kImg;
+  const uint32_t off_ring = 4 * kImg;
   const uint32_t off_bar = off_ring + kAttStages * blk_bytes;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -145,13 +145,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
     abort_flag = 0;
     for (int s = 0; s < kAttStages; ++s) {
       mbar_init(bar(AB_FULL + s), 1);
-      mbar_init(bar(AB_EMPTY + s), 256);
+      mbar_init(bar(AB_EMPTY + s), 384);
     }
     for (int e = 0; e < 2; ++e) {
-      mbar_init(bar(AB_PFULL + e), 128);
-      mbar_init(bar(AB_WFULL + e), 128);
-      mbar_init(bar(AB_MDONE + e), 1);
+      mbar_init(bar(AB_PFULL + e), 256);
       mbar_init(bar(AB_DONE + e), 1);
+    }
+    for (int k = 0; k < 4; ++k) {
+      mbar_init(bar(AB_WFULL + k), 128);
+      mbar_init(bar(AB_MDONE + k), 1);
     }
     fence_mbar_init();
   }
@@ -192,16 +194,18 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
   } else if (warp < kAttValWarp0) {
     // ------------------------------------------------------------ MMA issuers
     // issuer e takes the tiles i with i % 2 == e: value planes of TMEM entry e
-    // times weight image e, accumulated per parity plane into accumulator set e
+    // times weight image i % 4, accumulated per parity plane into accumulator
+    // set e; the commit for tile i lands on MDONE[i % 4]
     if (lane == 0) {
       const uint32_t e = (uint32_t)(warp - kAttIssuer0);
       constexpr uint32_t idesc = idesc_e4m3(128, N);
-      const uint64_t bdesc = sdesc_k_sw128(sb + e * kImg);
+      const uint64_t bdesc0 = sdesc_k_sw128(sb + e * kImg), bdesc1 = sdesc_k_sw128(sb + (e + 2) * kImg);
       const uint32_t d0 = tmem + e * kAcc, at0 = tmem + kSlot0 + e * kSlotCols;
       bool ok = true;
       uint32_t use = 0;
       for (uint32_t i = e; i < n_t; i += 2, ++use) {
-        if (!mbar_wait(bar(AB_PFULL + e), use & 1u, abort) || !mbar_wait(bar(AB_WFULL + e), use & 1u, abort)) {
+        const uint32_t k = i & 3u;  // e or e + 2
+        if (!mbar_wait(bar(AB_PFULL + e), use & 1u, abort) || !mbar_wait(bar(AB_WFULL + k), (i >> 2) & 1u, abort)) {
           ok = false;
           break;
         }
@@ -210,9 +214,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
         for (int T = 0; T < NT; ++T)
 #pragma unroll
           for (uint32_t kb = 0; kb < 4; ++kb)
-            mma_f8_ts(d0 + (uint32_t)(T * N), at0 + (uint32_t)(T * kPlaneCols) + 8u * kb, bdesc + 2u * kb, idesc,
+            mma_f8_ts(d0 + (uint32_t)(T * N), at0 + (uint32_t)(T * kPlaneCols) + 8u * kb,
+                      (k == e ? bdesc0 : bdesc1) + 2u * kb, idesc,
                       (use > 0 || kb > 0) ? 1u : 0u);
-        mma_commit(bar(AB_MDONE + e));
+        mma_commit(bar(AB_MDONE + k));
       }
       if (!ok) {
         *abort = 1;
@@ -224,17 +229,18 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
     }
   } else if (warp < kAttWgtWarp0) {
     // ------------------------------------------------------------ value planes
-    // value warpgroup e takes the tiles i with i % 2 == e (TMEM entry e);
-    // thread (warp w, lane l) owns coordinate j = 32 (w % 4) + l: its 16-byte
-    // chunk of each code plane holds the block's 128 tokens
-    const uint32_t e = (uint32_t)(warp - kAttValWarp0) >> 2;
+    // Both value warpgroups expand every tile, warpgroup v the parity planes
+    // T with T % 2 == v, into TMEM entry i % 2 (one warp moves only ~32 bytes
+    // per cycle to TMEM, so a tile's planes are spread over eight warps).
+    // Thread (warp w, lane l) owns coordinate j = 32 (w % 4) + l: its 16-byte
+    // chunk of each code plane holds the block's 128 tokens.
+    const uint32_t v = (uint32_t)(warp - kAttValWarp0) >> 2;
     const int quad = warp & 3;
     const int j = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + kSlot0;
     Ring slot;
-    slot.advance(e, kAttStages);
-    uint32_t use = 0;
-    for (uint32_t i = e; i < n_t; i += 2, ++use, slot.advance(2, kAttStages)) {
+    for (uint32_t i = 0; i < n_t; ++i, slot.advance(1, kAttStages)) {
+      const uint32_t e = i & 1u;  // TMEM entry of tile i
       if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(AB_FULL + slot.idx), slot.phase, abort))) {
         *abort = 1;
         atomicExch(a.err, 1);
@@ -248,7 +254,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
         w[3] = make_uint4(w[0].x ^ w[1].x ^ w[2].x, w[0].y ^ w[1].y ^ w[2].y, w[0].z ^ w[1].z ^ w[2].z,
                           w[0].w ^ w[1].w ^ w[2].w);
       mbar_arrive(bar(AB_EMPTY + slot.idx));
-      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(AB_MDONE + e), (use & 1u) ^ 1u, abort))) {
+      // TMEM entry e was last used by tile i - 2 (MDONE slot (i + 2) % 4; a
+      // fresh barrier's preceding phase for i < 2)
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(AB_MDONE + ((i + 2) & 3u)), (((i + 2) >> 2) & 1u) ^ 1u,
+                                                     abort))) {
         *abort = 1;
         atomicExch(a.err, 1);
         break;
@@ -257,6 +266,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
       const uint32_t taddr = lane_base + e * kSlotCols;
 #pragma unroll
       for (int T = 0; T < NT; ++T) {
+        if ((uint32_t)(T & 1) != v) continue;  // this warpgroup's planes
         uint32_t o[32];
         expand_word(w[T].x, o);
         expand_word(w[T].y, o + 8);
@@ -281,13 +291,54 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
 #pragma unroll
     for (int h = 0; h < HP; ++h) mh[h] = -INFINITY;
     const int64_t tok0 = t0 * kTokensPerBlock, tok1 = t1 * kTokensPerBlock < a.N ? t1 * kTokensPerBlock : a.N;
-    for (int64_t tok = tok0 + wt256; tok < tok1; tok += 256) {
+    // Four consecutive tokens per thread per pass, read as one float4 of each
+    // head's logits and two float4 of norm pairs, every load issued before the
+    // first use (the logits come from L2; dependent loads would serialise one
+    // round trip per token).  Rows whose length is not a multiple of four, and
+    // the ragged end, take single loads.
+    const bool vec = (a.N & 3) == 0;
+    for (int64_t tok = tok0 + 4 * (int64_t)wt256; tok < tok1; tok += 4 * 256) {
+      float l[HP][4], nv[4];
+      if (vec && tok + 4 <= tok1) {
 #pragma unroll
-      for (int h = 0; h < HP; ++h)
-        if (h < a.H) mh[h] = fmaxf(mh[h], sl2 * __ldg(a.logits + (g * a.H + h) * a.N + tok));
-      const int64_t r = tok - tok0;
-      nmax = fmaxf(nmax, __ldg(reinterpret_cast<const float*>(vblk0 + (r >> 7) * a.lay.block_bytes +
-                                                              a.lay.norms_off + (r & 127) * 8)));
+        for (int h = 0; h < HP; ++h) {
+          const float4 f = h < a.H ? __ldg(reinterpret_cast<const float4*>(a.logits + (g * a.H + h) * a.N + tok))
+                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          l[h][0] = f.x;
+          l[h][1] = f.y;
+          l[h][2] = f.z;
+          l[h][3] = f.w;
+        }
+        // tokens tok .. tok + 3 lie in one 128-token block (tok is a multiple of 4)
+        const int64_t r = tok - tok0;
+        const float4* np = reinterpret_cast<const float4*>(vblk0 + (r >> 7) * a.lay.block_bytes + a.lay.norms_off +
+                                                           (r & 127) * 8);
+        const float4 n01 = __ldg(np), n23 = __ldg(np + 1);
+        nv[0] = n01.x;
+        nv[1] = n01.z;
+        nv[2] = n23.x;
+        nv[3] = n23.z;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t t = tok + u;
+          const bool in = t < tok1;
+#pragma unroll
+          for (int h = 0; h < HP; ++h)
+            l[h][u] = (in && h < a.H) ? __ldg(a.logits + (g * a.H + h) * a.N + t) : -INFINITY;
+          const int64_t r = t - tok0;
+          nv[u] = in ? __ldg(reinterpret_cast<const float*>(vblk0 + (r >> 7) * a.lay.block_bytes +
+                                                            a.lay.norms_off + (r & 127) * 8))
+                     : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int h = 0; h < HP; ++h)
+          if (h < a.H && l[h][u] > -INFINITY) mh[h] = fmaxf(mh[h], sl2 * l[h][u]);
+        nmax = fmaxf(nmax, nv[u]);
+      }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
@@ -325,7 +376,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
     const int o_of_bit = tbit == 7 ? 7 : tbit >= 3 ? tbit - 3 : tbit + 4;  // inverse of c_src
     const int kk = 4 * (8 * tw + o_of_bit) + tbyte;
     const float comp = c_comp[o_of_bit & 3];
-    uint8_t* img = smem + (uint32_t)x * kImg;
+    // image slot i % 4 (x or x + 2): the image of tile i + 2 is written while
+    // the MMAs of tile i still read theirs
     float L[HP], P[HP];
 #pragma unroll
     for (int h = 0; h < HP; ++h) L[h] = P[h] = 0.f;
@@ -361,10 +413,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
         P[h] = fmaf(w, nv, P[h]);
         b[h] = w * bscale;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(AB_MDONE + (uint32_t)x), (use & 1u) ^ 1u, abort))) {
+      // image slot i % 4 was last read by the MMAs of tile i - 4
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(AB_MDONE + (i & 3u)), ((i >> 2) & 1u) ^ 1u, abort))) {
         ok = false;
         break;
       }
+      uint8_t* img = smem + (i & 3u) * kImg;
       // four e4m3 slices of each weight, two heads per conversion
 #pragma unroll
       for (int h = 0; h < HP; h += 2) {
@@ -385,7 +439,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
       }
       // the MMAs read the image through the async proxy
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(bar(AB_WFULL + (uint32_t)x));
+      mbar_arrive(bar(AB_WFULL + (i & 3u)));
 #pragma unroll
       for (int h = 0; h < HP; ++h) lc[h] = ln[h];
     }
@@ -433,8 +487,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
     for (int h = 0; h < HP; ++h) o_h[h] = a.px.c0 * s_P[h];
     int dummy = 0;
     for (uint32_t e = 0; e < 2 && e < n_t; ++e) {
-      const uint32_t uses = (n_t - e + 1) / 2;  // tiles of entry e
-      if (!mbar_wait(bar(AB_MDONE + e), (uses - 1) & 1u, &dummy)) atomicExch(a.err, 1);
+      const uint32_t last = e + 2 * ((n_t - 1 - e) / 2);  // the last tile of entry e
+      if (!mbar_wait(bar(AB_MDONE + (last & 3u)), (last >> 2) & 1u, &dummy)) atomicExch(a.err, 1);
     }
     tc_fence_after();
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
@@ -543,7 +597,7 @@ template <int HP, int KV>
 cudaError_t launch_att(const AttArgs& a, int64_t grid, cudaStream_t s) {
   constexpr int N = kSlices * HP;
   constexpr uint32_t kImg = ((uint32_t)N * 128u + 1023u) & ~1023u;
-  const size_t smem = 2 * kImg + kAttStages * (size_t)a.lay.block_bytes + AB_COUNT * 8 + 1024;
+  const size_t smem = 4 * kImg + kAttStages * (size_t)a.lay.block_bytes + AB_COUNT * 8 + 1024;
   auto kern = attend_values_kernel<HP, KV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
