@@ -31,17 +31,21 @@
 // any launch, share one at a time.
 // ||x|| comes from a pre-pass (key_norm_kernel) that writes it into the packed
 // block's norm slot.
-//  warp 0       producer: TMA loads into a 6-stage shared-memory ring; a stage
+//  warp 0       producer: TMA loads into a 3-stage shared-memory ring; a stage
 //               holds the B operand (hi and lo rows of 2^8 Pi or M for the
-//               job's 128 columns, 32 coordinates, 64-byte swizzle) and the A
+//               job's 128 columns, 64 coordinates, 128-byte swizzle) and the A
 //               source: the key tile (E2) or the residual tile from the scratch
-//               (E5, read by the MMA straight from shared memory).
+//               (E5, read by the MMA straight from shared memory).  Stages of
+//               64 coordinates carry 12 MMAs per commit: the issuing thread's
+//               commits and waits, not the tensor pipe, set the pace of a
+//               stage (~220 cycles per commit), so fewer, larger stages run
+//               faster.
 //  warp 1       TMEM owner (two partial accumulators in [0, 256), the E2 key
 //               operand ring in [256, 512)) and MMA issuer (one thread).
 //  warps 2-5    E2 key operand: thread (warp w, lane l) owns key row
-//               32 (w % 4) + l; per stage it reads its 32 coordinates from the
+//               32 (w % 4) + l; per stage it reads its 64 coordinates from the
 //               staged key tile and writes u = 2^8 x / ||x|| as fp16 hi, lo into
-//               TMEM (8-stage ring).
+//               TMEM (4-stage ring).
 //  warps 6-13   epilogue: two warpgroups, each taking half of a job's columns.
 // Every wait is bounded: on expiry the kernel raises the plan's error word,
 // drains what it issued and frees its TMEM.
@@ -58,15 +62,15 @@ using namespace ptx;
 
 constexpr int kEThreads = 448;
 constexpr int kEpiWarp0 = 6;       // warps 2-5 load the A operand
-constexpr int kStages = 6;         // shared-memory ring (B operand + A source)
-constexpr int kAStages = 8;        // TMEM ring of the E2 key operand
-constexpr uint32_t kPartBytes = 128 * 64;  // 128 rows x 32 16-bit values
-constexpr uint32_t kStageBytes = 4 * kPartBytes;  // B hi, B lo, A source (16 KB)
-constexpr int kStageK = 32;        // coordinates per stage
+constexpr int kStages = 3;         // shared-memory ring (B operand + A source)
+constexpr int kAStages = 4;        // TMEM ring of the E2 key operand
+constexpr uint32_t kPartBytes = 128 * 128;  // 128 rows x 64 16-bit values (one 128-byte swizzle row each)
+constexpr uint32_t kStageBytes = 4 * kPartBytes;  // B hi, B lo, A source (two parts): 64 KB
+constexpr int kStageK = 64;        // coordinates per stage
 constexpr int kARing = 256;        // first TMEM column of the A ring
-constexpr int kAPartCols = 16;     // TMEM columns of one A part per stage (32 16-bit values)
+constexpr int kAPartCols = 32;     // TMEM columns of one A part per stage (64 16-bit values)
 constexpr int kSliceCols = 128;    // output columns of a job (two partial accumulators of 128 columns)
-constexpr int kSliceStages = 4;    // stages (128 coordinates of K) per partial accumulator
+constexpr int kSliceStages = 2;    // stages (128 coordinates of K) per partial accumulator
 
 enum {
   BAR_FULL = 0,                       // B operand (and, for E5 stages, the residual tile) landed
@@ -100,10 +104,6 @@ __device__ __forceinline__ void raise(int* err, volatile int* abort) {
   atomicExch(err, 1);
 }
 
-__device__ __forceinline__ uint64_t sdesc_k_sw64(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(512u >> 4) << 32) | ((uint64_t)1 << 46) |
-         ((uint64_t)4 << 61);
-}
 
 __device__ __forceinline__ uint32_t smid() {
   uint32_t v;
@@ -212,7 +212,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       prefetch_tmap(&tmM);
       prefetch_tmap(&tmX);
       prefetch_tmap(&tmR);
-      constexpr uint32_t kXBytes = DT == 0 ? 2 * kPartBytes : kPartBytes;  // key tile: 128 rows x 32 values
+      constexpr uint32_t kXBytes = DT == 0 ? 2 * kPartBytes : kPartBytes;  // key tile: 128 rows x 64 values
       uint32_t b = 0, ph = 0, issued = 0;
       uint32_t xmask = 0, last_e2 = 0;  // per slot: parity of its next E2 fill; last fill was E2
       bool ok = true;
@@ -241,7 +241,10 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
             tma_load_2d(base + kPartBytes, map, st * kStageK, d + row0, bar(BAR_FULL + b));
             if (e2) {
               mbar_arrive_expect_tx(bar(BAR_XFULL + b), kXBytes);
+              // fp32 keys: two boxes of 32 values (128-byte rows); 16-bit keys: one of 64
               tma_load_2d(base + 2 * kPartBytes, &tmX, st * kStageK, xrow0, bar(BAR_XFULL + b));
+              if constexpr (DT == 0)
+                tma_load_2d(base + 3 * kPartBytes, &tmX, st * kStageK + 32, xrow0, bar(BAR_XFULL + b));
               xmask ^= 1u << b;
               last_e2 |= 1u << b;
             } else {
@@ -293,9 +296,13 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
               tc_fence_after();
               const uint32_t bq = sb + b * kStageBytes;
               const uint32_t at = tmem + kARing + s * (2 * kAPartCols);
+              // k steps of 16 values: 32 bytes within the 128-byte swizzle rows
+              // (descriptor address units of 16 bytes)
+              const uint64_t bh0 = sdesc_k_sw128(bq), bl0 = sdesc_k_sw128(bq + kPartBytes);
+              const uint64_t rh0 = sdesc_k_sw128(bq + 2 * kPartBytes), rl0 = sdesc_k_sw128(bq + 3 * kPartBytes);
 #pragma unroll
-              for (int ks = 0; ks < 2; ++ks) {
-                const uint64_t b_hi = sdesc_k_sw64(bq) + 2u * ks, b_lo = sdesc_k_sw64(bq + kPartBytes) + 2u * ks;
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t b_hi = bh0 + 2u * ks, b_lo = bl0 + 2u * ks;
                 const uint32_t acc = (st == 0 && ks == 0) ? 0u : 1u;
                 if (e2) {
                   const uint32_t a_hi = at + 8 * ks, a_lo = at + kAPartCols + 8 * ks;
@@ -303,8 +310,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
                   mma_f16_ts(d_acc, a_hi, b_lo, idesc, 1u);
                   mma_f16_ts(d_acc, a_lo, b_hi, idesc, 1u);
                 } else {
-                  const uint64_t r_hi = sdesc_k_sw64(bq + 2 * kPartBytes) + 2u * ks;
-                  const uint64_t r_lo = sdesc_k_sw64(bq + 3 * kPartBytes) + 2u * ks;
+                  const uint64_t r_hi = rh0 + 2u * ks, r_lo = rl0 + 2u * ks;
                   mma_f16_ss(d_acc, r_hi, b_hi, idesc, acc);
                   mma_f16_ss(d_acc, r_hi, b_lo, idesc, 1u);
                   mma_f16_ss(d_acc, r_lo, b_hi, idesc, 1u);
@@ -354,33 +360,39 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
         }
         tc_fence_after();
         const uint8_t* xs = smem + b * kStageBytes + 2 * kPartBytes;
-        uint32_t hi[16], lo[16];
-        if constexpr (DT == 0) {
-          // 128-byte rows, 16-byte chunk c at position c ^ (row % 8)
-          const uint8_t* xr = xs + row * 128;
+        const uint32_t col = t_lane + s * (2 * kAPartCols);
+        // 128-byte rows, 16-byte chunk c at position c ^ (row % 8); values in
+        // two halves of 32, each one 16-column TMEM store per part
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float4 f = *reinterpret_cast<const float4*>(xr + ((c ^ (row & 7)) << 4));
-            split_h2(f.x * inv, f.y * inv, hi[2 * c], lo[2 * c]);
-            split_h2(f.z * inv, f.w * inv, hi[2 * c + 1], lo[2 * c + 1]);
-          }
-        } else {
-          // 64-byte rows, 16-byte chunk c at position c ^ ((row / 2) % 4)
-          const uint8_t* xr = xs + row * 64;
+        for (int hv = 0; hv < 2; ++hv) {
+          uint32_t hi[16], lo[16];
+          if constexpr (DT == 0) {
+            // fp32: half hv is its own box of 32 values
+            const uint8_t* xr = xs + hv * kPartBytes + row * 128;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 w = *reinterpret_cast<const uint4*>(xr + ((c ^ ((row >> 1) & 3)) << 4));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int c = 0; c < 8; ++c) {
+              const float4 f = *reinterpret_cast<const float4*>(xr + ((c ^ (row & 7)) << 4));
+              split_h2(f.x * inv, f.y * inv, hi[2 * c], lo[2 * c]);
+              split_h2(f.z * inv, f.w * inv, hi[2 * c + 1], lo[2 * c + 1]);
+            }
+          } else {
+            // 16-bit: chunks 4 hv .. 4 hv + 3 of the row (8 values each)
+            const uint8_t* xr = xs + row * 128;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = key_pair<DT>(ws[e]);
-              split_h2(f.x * inv, f.y * inv, hi[4 * c + e], lo[4 * c + e]);
+            for (int cc = 0; cc < 4; ++cc) {
+              const int c = 4 * hv + cc;
+              const uint4 w = *reinterpret_cast<const uint4*>(xr + ((c ^ (row & 7)) << 4));
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = key_pair<DT>(ws[e]);
+                split_h2(f.x * inv, f.y * inv, hi[4 * cc + e], lo[4 * cc + e]);
+              }
             }
           }
+          tmem_st16(col + 16 * hv, hi);
+          tmem_st16(col + kAPartCols + 16 * hv, lo);
         }
-        const uint32_t col = t_lane + s * (2 * kAPartCols);
-        tmem_st16(col, hi);
-        tmem_st16(col + kAPartCols, lo);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(BAR_AFULL + s));
@@ -721,20 +733,21 @@ cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, 
   EncMaps mp;
   const uint32_t nc = (uint32_t)a.NC;
   cudaError_t e = make_tmap_2d(&mp.pi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pi, (uint64_t)d, 2 * (uint64_t)d,
-                               (uint64_t)d * 2, kStageK, nc, CU_TENSOR_MAP_SWIZZLE_64B);
+                               (uint64_t)d * 2, kStageK, nc, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e == cudaSuccess && p->lay.prod)
     e = make_tmap_2d(&mp.m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, m, (uint64_t)d, 2 * (uint64_t)d, (uint64_t)d * 2, kStageK,
-                     nc, CU_TENSOR_MAP_SWIZZLE_64B);
+                     nc, CU_TENSOR_MAP_SWIZZLE_128B);
   else if (e == cudaSuccess)
     mp.m = mp.pi;  // an MSE plan holds no M; its encode has no E5 and never reads this map
-  // key tiles: 128 rows x 32 values (rows past G N read as zero)
+  // key tiles: 128 rows x 64 values, in boxes of 128-byte rows (two per stage
+  // for fp32 keys); rows past G N read as zero
   if (e == cudaSuccess) {
     const CUtensorMapDataType xt = dt == TQ_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : dt == TQ_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t es = dt == TQ_F32 ? 4 : 2;
-    e = make_tmap_2d(&mp.x, xt, keys, (uint64_t)d, (uint64_t)(G * N), (uint64_t)d * es, kStageK, kTokensPerBlock,
-                     dt == TQ_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    e = make_tmap_2d(&mp.x, xt, keys, (uint64_t)d, (uint64_t)(G * N), (uint64_t)d * es,
+                     dt == TQ_F32 ? kStageK / 2 : kStageK, kTokensPerBlock, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   // residual rows of the per-SM scratch: [slot][hi, lo][128][d] fp16 (Prod; an
   // MSE encode has no E5 and never reads this map)
@@ -742,7 +755,7 @@ cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, 
     if (p->lay.prod)
       e = make_tmap_2d(&mp.r, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p->wide_scratch, (uint64_t)d,
                        (uint64_t)p->wide_slots * 256, (uint64_t)d * 2, kStageK, kTokensPerBlock,
-                       CU_TENSOR_MAP_SWIZZLE_64B);
+                       CU_TENSOR_MAP_SWIZZLE_128B);
     else
       mp.r = mp.pi;
   }
