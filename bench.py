@@ -568,9 +568,11 @@ def run_ours(args, world, rank):
                 "score_speedup_vs_fp32_keys": round(bms / sc_cold_ms, 3)}
         del keys32, base_l
 
-    # decode of every key (not part of the step), cold L2, where it runs on tensor cores
+    # decode of every key (not part of the step), cold L2, on the tensor-core decode
+    # of the plan's d (tensor_d128 or tensor_wide)
     dec = None
-    if plan.decode_path() == "tensor_d128" and d * G * N * 4 < 40e9:
+    dpath = plan.decode_path()
+    if dpath in kernels and d * G * N * 4 < 40e9:
         xh = torch.empty(G, N, d, dtype=torch.float32, device=dev)
         dt = []
         for _ in range(max(3, args.steps)):
@@ -587,7 +589,8 @@ def run_ours(args, world, rank):
         # algorithmic bytes: the packed keys in, fp32 rows out; flops: one d x d
         # product per key, two in Prod
         dec = {"ms": round(dms, 5), "vectors_per_s": G * N / (dms * 1e-3),
-               "roofline": roof(P + G * N * d * 4, dms, "decode_tc", "k_decode_tc.cu",
+               "roofline": roof(P + G * N * d * 4, dms, kernels[dpath][0].format("decode"),
+                                kernels[dpath][1].format("decode"),
                                 flops=(2 if plan.mode == "prod" else 1) * 2 * d * d * G * N)}
         del xh
 

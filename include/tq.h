@@ -282,7 +282,9 @@ tq_status tq_attend(const tq_plan* kplan, const tq_plan* vplan, const float* que
 
 /* Reconstruct keys ([PT-KR] usage listing: ``tq.decompress``):
  * x_hat = n Pi^T c[idx] + rho sqrt(pi/2)/m S^T (2z - 1)  (TQ_MSE: first term),
- * so that <q, x_hat> equals tq_score's logit.  out: device fp32 [G][N][d]. */
+ * so that <q, x_hat> equals tq_score's logit.  out: device fp32 [G][N][d].
+ * Runs on tensor cores at every d (tq_decode_path).  Errors: TQ_EINVAL,
+ * TQ_EALIGN, TQ_ECUDA. */
 tq_status tq_decode(const tq_plan* plan, const void* packed, int64_t n_groups, int64_t n_tokens,
                     float* out, void* stream);
 
@@ -331,9 +333,10 @@ int tq_format_version(void);
  *                        keys, either mode; score: H <= 16, odd-symmetric
  *                        codebook, k <= 3);
  *   TQ_PATH_TENSOR_WIDE  tcgen05 kernels for any d (multiple of 128): encode of
- *                        every other plan and key dtype, score up to 256 heads;
- *   TQ_PATH_CUDA_CORE    CUDA-core kernels: decode for d > 128.
- * tq_decode takes a tcgen05 kernel at d = 128 (either mode).
+ *                        every other plan and key dtype, score up to 256 heads,
+ *                        decode for d > 128;
+ *   TQ_PATH_CUDA_CORE    CUDA-core kernels (no current path takes one; the value
+ *                        stays reserved).
  * Returns the path, or TQ_EINVAL for a null plan or an out-of-range argument
  * (TQ_EUNSUPPORTED if no kernel takes the shape; none of the shapes the entry
  * points accept). */

@@ -156,14 +156,19 @@ def test_score_top_k(cuda, d, G, N, H, k):
     (128, 2, 300, 3, "prod"), (256, 1, 129, 4, "prod"), (128, 1, 200, 2, "mse"),
     # the d = 128 tensor-core decode: one key, several tiles per CTA (both
     # modes, 16 levels), 1-bit codes over a ragged tail
-    (128, 1, 1, 2, "prod"), (128, 1, 40000, 4, "prod"), (128, 2, 20000, 4, "mse"), (128, 3, 129, 1, "mse")])
+    (128, 1, 1, 2, "prod"), (128, 1, 40000, 4, "prod"), (128, 2, 20000, 4, "mse"), (128, 3, 129, 1, "mse"),
+    # the wide tensor-core decode: every code width of both modes (register
+    # levels for k <= 2, the pair table for k >= 3), the vector-search d, a
+    # ragged tail and several tiles per CTA
+    (256, 2, 300, 2, "prod"), (384, 1, 77, 3, "prod"), (256, 1, 130, 1, "mse"), (512, 1, 260, 3, "mse"),
+    (256, 1, 129, 4, "mse"), (1536, 1, 200, 4, "prod"), (256, 1, 40000, 3, "prod")])
 def test_decode_matches_oracle(cuda, d, G, N, bits, mode):
     w, inp = _case_inputs(d, G, N, torch.float32, bits, mode, False, seed=41)
     keys = tq_synth.keys(w)
     buf, e = oracle_encode(inp, keys)
     want = o.decode_packed(buf, inp.Pi_o, inp.S_o, inp.c_o, d, bits, mode, G, N)
     plan = inp.plan()
-    assert plan.decode_path() == ("tensor_d128" if d == 128 else "cuda_core")
+    assert plan.decode_path() == ("tensor_d128" if d == 128 else "tensor_wide")
     got = tq.tq_decode(plan, torch.from_numpy(buf.copy()).to(cuda), G, N)
     torch.cuda.synchronize()
     assert plan.status() == 0

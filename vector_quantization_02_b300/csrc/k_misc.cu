@@ -34,69 +34,6 @@ __global__ void transpose_kernel(const float* __restrict__ A, int d, float* __re
   for (int i = threadIdx.y; i < 32; i += blockDim.y) AT[(int64_t)(yo0 + i) * d + xo] = tile[threadIdx.x][i];
 }
 
-// Decode: out_j = n sum_i Pi[i][j] c[idx_i] + rho kappa sum_i S[i][j] (2 z_i - 1).
-// KB keys per CTA pass; thread j owns output coordinate j (Pi rows read coalesced).
-template <int KB>
-__global__ void __launch_bounds__(256)
-decode_simt_kernel(const uint8_t* __restrict__ packed, int64_t G, int64_t N, Layout lay, CodeParams cp,
-                   float kappa, const float* __restrict__ Pi, const float* __restrict__ S,
-                   float* __restrict__ out) {
-  extern __shared__ float sm[];
-  const int d = lay.d;
-  float* Yt = sm;              // [KB][d] centroid values
-  float* Sg = sm + KB * d;     // [KB][d] +-1
-  __shared__ float s_n[KB], s_r[KB];
-  const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
-  const int tiles_per_block = kTokensPerBlock / KB;
-  const int64_t n_tiles = G * nb * tiles_per_block;
-  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const int64_t gb = tile / tiles_per_block;
-    const int64_t g = gb / nb, blk = gb % nb;
-    const int t0 = (int)(tile % tiles_per_block) * KB;
-    const uint8_t* in = packed + gb * lay.block_bytes;
-    __syncthreads();
-    for (int i = threadIdx.x; i < KB * d; i += blockDim.x) {
-      const int kk = i / d, j = i - kk * d;
-      const int c = j / kChunk, wd = (j % kChunk) / 32, b = j % 32;
-      int idx = 0;
-      for (int p = 0; p < lay.k; ++p) {
-        unsigned w = *reinterpret_cast<const unsigned*>(in + lay.plane_off(p, c, t0 + kk) + 4 * wd);
-        idx |= ((w >> b) & 1u) << p;
-      }
-      Yt[i] = cp.c[idx];
-      if (lay.prod) {
-        unsigned w = *reinterpret_cast<const unsigned*>(in + lay.plane_off(lay.k, c, t0 + kk) + 4 * wd);
-        Sg[i] = ((w >> b) & 1u) ? 1.f : -1.f;
-      }
-    }
-    if (threadIdx.x < KB) {
-      float2 nr = *reinterpret_cast<const float2*>(in + lay.norms_off + (int64_t)(t0 + threadIdx.x) * 8);
-      s_n[threadIdx.x] = nr.x;
-      s_r[threadIdx.x] = nr.y * kappa;
-    }
-    __syncthreads();
-    for (int j = threadIdx.x; j < d; j += blockDim.x) {
-      float a[KB], b[KB];
-#pragma unroll
-      for (int kk = 0; kk < KB; ++kk) a[kk] = b[kk] = 0.f;
-      for (int i = 0; i < d; ++i) {
-        const float pij = __ldg(Pi + (int64_t)i * d + j);
-        const float sij = lay.prod ? __ldg(S + (int64_t)i * d + j) : 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KB; ++kk) {
-          a[kk] = fmaf(pij, Yt[kk * d + i], a[kk]);
-          if (lay.prod) b[kk] = fmaf(sij, Sg[kk * d + i], b[kk]);
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < KB; ++kk) {
-        const int64_t tok = blk * kTokensPerBlock + t0 + kk;
-        if (tok < N) out[(g * N + tok) * d + j] = s_n[kk] * a[kk] + (lay.prod ? s_r[kk] * b[kk] : 0.f);
-      }
-    }
-  }
-}
-
 // fp32 baseline: a CTA stages KT keys of one group in shared memory (coalesced),
 // then thread (key, head) computes the dot product; the key row is read with a
 // rotated start so that a warp's 32 keys hit 32 banks.
@@ -125,24 +62,6 @@ score_fp32_kernel(const float* __restrict__ q, const float* __restrict__ x, int6
     }
     logits[(g * H + h) * N + tok0 + k] = acc;
   }
-}
-
-template <int KB>
-cudaError_t launch_decode_kb(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
-                             cudaStream_t s) {
-  const size_t smem = (size_t)2 * KB * p->d * sizeof(float);
-  auto kern = decode_simt_kernel<KB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t nb = (N + kTokensPerBlock - 1) / kTokensPerBlock;
-  const int64_t tiles = G * nb * (kTokensPerBlock / KB);
-  int64_t grid = (int64_t)sms * 2;
-  if (grid > tiles) grid = tiles;
-  kern<<<(unsigned)grid, 256, smem, s>>>(packed, G, N, p->lay, p->cp, p->kappa, p->Pi, p->S, out);
-  return cudaGetLastError();
 }
 
 // Streaming form for d % 4 == 0, d <= 1024: thread t of a block owns key t of
@@ -405,14 +324,6 @@ cudaError_t launch_plan_derive(tq_plan* p, cudaStream_t s) {
     abt_f64_kernel<<<g16, b16, 0, s>>>(p->S, p->Pi, d, p->M, p->MT);
   }
   return cudaGetLastError();
-}
-
-cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
-                               cudaStream_t s) {
-  if (G * N == 0) return cudaSuccess;
-  if (p->lay.frac) return cudaErrorNotSupported;  // fractional widths decode on the d = 128 tensor-core path
-  if (p->d <= 128) return launch_decode_kb<16>(p, packed, G, N, out, s);
-  return launch_decode_kb<8>(p, packed, G, N, out, s);
 }
 
 template <int KT>

@@ -32,6 +32,7 @@ void free_plan(tq_plan* p) {
   if (p->err) cudaFree(p->err);
   if (p->tc_ops) cudaFree(p->tc_ops);
   if (p->wide_ops) cudaFree(p->wide_ops);
+  if (p->dec_wide_ops) cudaFree(p->dec_wide_ops);
   if (p->wide_scratch) cudaFree(p->wide_scratch);
   delete p;
 }
@@ -92,7 +93,41 @@ cudaError_t build_wide_ops(tq_plan* p) {
   }
   e = cudaMalloc(&p->wide_ops, host.size() * 2);
   if (e == cudaSuccess) e = cudaMemcpy(p->wide_ops, host.data(), host.size() * 2, cudaMemcpyHostToDevice);
-  if (e != cudaSuccess || !p->lay.prod) return e;  // an MSE encode needs no residual scratch
+  if (e != cudaSuccess) return e;
+  if (p->d > 128) {
+    // the tensor-core decode of larger d: 2^8 Pi^T and (Prod) 2^8 S^T, split
+    // hi + lo in fp16 (row j holds column j of Pi and of S), and the split
+    // levels 2^8 c_i
+    std::vector<float> S(p->lay.prod ? dd : 0);
+    if (p->lay.prod) e = cudaMemcpy(S.data(), p->S, dd * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return e;
+    const size_t d = (size_t)p->d;
+    std::vector<uint16_t> dh((p->lay.prod ? 4 : 2) * dd);
+    auto split_to = [&](float v, size_t hi_at, size_t lo_at) {
+      const __half h = __float2half_rn(v);
+      const __half l = __float2half_rn(v - __half2float(h));
+      std::memcpy(&dh[hi_at], &h, 2);
+      std::memcpy(&dh[lo_at], &l, 2);
+    };
+    for (size_t j = 0; j < d; ++j)
+      for (size_t i = 0; i < d; ++i) {
+        split_to(256.f * Pi[i * d + j], j * d + i, dd + j * d + i);
+        if (p->lay.prod) split_to(256.f * S[i * d + j], 2 * dd + j * d + i, 3 * dd + j * d + i);
+      }
+    e = cudaMalloc(&p->dec_wide_ops, dh.size() * 2);
+    if (e == cudaSuccess) e = cudaMemcpy(p->dec_wide_ops, dh.data(), dh.size() * 2, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < 16; ++i) {
+      const float v = i < p->cp.L ? 256.f * p->cp.c[i] : 0.f;
+      const __half h = __float2half_rn(v);
+      const __half l = __float2half_rn(v - __half2float(h));
+      uint16_t hb, lb;
+      std::memcpy(&hb, &h, 2);
+      std::memcpy(&lb, &l, 2);
+      p->dec_ctab[i] = (uint32_t)hb | ((uint32_t)lb << 16);
+    }
+  }
+  if (!p->lay.prod) return e;  // an MSE encode needs no residual scratch
   int slots = tq::query_nsmid();
   if (slots <= 0) return cudaErrorUnknown;
   p->wide_slots = slots;
@@ -275,7 +310,9 @@ int tq_score_path(const tq_plan* p, int H) {
 
 int tq_decode_path(const tq_plan* p) {
   if (!p) return TQ_EINVAL;
-  return tq::decode_tc_supported(p) ? TQ_PATH_TENSOR_D128 : TQ_PATH_CUDA_CORE;
+  return tq::decode_tc_supported(p)     ? TQ_PATH_TENSOR_D128
+         : tq::decode_wide_supported(p) ? TQ_PATH_TENSOR_WIDE
+                                        : TQ_EUNSUPPORTED;
 }
 
 int tq_encode_path(const tq_plan* p, tq_dtype dt) {
@@ -726,7 +763,9 @@ tq_status tq_decode(const tq_plan* p, const void* packed, int64_t G, int64_t N, 
   if (!aligned16(packed) || !aligned16(out)) return TQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (decode_tc_supported(p)) return from_cuda(launch_decode_tc(p, static_cast<const uint8_t*>(packed), G, N, out, s));
-  return from_cuda(launch_decode_simt(p, static_cast<const uint8_t*>(packed), G, N, out, s));
+  if (decode_wide_supported(p))
+    return from_cuda(launch_decode_wide(p, static_cast<const uint8_t*>(packed), G, N, out, s));
+  return TQ_EUNSUPPORTED;  // every plan the library creates takes one of the two
 }
 
 tq_status tq_score_fp32(const float* queries, const float* keys, int64_t G, int H, int64_t N, int d, float* logits,

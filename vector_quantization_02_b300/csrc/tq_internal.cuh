@@ -85,6 +85,7 @@ struct tq_plan {
   float* M;           // [d][d] = S Pi^T (PROD)
   float* MT;          // [d][d] = M^T (PROD)
   uint16_t* wide_ops;  // row-major fp16 [4][d][d]: (2^8 Pi) hi, lo; (PROD) M hi, lo
+  uint16_t* dec_wide_ops;  // d > 128: row-major fp16 [4][d][d]: (2^8 Pi^T) hi, lo; (PROD) (2^8 S^T) hi, lo
   void* wide_scratch;  // (PROD) residual rows of the wide encode: [wide_slots][2][128][d] bf16
   int wide_slots;      // SM ids of the device (%nsmid)
   uint8_t* tc_ops;    // tensor-core operand images (d = 128), 32 KB each, K-major
@@ -105,9 +106,10 @@ cudaError_t launch_encode_tc(const tq_plan* p, const void* keys, tq_dtype dt, in
                              cudaStream_t s, bool drop_first = false);
 cudaError_t launch_topk(const float* logits, int64_t rows, int64_t N, int k, float* top_scores,
                         int64_t* top_idx, void* ws, cudaStream_t s);
-cudaError_t launch_decode_simt(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
-                               cudaStream_t s);
 bool decode_tc_supported(const tq_plan* p);
+bool decode_wide_supported(const tq_plan* p);
+cudaError_t launch_decode_wide(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
+                               cudaStream_t s);
 cudaError_t launch_decode_tc(const tq_plan* p, const uint8_t* packed, int64_t G, int64_t N, float* out,
                              cudaStream_t s);
 // index of decode image j in tc_ops (0, 1: Pi^T hi, lo; 2, 3: S^T hi, lo)
