@@ -161,7 +161,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       for (int64_t i = 0; i < n_my; ++i) {
         const int s = (int)(i % kStages);
         const uint32_t use = (uint32_t)(i / kStages);
-        if (!mbar_wait(bar(BAR_XEMPTY + s), (use & 1) ^ 1, abort)) {
+        if (!mbar_wait_suspend(bar(BAR_XEMPTY + s), (use & 1) ^ 1, abort)) {
           raise(a.err, abort);
           break;
         }
@@ -197,15 +197,15 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
                      dpil = sdesc_k_sw128(sb + kOffPiLo), dmh = sdesc_k_sw128(sb + kOffMHi),
                      dml = sdesc_k_sw128(sb + kOffMLo);
       const int64_t n_iss = (PROD || e2) ? n_my : 0;  // MSE has no E5
-      bool ok = mbar_wait(bar(BAR_OPS), 0, abort);
+      bool ok = mbar_wait_suspend(bar(BAR_OPS), 0, abort);
       for (int64_t i = 0; ok && i < n_iss; ++i) {
         const int b = (int)(i & 1);
         const uint32_t j = (uint32_t)(i >> 1);
         if (e2) {
           // E2: Y = X Pi^T, Pi split hi + lo
           const int s = (int)(i % kStages);
-          if (!mbar_wait(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort) ||
-              !mbar_wait(bar(BAR_ACCEMPTY + b), (j & 1) ^ 1, abort)) {
+          if (!mbar_wait_suspend(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort) ||
+              !mbar_wait_suspend(bar(BAR_ACCEMPTY + b), (j & 1) ^ 1, abort)) {
             ok = false;
             break;
           }
@@ -228,7 +228,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
             if ((kb & 3) == 0) {
-              if (!mbar_wait(bar(BAR_RFULL + 2 * b + (kb >> 2)), j & 1, abort)) {
+              if (!mbar_wait_suspend(bar(BAR_RFULL + 2 * b + (kb >> 2)), j & 1, abort)) {
                 ok = false;
                 break;
               }
@@ -267,7 +267,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       // E1: ||x|| from the staged key row (two 128-byte-swizzled K halves)
       // every lane polls; the warp proceeds (or gives up) as one, because the
       // tcgen05 loads and stores below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort))) {
         raise(a.err, abort);
         break;
       }
@@ -320,7 +320,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
 
       // E2 result -> E3 codes, E4 residual; the residual's bf16 split goes back
       // into the same TMEM columns as the A operand of E5
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_YFULL + wg), j & 1, abort))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_YFULL + wg), j & 1, abort))) {
         raise(a.err, abort);
         break;
       }
@@ -429,7 +429,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
       uint32_t zs[4] = {0u, 0u, 0u, 0u};
       if constexpr (PROD) {
         // E5 result -> sign plane
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PFULL + wg), j & 1, abort))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_PFULL + wg), j & 1, abort))) {
           raise(a.err, abort);
           break;
         }
