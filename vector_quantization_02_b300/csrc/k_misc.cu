@@ -1,4 +1,4 @@
-// Plan derivation, decode, and the uncompressed fp32 baseline.
+// Plan derivation, the uncompressed fp32 baseline, and the bounded-wait self-test.
 #include "ptx_sm100.cuh"
 #include "tq_internal.cuh"
 
