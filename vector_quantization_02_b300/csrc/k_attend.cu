@@ -195,8 +195,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
     // ------------------------------------------------------------ MMA issuers
     // issuer e takes the tiles i with i % 2 == e: value planes of TMEM entry e
     // times weight image i % 4, accumulated per parity plane into accumulator
-    // set e; the commit for tile i lands on MDONE[i % 4]
-    if (lane == 0) {
+    // set e; the commit for tile i lands on MDONE[i % 4].  The whole warp runs
+    // the loop (its operands stay warp-uniform); one elected lane issues each
+    // MMA and commit.
+    {
       const uint32_t e = (uint32_t)(warp - kAttIssuer0);
       constexpr uint32_t idesc = idesc_e4m3(128, N);
       const uint64_t bdesc0 = sdesc_k_sw128(sb + e * kImg), bdesc1 = sdesc_k_sw128(sb + (e + 2) * kImg);
@@ -205,7 +207,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
       uint32_t use = 0;
       for (uint32_t i = e; i < n_t; i += 2, ++use) {
         const uint32_t k = i & 3u;  // e or e + 2
-        if (!mbar_wait(bar(AB_PFULL + e), use & 1u, abort) || !mbar_wait(bar(AB_WFULL + k), (i >> 2) & 1u, abort)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(AB_PFULL + e), use & 1u, abort) &&
+                                         mbar_wait(bar(AB_WFULL + k), (i >> 2) & 1u, abort))) {
           ok = false;
           break;
         }
@@ -214,16 +217,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_values_kernel(const Att
         for (int T = 0; T < NT; ++T)
 #pragma unroll
           for (uint32_t kb = 0; kb < 4; ++kb)
-            mma_f8_ts(d0 + (uint32_t)(T * N), at0 + (uint32_t)(T * kPlaneCols) + 8u * kb,
+            mma_f8_ts_w(d0 + (uint32_t)(T * N), at0 + (uint32_t)(T * kPlaneCols) + 8u * kb,
                       (k == e ? bdesc0 : bdesc1) + 2u * kb, idesc,
                       (use > 0 || kb > 0) ? 1u : 0u);
-        mma_commit(bar(AB_MDONE + k));
+        mma_commit_w(bar(AB_MDONE + k));
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         *abort = 1;
         atomicExch(a.err, 1);
       }
-      mma_commit(bar(AB_DONE + e));
+      mma_commit_w(bar(AB_DONE + e));
       int dummy = 0;
       mbar_wait(bar(AB_DONE + e), 0, &dummy);
     }

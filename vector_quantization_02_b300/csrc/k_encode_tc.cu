@@ -17,10 +17,11 @@
 // Work per CTA (persistent, one CTA per SM, 128 keys = one packed block per tile):
 //  warp 0      TMA producer: key tiles (K-major, 128-byte swizzle) into a
 //              2-stage ring; once, the swizzled images of Pi_hi/lo and M_hi/lo.
-//  warp 1      TMEM owner (512 columns) and E2 issuer (one thread);
-//  warp 10     E5 issuer (one thread).  Two issuers, because a single thread
-//              issues one tcgen05.mma only every ~50-80 cycles and E5 of tile i
-//              must not wait behind E2 of tile i + 1.
+//  warp 1      TMEM owner (512 columns) and E2 issuer;
+//  warp 10     E5 issuer.  Two issuers, because one issuing warp puts out a
+//              tcgen05.mma only every ~50-80 cycles and E5 of tile i must not
+//              wait behind E2 of tile i + 1.  Each issuer warp runs its loop
+//              converged and one elected lane issues.
 //  warps 2-9   two epilogue warpgroups; tile i goes to warpgroup i % 2, which
 //              owns TMEM columns [256 b, 256 b + 256): Y/R in the first 128
 //              (the bf16 residual split is written back over the Y columns it
@@ -186,7 +187,9 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
     }
   } else if (warp == 1 || warp == kE5Warp) {
     // ------------------------------------------------------------ MMA issuers
-    if (lane == 0) {
+    // The whole warp runs the loop (its operands stay warp-uniform); one
+    // elected lane issues each MMA and commit.
+    {
       constexpr uint32_t idesc_x = idesc_f16(kBF16 ? 1u : 0u, 128, 128);
       constexpr uint32_t idesc_r = idesc_f16(1u, 128, 128);
       const bool e2 = warp == 1;
@@ -197,15 +200,15 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
                      dpil = sdesc_k_sw128(sb + kOffPiLo), dmh = sdesc_k_sw128(sb + kOffMHi),
                      dml = sdesc_k_sw128(sb + kOffMLo);
       const int64_t n_iss = (PROD || e2) ? n_my : 0;  // MSE has no E5
-      bool ok = mbar_wait_suspend(bar(BAR_OPS), 0, abort);
+      bool ok = __all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_OPS), 0, abort));
       for (int64_t i = 0; ok && i < n_iss; ++i) {
         const int b = (int)(i & 1);
         const uint32_t j = (uint32_t)(i >> 1);
         if (e2) {
           // E2: Y = X Pi^T, Pi split hi + lo
           const int s = (int)(i % kStages);
-          if (!mbar_wait_suspend(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort) ||
-              !mbar_wait_suspend(bar(BAR_ACCEMPTY + b), (j & 1) ^ 1, abort)) {
+          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_XFULL + s), (uint32_t)(i / kStages) & 1, abort) &&
+                                           mbar_wait_suspend(bar(BAR_ACCEMPTY + b), (j & 1) ^ 1, abort))) {
             ok = false;
             break;
           }
@@ -215,11 +218,11 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
             const uint32_t off16 = ((kb >> 2) * kAtomBytes + (kb & 3) * 32) >> 4;
-            mma_f16_ss(d, dx + off16, dpih + off16, idesc_x, kb > 0);
-            if (!a.e2_single) mma_f16_ss(d, dx + off16, dpil + off16, idesc_x, 1);
+            mma_f16_ss_w(d, dx + off16, dpih + off16, idesc_x, kb > 0);
+            if (!a.e2_single) mma_f16_ss_w(d, dx + off16, dpil + off16, idesc_x, 1);
           }
-          mma_commit(bar(BAR_YFULL + b));
-          mma_commit(bar(BAR_XEMPTY + s));
+          mma_commit_w(bar(BAR_YFULL + b));
+          mma_commit_w(bar(BAR_XEMPTY + s));
         } else {
           // E5: P = R' M^T with R' = R_hi + R_lo and M = M_hi + M_lo (bf16), R_lo M_lo dropped;
           // the first 64 coordinates' MMAs start while the epilogue still
@@ -228,7 +231,7 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
             if ((kb & 3) == 0) {
-              if (!mbar_wait_suspend(bar(BAR_RFULL + 2 * b + (kb >> 2)), j & 1, abort)) {
+              if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_RFULL + 2 * b + (kb >> 2)), j & 1, abort))) {
                 ok = false;
                 break;
               }
@@ -236,18 +239,18 @@ encode_tc_kernel(const __grid_constant__ CUtensorMap tmX, const EncTcArgs a) {
             }
             const uint32_t off16 = ((kb >> 2) * kAtomBytes + (kb & 3) * 32) >> 4;
             const uint32_t a_hi = r + 32 * (kb >> 1) + 8 * (kb & 1), a_lo = a_hi + 16;
-            mma_f16_ts(d, a_hi, dmh + off16, idesc_r, kb > 0);
-            mma_f16_ts(d, a_hi, dml + off16, idesc_r, 1);
-            mma_f16_ts(d, a_lo, dmh + off16, idesc_r, 1);
+            mma_f16_ts_w(d, a_hi, dmh + off16, idesc_r, kb > 0);
+            mma_f16_ts_w(d, a_hi, dml + off16, idesc_r, 1);
+            mma_f16_ts_w(d, a_lo, dmh + off16, idesc_r, 1);
           }
           if (!ok) break;
-          mma_commit(bar(BAR_PFULL + b));
+          mma_commit_w(bar(BAR_PFULL + b));
         }
       }
-      if (!ok) raise(a.err, abort);
+      if (!ok && lane == 0) raise(a.err, abort);
       // all issued MMAs complete before TMEM is freed
       const int done = e2 ? BAR_DONE : BAR_DONE5;
-      mma_commit(bar(done));
+      mma_commit_w(bar(done));
       int dummy = 0;
       mbar_wait(bar(done), 0, &dummy);
     }

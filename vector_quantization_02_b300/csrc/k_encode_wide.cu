@@ -41,7 +41,8 @@
 //               stage (~220 cycles per commit), so fewer, larger stages run
 //               faster.
 //  warp 1       TMEM owner (two partial accumulators in [0, 256), the E2 key
-//               operand ring in [256, 512)) and MMA issuer (one thread).
+//               operand ring in [256, 512)) and MMA issuer (the warp runs
+//               the loop converged, one elected lane issues).
 //  warps 2-5    E2 key operand: thread (warp w, lane l) owns key row
 //               32 (w % 4) + l; per stage it reads its 64 coordinates from the
 //               staged key tile and writes u = 2^8 x / ||x|| as fp16 hi, lo into
@@ -63,22 +64,20 @@ using namespace ptx;
 constexpr int kEThreads = 448;
 constexpr int kEpiWarp0 = 6;       // warps 2-5 load the A operand
 constexpr int kStages = 3;         // shared-memory ring (B operand + A source)
-constexpr int kAStages = 4;        // TMEM ring of the E2 key operand
 constexpr uint32_t kPartBytes = 128 * 128;  // 128 rows x 64 16-bit values (one 128-byte swizzle row each)
 constexpr uint32_t kStageBytes = 4 * kPartBytes;  // B hi, B lo, A source (two parts): 64 KB
 constexpr int kStageK = 64;        // coordinates per stage
-constexpr int kARing = 256;        // first TMEM column of the A ring
+constexpr int kARing = 256;        // first TMEM column of the E2 key operand, one slot per ring stage
 constexpr int kAPartCols = 32;     // TMEM columns of one A part per stage (64 16-bit values)
 constexpr int kSliceCols = 128;    // output columns of a job (two partial accumulators of 128 columns)
 constexpr int kSliceStages = 2;    // stages (128 coordinates of K) per partial accumulator
 
 enum {
-  BAR_FULL = 0,                       // B operand (and, for E5 stages, the residual tile) landed
-  BAR_XFULL = BAR_FULL + kStages,     // key tile of an E2 stage landed (only E2 fills advance it)
+  BAR_FULL = 0,                       // E5 stage landed: B operand and residual tile (only E5 fills advance it)
+  BAR_XFULL = BAR_FULL + kStages,     // E2 stage landed: B operand and key tile (only E2 fills advance it)
   BAR_EMPTY = BAR_XFULL + kStages,
-  BAR_AFULL = BAR_EMPTY + kStages,
-  BAR_AEMPTY = BAR_AFULL + kAStages,
-  BAR_DFULL = BAR_AEMPTY + kAStages,   // [2] partial accumulators
+  BAR_AFULL = BAR_EMPTY + kStages,    // E2 key operand of the stage written to TMEM
+  BAR_DFULL = BAR_AFULL + kStages,    // [2] partial accumulators
   BAR_DEMPTY = BAR_DFULL + 2,
   BAR_RREADY = BAR_DEMPTY + 2,
   BAR_RHO = BAR_RREADY + 1,
@@ -170,10 +169,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       mbar_init(bar(BAR_FULL + s), 1);
       mbar_init(bar(BAR_XFULL + s), 1);
       mbar_init(bar(BAR_EMPTY + s), 1);
-    }
-    for (int s = 0; s < kAStages; ++s) {
       mbar_init(bar(BAR_AFULL + s), 128);
-      mbar_init(bar(BAR_AEMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(BAR_DFULL + b), 1);
@@ -214,7 +210,8 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       prefetch_tmap(&tmR);
       constexpr uint32_t kXBytes = DT == 0 ? 2 * kPartBytes : kPartBytes;  // key tile: 128 rows x 64 values
       uint32_t b = 0, ph = 0, issued = 0;
-      uint32_t xmask = 0, last_e2 = 0;  // per slot: parity of its next E2 fill; last fill was E2
+      // per slot: parity of its next E2 fill, of its next E5 fill; its last fill was E2
+      uint32_t xmask = 0, fmask = 0, last_e2 = 0;
       bool ok = true;
       for (int64_t i = 0; ok && i < n_my; ++i) {
         const int64_t tile = blockIdx.x + i * gridDim.x;
@@ -236,22 +233,24 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
               break;
             }
             const uint32_t base = sb + b * kStageBytes;
-            mbar_arrive_expect_tx(bar(BAR_FULL + b), e2 ? 2 * kPartBytes : 4 * kPartBytes);
-            tma_load_2d(base, map, st * kStageK, row0, bar(BAR_FULL + b));
-            tma_load_2d(base + kPartBytes, map, st * kStageK, d + row0, bar(BAR_FULL + b));
+            // an E2 stage (B operand and key tile) lands on XFULL, which the
+            // key-operand warps wait for; an E5 stage (B operand and residual
+            // tile) on FULL, which the issuer waits for
+            const uint32_t fb = bar((e2 ? BAR_XFULL : BAR_FULL) + b);
+            mbar_arrive_expect_tx(fb, e2 ? 2 * kPartBytes + kXBytes : 4 * kPartBytes);
+            tma_load_2d(base, map, st * kStageK, row0, fb);
+            tma_load_2d(base + kPartBytes, map, st * kStageK, d + row0, fb);
             if (e2) {
-              mbar_arrive_expect_tx(bar(BAR_XFULL + b), kXBytes);
               // fp32 keys: two boxes of 32 values (128-byte rows); 16-bit keys: one of 64
-              tma_load_2d(base + 2 * kPartBytes, &tmX, st * kStageK, xrow0, bar(BAR_XFULL + b));
-              if constexpr (DT == 0)
-                tma_load_2d(base + 3 * kPartBytes, &tmX, st * kStageK + 32, xrow0, bar(BAR_XFULL + b));
+              tma_load_2d(base + 2 * kPartBytes, &tmX, st * kStageK, xrow0, fb);
+              if constexpr (DT == 0) tma_load_2d(base + 3 * kPartBytes, &tmX, st * kStageK + 32, xrow0, fb);
               xmask ^= 1u << b;
               last_e2 |= 1u << b;
             } else {
+              tma_load_2d(base + 2 * kPartBytes, &tmR, st * kStageK, (int32_t)(s_slot * 256), fb);
+              tma_load_2d(base + 3 * kPartBytes, &tmR, st * kStageK, (int32_t)(s_slot * 256 + 128), fb);
+              fmask ^= 1u << b;
               last_e2 &= ~(1u << b);
-              tma_load_2d(base + 2 * kPartBytes, &tmR, st * kStageK, (int32_t)(s_slot * 256), bar(BAR_FULL + b));
-              tma_load_2d(base + 3 * kPartBytes, &tmR, st * kStageK, (int32_t)(s_slot * 256 + 128),
-                          bar(BAR_FULL + b));
             }
             ++issued;
             if (++b == kStages) {
@@ -266,16 +265,20 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       int dummy = 0;
       for (uint32_t k = 0; k < (issued < kStages ? issued : kStages); ++k) {
         b = b == 0 ? kStages - 1 : b - 1;
-        if (b == kStages - 1) ph ^= 1u;
-        mbar_wait(bar(BAR_FULL + b), ph, &dummy);
-        if ((last_e2 >> b) & 1u) mbar_wait(bar(BAR_XFULL + b), ((xmask >> b) & 1u) ^ 1u, &dummy);
+        if ((last_e2 >> b) & 1u)
+          mbar_wait(bar(BAR_XFULL + b), ((xmask >> b) & 1u) ^ 1u, &dummy);
+        else
+          mbar_wait(bar(BAR_FULL + b), ((fmask >> b) & 1u) ^ 1u, &dummy);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (its operands stay warp-uniform); one
+    // elected lane issues each MMA and commit.
+    {
       const uint32_t idesc = idesc_f16(0u, 128, (uint32_t)NC);
-      uint32_t b = 0, bph = 0, s = 0, aph = 0, cq = 0;
+      // ring slot; per slot, parity of its next E2 fill and of its next E5 fill
+      uint32_t b = 0, xmask = 0, fmask = 0, cq = 0;
       bool ok = true;
       for (int64_t i = 0; ok && i < n_my; ++i) {
         for (int job = 0; ok && job < JOBS; ++job) {
@@ -283,19 +286,22 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
           // K in slices of 128 coordinates, each into a fresh partial accumulator
           for (int c = 0; ok && c < S / kSliceStages; ++c, ++cq) {
             const uint32_t pb = cq & 1u, d_acc = tmem + pb * kSliceCols;
-            if (!mbar_wait_suspend(bar(BAR_DEMPTY + pb), ((cq >> 1) & 1u) ^ 1u, abort)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_DEMPTY + pb), ((cq >> 1) & 1u) ^ 1u, abort))) {
               ok = false;
               break;
             }
             for (int st = 0; st < kSliceStages; ++st) {
-              if (!mbar_wait_suspend(bar(BAR_FULL + b), bph, abort) ||
-                  (e2 && !mbar_wait_suspend(bar(BAR_AFULL + s), aph, abort))) {
+              // E2: the key-operand warps saw the stage land and wrote its
+              // A operand (one wait covers both); E5: the stage landed
+              const bool got = e2 ? mbar_wait_suspend(bar(BAR_AFULL + b), (xmask >> b) & 1u, abort)
+                                  : mbar_wait_suspend(bar(BAR_FULL + b), (fmask >> b) & 1u, abort);
+              if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
               const uint32_t bq = sb + b * kStageBytes;
-              const uint32_t at = tmem + kARing + s * (2 * kAPartCols);
+              const uint32_t at = tmem + kARing + b * (2 * kAPartCols);
               // k steps of 16 values: 32 bytes within the 128-byte swizzle rows
               // (descriptor address units of 16 bytes)
               const uint64_t bh0 = sdesc_k_sw128(bq), bl0 = sdesc_k_sw128(bq + kPartBytes);
@@ -306,36 +312,33 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
                 const uint32_t acc = (st == 0 && ks == 0) ? 0u : 1u;
                 if (e2) {
                   const uint32_t a_hi = at + 8 * ks, a_lo = at + kAPartCols + 8 * ks;
-                  mma_f16_ts(d_acc, a_hi, b_hi, idesc, acc);
-                  mma_f16_ts(d_acc, a_hi, b_lo, idesc, 1u);
-                  mma_f16_ts(d_acc, a_lo, b_hi, idesc, 1u);
+                  mma_f16_ts_w(d_acc, a_hi, b_hi, idesc, acc);
+                  mma_f16_ts_w(d_acc, a_hi, b_lo, idesc, 1u);
+                  mma_f16_ts_w(d_acc, a_lo, b_hi, idesc, 1u);
                 } else {
                   const uint64_t r_hi = rh0 + 2u * ks, r_lo = rl0 + 2u * ks;
-                  mma_f16_ss(d_acc, r_hi, b_hi, idesc, acc);
-                  mma_f16_ss(d_acc, r_hi, b_lo, idesc, 1u);
-                  mma_f16_ss(d_acc, r_lo, b_hi, idesc, 1u);
+                  mma_f16_ss_w(d_acc, r_hi, b_hi, idesc, acc);
+                  mma_f16_ss_w(d_acc, r_hi, b_lo, idesc, 1u);
+                  mma_f16_ss_w(d_acc, r_lo, b_hi, idesc, 1u);
                 }
               }
-              mma_commit(bar(BAR_EMPTY + b));
-              if (++b == kStages) {
-                b = 0;
-                bph ^= 1u;
-              }
-              if (e2) {
-                mma_commit(bar(BAR_AEMPTY + s));
-                if (++s == kAStages) {
-                  s = 0;
-                  aph ^= 1u;
-                }
-              }
+              // frees the slot's shared memory and its TMEM A columns: the
+              // key-operand warps rewrite those only after the slot's next
+              // fill lands, which the producer issues after this commit
+              mma_commit_w(bar(BAR_EMPTY + b));
+              if (e2)
+                xmask ^= 1u << b;
+              else
+                fmask ^= 1u << b;
+              if (++b == kStages) b = 0;
             }
             if (!ok) break;
-            mma_commit(bar(BAR_DFULL + pb));
+            mma_commit_w(bar(BAR_DFULL + pb));
           }
         }
       }
-      if (!ok) raise(a.err, abort);
-      mma_commit(bar(BAR_DONE));
+      if (!ok && lane == 0) raise(a.err, abort);
+      mma_commit_w(bar(BAR_DONE));
       int dummy = 0;
       mbar_wait(bar(BAR_DONE), 0, &dummy);
     }
@@ -344,7 +347,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + kARing;
-    uint32_t b = 0, xmask = 0, s = 0, aph = 0;  // ring slot, per-slot parity of its next E2 fill
+    uint32_t b = 0, xmask = 0;  // ring slot, per-slot parity of its next E2 fill
     bool ok = true;
     for (int64_t i = 0; ok && i < n_my; ++i) {
       const int64_t tile = blockIdx.x + i * gridDim.x;
@@ -353,14 +356,15 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       const float n = *reinterpret_cast<const float*>(a.packed + tile * a.lay.block_bytes + a.lay.norms_off + row * 8);
       const float inv = n > 0.f ? 256.f / n : 0.f;
       for (int t = 0; ok && t < J * S; ++t) {
-        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_XFULL + b), (xmask >> b) & 1u, abort)) ||
-            !__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_AEMPTY + s), aph ^ 1u, abort))) {
+        // the stage landed; its TMEM A columns are free (the MMAs that last
+        // read them completed before the producer refilled the slot)
+        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_XFULL + b), (xmask >> b) & 1u, abort))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint8_t* xs = smem + b * kStageBytes + 2 * kPartBytes;
-        const uint32_t col = t_lane + s * (2 * kAPartCols);
+        const uint32_t col = t_lane + b * (2 * kAPartCols);
         // 128-byte rows, 16-byte chunk c at position c ^ (row % 8); values in
         // two halves of 32, each one 16-column TMEM store per part
 #pragma unroll
@@ -395,11 +399,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(BAR_AFULL + s));
-        if (++s == kAStages) {
-          s = 0;
-          aph ^= 1u;
-        }
+        mbar_arrive(bar(BAR_AFULL + b));
         xmask ^= 1u << b;
         if (++b == kStages) b = 0;
       }

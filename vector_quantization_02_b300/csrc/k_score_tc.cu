@@ -168,7 +168,7 @@ __device__ __forceinline__ void issue_job(uint32_t d, uint32_t at, uint64_t b, u
     for (uint32_t kb = 0; kb < 4; ++kb)
       // plane p of the image: N rows x 128 B (one swizzle atom column), p N 128
       // bytes in; K step kb starts 32 bytes further (descriptor units of 16 B)
-      mma_f8_ts(d, at + (uint32_t)(p * kPlaneCols) + 8u * kb,
+      mma_f8_ts_w(d, at + (uint32_t)(p * kPlaneCols) + 8u * kb,
                 b + (uint64_t)(((uint32_t)p * (uint32_t)N * 128u) >> 4) + 2u * kb, idesc,
                 (p > P0 || kb > 0) ? 1u : 0u);
 }
@@ -286,8 +286,10 @@ __global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_ke
     // warp w issues every MMA of the tiles i with i % I == w (TMEM entries
     // i % R), then one commit: the tile's plane slots are free and its
     // accumulators full (the expansion and the epilogue of that entry both
-    // wait on it, each for every phase in turn)
-    if (lane == 0) {
+    // wait on it, each for every phase in turn).  The whole warp runs the loop
+    // (its operands stay warp-uniform); one elected lane issues each MMA and
+    // commit.
+    {
       constexpr uint32_t idesc = idesc_e4m3(128, N);
       // descriptors of the two query-image buffers, computed once
       const uint64_t bdesc0 = sdesc_k_sw128(sb), bdesc1 = sdesc_k_sw128(sb + a.img_bytes);
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_ke
           pos.advance(1, nb);
           if (pos.g != g0) {
             // this warp's MMAs on the previous group's image are all issued
-            mma_commit(bar(BAR_BEMPTY + (epoch & 1u)));
+            mma_commit_w(bar(BAR_BEMPTY + (epoch & 1u)));
             ++epoch;
             need_b = true;
           }
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_ke
         // every issuer waits for every group's image, owning tiles there or
         // not, so that it sees each phase of the image barriers in turn
         if (need_b) {
-          if (!mbar_wait_suspend(bar(BAR_BFULL + (epoch & 1u)), (epoch >> 1) & 1u, abort)) {
+          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_BFULL + (epoch & 1u)), (epoch >> 1) & 1u, abort))) {
             ok = false;
             break;
           }
@@ -320,8 +322,8 @@ __global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_ke
         // polled with a suspend hint: a spinning issuer takes issue slots from
         // the expansion and epilogue warps that share its SM sub-partition
         // (measured: 3 % faster on the decode cache, 7 % on the Llama cache)
-        if (!mbar_wait_suspend(bar(BAR_PFULL + ent.idx), ent.phase, abort) ||
-            !mbar_wait_suspend(bar(BAR_DEMPTY + ent.idx), ent.phase ^ 1u, abort)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_PFULL + ent.idx), ent.phase, abort) &&
+                                         mbar_wait_suspend(bar(BAR_DEMPTY + ent.idx), ent.phase ^ 1u, abort))) {
           ok = false;
           break;
         }
@@ -331,10 +333,10 @@ __global__ void __launch_bounds__(TcRoles<HP, K, PROD>::kThreads, 1) score_tc_ke
         const uint64_t b = (epoch & 1u) ? bdesc1 : bdesc0;
         issue_job<0, NA, N>(d, at, b, idesc);
         if constexpr (PROD) issue_job<NA, NP, N>(d + (uint32_t)N, at, b, idesc);
-        mma_commit(bar(BAR_MDONE + ent.idx));
+        mma_commit_w(bar(BAR_MDONE + ent.idx));
       }
-      if (!ok) raise(a.err, abort);
-      mma_commit(bar(BAR_DONE + warp));
+      if (!ok && lane == 0) raise(a.err, abort);
+      mma_commit_w(bar(BAR_DONE + warp));
       int dummy = 0;
       mbar_wait(bar(BAR_DONE + warp), 0, &dummy);
     }
