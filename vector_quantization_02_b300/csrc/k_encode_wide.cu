@@ -19,37 +19,43 @@
 // 2^16 t; the residual enters E5 as 2^10 r'.  Signs do not see the scales.
 //
 // A tile is 128 keys (one packed block).  Its work is a sequence of jobs,
-// each 128 keys x 128 coordinates over K = d in stages of 32 coordinates,
-// accumulated in TMEM per 128-coordinate slice of K and summed in fp32 by the
-// epilogue (one tensor-core accumulator over K = 1536 loses too much):
+// each 128 keys x 128 coordinates (one chunk) over K = d in stages of 64
+// coordinates, accumulated in TMEM per 128-coordinate slice of K and summed in
+// fp32 by the epilogue (one tensor-core accumulator over K = 1536 loses too
+// much):
 //   d / NC E2 jobs  Y[:, chunk] = X Pi[chunk]^T, then quantised: code bits
-//                   into the packed block, the residual's split into a
-//                   per-SM scratch row (rows of this SM's CTA only),
+//                   into the packed block, the residual's split into the
+//                   cluster's scratch rows,
 //   d / NC E5 jobs  P[:, chunk] = R M[chunk]^T, then the sign bits.
-// The scratch belongs to the SM: this kernel needs a whole SM (all 512 TMEM
-// columns, more than half of the shared memory), so no two of its CTAs, from
-// any launch, share one at a time.
+// A thread-block cluster of CL CTAs (one per SM) works on each tile: CTA r
+// takes the chunks r, r + CL, ...  Every job re-reads the whole key tile (E2)
+// or residual tile (E5); shared by the cluster, the tiles being worked on fit
+// in L2, and those re-reads stay out of DRAM.  The CTAs meet twice per tile:
+// every CTA's residual columns are written before any CTA's E5 stages load the
+// residual (a barrier each CTA arrives on in every CTA), and rank 0 adds the
+// CTAs' partial ||r||^2 (sent to its shared memory) into rho.
+// The scratch slot of a cluster is its rank-0 SM's id: this kernel needs a
+// whole SM (all 512 TMEM columns, more than half of the shared memory), so no
+// two of its CTAs, from any launch, share one at a time.
 // ||x|| comes from a pre-pass (key_norm_kernel) that writes it into the packed
 // block's norm slot.
 //  warp 0       producer: TMA loads into a 3-stage shared-memory ring; a stage
 //               holds the B operand (hi and lo rows of 2^8 Pi or M for the
 //               job's 128 columns, 64 coordinates, 128-byte swizzle) and the A
 //               source: the key tile (E2) or the residual tile from the scratch
-//               (E5, read by the MMA straight from shared memory).  Stages of
-//               64 coordinates carry 12 MMAs per commit: the issuing thread's
-//               commits and waits, not the tensor pipe, set the pace of a
-//               stage (~220 cycles per commit), so fewer, larger stages run
-//               faster.
+//               (E5, read by the MMA straight from shared memory).
 //  warp 1       TMEM owner (two partial accumulators in [0, 256), the E2 key
-//               operand ring in [256, 512)) and MMA issuer (the warp runs
-//               the loop converged, one elected lane issues).
+//               operand of each ring stage in [256, 448)) and MMA issuer (the
+//               warp runs the loop converged, one elected lane issues): one
+//               wait and one commit per stage of 12 MMAs.
 //  warps 2-5    E2 key operand: thread (warp w, lane l) owns key row
 //               32 (w % 4) + l; per stage it reads its 64 coordinates from the
 //               staged key tile and writes u = 2^8 x / ||x|| as fp16 hi, lo into
-//               TMEM (4-stage ring).
+//               the stage's TMEM columns.
 //  warps 6-13   epilogue: two warpgroups, each taking half of a job's columns.
 // Every wait is bounded: on expiry the kernel raises the plan's error word,
-// drains what it issued and frees its TMEM.
+// drains what it issued and frees its TMEM; the CTAs of a cluster leave
+// together.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -71,6 +77,7 @@ constexpr int kARing = 256;        // first TMEM column of the E2 key operand, o
 constexpr int kAPartCols = 32;     // TMEM columns of one A part per stage (64 16-bit values)
 constexpr int kSliceCols = 128;    // output columns of a job (two partial accumulators of 128 columns)
 constexpr int kSliceStages = 2;    // stages (128 coordinates of K) per partial accumulator
+constexpr int kMaxCluster = 4;     // CTAs per cluster at most (a power of two)
 
 enum {
   BAR_FULL = 0,                       // E5 stage landed: B operand and residual tile (only E5 fills advance it)
@@ -90,6 +97,7 @@ struct EncWideArgs {
   CodeParams cp;
   ParityExpansion px;
   int NC, J, S;               // chunk columns, jobs per phase, stages per job
+  int CL;                     // CTAs per cluster (a divisor of J): CTA r of a cluster takes chunks r, r + CL, ...
   int nslots;                 // scratch slots (SM ids)
   int64_t G, N, nb, n_tiles;
   const void* keys;
@@ -152,10 +160,16 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
-  const int d = a.lay.d, NC = a.NC, J = a.J, S = a.S;
-  const int JOBS = PROD ? 2 * J : J;  // E2 jobs, then (Prod) E5 jobs
+  const int d = a.lay.d, NC = a.NC, J = a.J, S = a.S, CL = a.CL;
+  const uint32_t rank = cluster_ctarank();
+  // this CTA's jobs: its E2 chunks rank, rank + CL, ... (Jm of them), then (Prod)
+  // the E5 jobs of the same chunks; the cluster's CTAs share each tile
+  const int Jm = J / CL;
+  const int MYJOBS = PROD ? 2 * Jm : Jm;
+  auto job_of = [&](int t) { return t < Jm ? (int)rank + CL * t : J + (int)rank + CL * (t - Jm); };
   const uint32_t off_bar = kStages * kStageBytes;
   float* s_rr = reinterpret_cast<float*>(smem + off_bar + BAR_COUNT * 8);  // [2][128]
+  float* s_rr_peer = s_rr + 256;  // [CL - 1][128] (rank 0): the other CTAs' partial ||r||^2 per row
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ uint32_t s_slot;
@@ -175,8 +189,11 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       mbar_init(bar(BAR_DFULL + b), 1);
       mbar_init(bar(BAR_DEMPTY + b), 256);
     }
-    mbar_init(bar(BAR_RREADY), 256);
-    mbar_init(bar(BAR_RHO), 256);
+    // the residual rows of a tile: every epilogue thread of every CTA of the cluster
+    mbar_init(bar(BAR_RREADY), 256 * CL);
+    // the tile's ||r||^2 partials: both local warpgroups, and on rank 0 one
+    // warpgroup of each other CTA
+    mbar_init(bar(BAR_RHO), rank == 0 ? 256 + 128 * (CL - 1) : 256);
     mbar_init(bar(BAR_DONE), 1);
     fence_mbar_init();
   }
@@ -187,19 +204,28 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every CTA of the cluster has initialised its barriers before any remote
+  // arrival; the cluster's residual scratch slot is rank 0's SM id (no two
+  // running CTAs of this kernel share an SM: its shared memory use rules it out)
+  cluster_sync_all();
+  if (threadIdx.x == 0 && rank != 0) s_slot = ld_cluster_u32(mapa_shared(smem_u32(&s_slot), 0));
+  __syncthreads();
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &abort_flag;
-  // (Prod) the residual scratch slot of this SM; cannot be out of range with
-  // a plan built on this device
+  // (Prod) cannot be out of range with a plan built on this device; the same
+  // slot, so the same decision, in every CTA of the cluster
   if (PROD && s_slot >= (uint32_t)a.nslots) {
     if (threadIdx.x == 0) raise(a.err, abort);
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, 512);
+    cluster_sync_all();
     return;
   }
   uint16_t* scr = PROD ? static_cast<uint16_t*>(a.scratch) + (size_t)s_slot * 2 * 128 * d : nullptr;
 
-  const int64_t n_my = blockIdx.x < a.n_tiles ? (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  // tiles of this cluster: c, c + P, ... (P clusters)
+  const int64_t cid = blockIdx.x / CL, P = gridDim.x / CL;
+  const int64_t n_my = cid < a.n_tiles ? (a.n_tiles - 1 - cid) / P + 1 : 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -214,16 +240,19 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       uint32_t xmask = 0, fmask = 0, last_e2 = 0;
       bool ok = true;
       for (int64_t i = 0; ok && i < n_my; ++i) {
-        const int64_t tile = blockIdx.x + i * gridDim.x;
+        const int64_t tile = cid + i * P;
         const int64_t g = tile / a.nb, blk = tile - g * a.nb;
         const int32_t xrow0 = (int32_t)(g * a.N + blk * kTokensPerBlock);
-        for (int job = 0; ok && job < JOBS; ++job) {
-          const bool e2 = job < J;
-          if (job == J) {  // the residual rows of this tile are in the scratch
-            if (!mbar_wait_suspend(bar(BAR_RREADY), (uint32_t)i & 1u, abort)) {
+        for (int t = 0; ok && t < MYJOBS; ++t) {
+          const int job = job_of(t);
+          const bool e2 = t < Jm;
+          if (t == Jm) {  // every CTA of the cluster has written its residual columns of this tile
+            if (!mbar_wait_suspend_cluster(bar(BAR_RREADY), (uint32_t)i & 1u, abort)) {
               ok = false;
               break;
             }
+            // the other CTAs' generic stores, read next by the async proxy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
           }
           const CUtensorMap* map = e2 ? &tmPi : &tmM;
           const int row0 = (job % J) * NC;
@@ -281,8 +310,8 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       uint32_t b = 0, xmask = 0, fmask = 0, cq = 0;
       bool ok = true;
       for (int64_t i = 0; ok && i < n_my; ++i) {
-        for (int job = 0; ok && job < JOBS; ++job) {
-          const bool e2 = job < J;
+        for (int t = 0; ok && t < MYJOBS; ++t) {
+          const bool e2 = t < Jm;
           // K in slices of 128 coordinates, each into a fresh partial accumulator
           for (int c = 0; ok && c < S / kSliceStages; ++c, ++cq) {
             const uint32_t pb = cq & 1u, d_acc = tmem + pb * kSliceCols;
@@ -350,12 +379,12 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
     uint32_t b = 0, xmask = 0;  // ring slot, per-slot parity of its next E2 fill
     bool ok = true;
     for (int64_t i = 0; ok && i < n_my; ++i) {
-      const int64_t tile = blockIdx.x + i * gridDim.x;
+      const int64_t tile = cid + i * P;
       // ||x|| from the pre-pass (0 for padded rows, whose staged rows may hold
       // another group's keys)
       const float n = *reinterpret_cast<const float*>(a.packed + tile * a.lay.block_bytes + a.lay.norms_off + row * 8);
       const float inv = n > 0.f ? 256.f / n : 0.f;
-      for (int t = 0; ok && t < J * S; ++t) {
+      for (int t = 0; ok && t < Jm * S; ++t) {
         // the stage landed; its TMEM A columns are free (the MMAs that last
         // read them completed before the producer refilled the slot)
         if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_XFULL + b), (xmask >> b) & 1u, abort))) {
@@ -404,7 +433,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
         if (++b == kStages) b = 0;
       }
       // the tile's E5 stages pass through the ring without this role
-      if constexpr (PROD) b = (uint32_t)((b + (uint32_t)(J * S)) % kStages);
+      if constexpr (PROD) b = (uint32_t)((b + (uint32_t)(Jm * S)) % kStages);
     }
     if (!ok) raise(a.err, abort);
   } else {
@@ -420,7 +449,7 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
     uint32_t cq = 0;
     bool ok = true;
     for (int64_t i = 0; ok && i < n_my; ++i) {
-      const int64_t tile = blockIdx.x + i * gridDim.x;
+      const int64_t tile = cid + i * P;
       const int64_t blk = tile % a.nb;
       const bool live = blk * kTokensPerBlock + row < a.N;
       uint8_t* out = a.packed + tile * a.lay.block_bytes;
@@ -428,17 +457,18 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
       float nt[L - 1], nc[L];
       uint32_t nhalf[NT];
       float nmid = 0.f;
-      for (int job = 0; ok && job < JOBS; ++job) {
-        const bool e2 = job < J;
-        if (job == 0) {
+      for (int t = 0; ok && t < MYJOBS; ++t) {
+        const int job = job_of(t);
+        const bool e2 = t < Jm;
+        if (t == 0) {
           n = *reinterpret_cast<const float*>(out + a.lay.norms_off + row * 8);
           // thresholds and centroids in the scale of Y = 2^16 Pi u (exact)
 #pragma unroll
-          for (int t = 0; t < L - 1; ++t) nt[t] = kYScale * a.cp.t[t];
+          for (int q = 0; q < L - 1; ++q) nt[q] = kYScale * a.cp.t[q];
 #pragma unroll
-          for (int t = 0; t < L; ++t) nc[t] = kYScale * a.cp.c[t];
+          for (int q = 0; q < L; ++q) nc[q] = kYScale * a.cp.c[q];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) nhalf[t] = __float_as_uint(-(kYScale * a.px.half[t]));
+          for (int q = 0; q < NT; ++q) nhalf[q] = __float_as_uint(-(kYScale * a.px.half[q]));
           nmid = kYScale * a.px.mid;
         }
         // the job's sums: partial accumulators of 128-coordinate K slices,
@@ -484,17 +514,17 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
                 uint32_t sbit[L - 1];
                 float cv = nc[0];
 #pragma unroll
-                for (int t = 0; t < L - 1; ++t) {
-                  sbit[t] = __float_as_uint(nt[t] - y);
-                  if constexpr (!PX) cv = (int)sbit[t] < 0 ? nc[t + 1] : cv;
+                for (int q = 0; q < L - 1; ++q) {
+                  sbit[q] = __float_as_uint(nt[q] - y);
+                  if constexpr (!PX) cv = (int)sbit[q] < 0 ? nc[q + 1] : cv;
                 }
                 uint32_t xb[K];
 #pragma unroll
                 for (int p = 0; p < K; ++p) {
                   uint32_t x = 0;
 #pragma unroll
-                  for (int t = 0; t < L - 1; ++t)
-                    if (((t + 1) & ((1 << p) - 1)) == 0) x ^= sbit[t];
+                  for (int q = 0; q < L - 1; ++q)
+                    if (((q + 1) & ((1 << p) - 1)) == 0) x ^= sbit[q];
                   xb[p] = x;
                   w[p] = __funnelshift_l(x, w[p], 1);
                 }
@@ -517,9 +547,9 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
               uint4* dh = reinterpret_cast<uint4*>(rhi + cbase + 32 * g32);
               uint4* dl = reinterpret_cast<uint4*>(rlo + cbase + 32 * g32);
   #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                __stcg(dh + t, make_uint4(hi[4 * t], hi[4 * t + 1], hi[4 * t + 2], hi[4 * t + 3]));
-                __stcg(dl + t, make_uint4(lo[4 * t], lo[4 * t + 1], lo[4 * t + 2], lo[4 * t + 3]));
+              for (int q = 0; q < 4; ++q) {
+                __stcg(dh + q, make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]));
+                __stcg(dl + q, make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]));
               }
             }
 #pragma unroll
@@ -537,30 +567,44 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
           uint8_t* dst = out + a.lay.plane_off(p, chunk, row) + 4 * w0;
           *reinterpret_cast<uint2*>(dst) = live ? make_uint2(pl[p][0], pl[p][1]) : make_uint2(0, 0);
         }
-        if (PROD && e2 && job == J - 1) {
-          // every residual row of the tile written by this thread, made
-          // visible to the TMA loads (async proxy) that read them
+        if (PROD && t == Jm - 1) {
+          // every residual column of the tile this thread writes is stored,
+          // made visible to the TMA loads (async proxy) of every CTA of the
+          // cluster.  The local arrival comes first: once a peer has seen this
+          // thread's remote arrival, this CTA's phase has it too, so no
+          // CTA's next-tile arrivals can reach a phase that is still open.
           asm volatile("fence.proxy.async.global;" ::: "memory");
           mbar_arrive(bar(BAR_RREADY));
+          for (int q = 1; q < CL; ++q) mbar_arrive_cluster(mapa_shared(bar(BAR_RREADY), (rank + (uint32_t)q) % (uint32_t)CL));
         }
       }
       if (!ok) break;
       if constexpr (PROD) {
-        // rho: the two warpgroups' partial sums.  Warpgroup 1 cannot run a
-        // whole tile ahead here (the tile's E5 waits for both warpgroups'
-        // residual rows), so this barrier's phases cannot alias.
+        // rho: the partial sums of both warpgroups of every CTA of the
+        // cluster, added on rank 0.  No arrival can come a tile early: a
+        // CTA's next tile needs that tile's residual columns from every
+        // CTA, which rank 0's warpgroup 0 writes only after this exchange.
         s_rr[wg * 128 + row] = rr;
         mbar_arrive(bar(BAR_RHO));
         if (wg == 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait_suspend(bar(BAR_RHO), (uint32_t)i & 1u, abort))) {
+          const bool got = rank == 0 ? mbar_wait_suspend_cluster(bar(BAR_RHO), (uint32_t)i & 1u, abort)
+                                     : mbar_wait_suspend(bar(BAR_RHO), (uint32_t)i & 1u, abort);
+          if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
           }
-          const float rho = n * (sqrtf(s_rr[row] + s_rr[128 + row]) * (1.f / kYScale));
-          *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, rho)
-                                                                               : make_float2(0.f, 0.f);
+          float r2 = s_rr[row] + s_rr[128 + row];
+          if (rank == 0) {
+            for (int q = 1; q < CL; ++q) r2 += s_rr_peer[(q - 1) * 128 + row];
+            const float rho = n * (sqrtf(r2) * (1.f / kYScale));
+            *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, rho)
+                                                                                 : make_float2(0.f, 0.f);
+          } else {
+            st_cluster_f32(mapa_shared(smem_u32(s_rr_peer + (rank - 1) * 128 + row), 0), r2);
+            mbar_arrive_cluster(mapa_shared(bar(BAR_RHO), 0));
+          }
         }
-      } else if (wg == 0) {
+      } else if (wg == 0 && rank == 0) {
         // MSE stores ||r|| = 0 and needs no exchange (which, with one K slice
         // per tile at d = 128, would let warpgroup 1 lap this barrier)
         *reinterpret_cast<float2*>(out + a.lay.norms_off + row * 8) = live ? make_float2(n, 0.f)
@@ -574,6 +618,10 @@ encode_wide_kernel(const __grid_constant__ CUtensorMap tmPi, const __grid_consta
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  // no CTA leaves while another may still arrive on its barriers or write its
+  // shared memory (on a bounded-wait abort; otherwise each CTA has waited for
+  // every arrival aimed at it)
+  cluster_sync_all();
 }
 
 __global__ void nsmid_kernel(int* out) {
@@ -583,10 +631,19 @@ __global__ void nsmid_kernel(int* out) {
 }
 
 // at least 120 KB, so that no two CTAs of this kernel share an SM (the
-// residual scratch is indexed by the SM)
+// residual scratch is indexed by an SM id)
 size_t enc_wide_smem(int) {
-  const size_t need = (size_t)kStages * kStageBytes + BAR_COUNT * 8 + 2 * 128 * sizeof(float) + 1024;
+  const size_t need = (size_t)kStages * kStageBytes + BAR_COUNT * 8 + (2 + kMaxCluster - 1) * 128 * sizeof(float) + 1024;
   return need > 120 * 1024 ? need : 120 * 1024;
+}
+
+// CTAs per cluster for J chunks per phase: the CTAs of a cluster split each
+// tile's chunks, so that a key or residual tile, re-read once per chunk, is
+// shared by them and the tiles being worked on fit in L2
+int enc_wide_cluster(int J) {
+  for (int c = kMaxCluster; c > 1; c >>= 1)
+    if (J % c == 0) return c;
+  return 1;
 }
 
 // ||x|| of every row of every 128-token block (0 for padded rows) into the
@@ -655,8 +712,27 @@ cudaError_t launch_ew(const tq_plan* p, const EncWideArgs& a, const EncMaps& mp,
   const size_t smem = enc_wide_smem(a.NC);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int64_t grid = a.n_tiles < sms ? a.n_tiles : sms;
-  kern<<<(unsigned)grid, kEThreads, smem, s>>>(mp.pi, mp.m, mp.x, mp.r, a);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kEThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // one persistent cluster per group of CL SMs that can hold one at a time
+  cfg.gridDim = dim3((unsigned)(sms / a.CL * a.CL));
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  const int64_t n_cl = a.n_tiles < clusters ? a.n_tiles : clusters;
+  cfg.gridDim = dim3((unsigned)(n_cl * a.CL));
+  e = cudaLaunchKernelEx(&cfg, kern, mp.pi, mp.m, mp.x, mp.r, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -716,6 +792,7 @@ cudaError_t launch_encode_wide(const tq_plan* p, const void* keys, tq_dtype dt, 
   a.px = p->px;
   a.NC = enc_wide_nc(d);
   a.J = d / a.NC;
+  a.CL = enc_wide_cluster(a.J);
   a.S = d / kStageK;
   a.nslots = p->wide_slots;
   a.G = G;

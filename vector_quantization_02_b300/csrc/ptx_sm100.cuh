@@ -79,6 +79,54 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// ---------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: writes before are visible to the
+// cluster's threads after (release/acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the variable at shared::cta address a in CTA rank r.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t r) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(r));
+  return d;
+}
+// Arrive once on an mbarrier of another CTA of the cluster (shared::cluster
+// address), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t caddr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+  return v;
+}
+// mbar_wait_suspend for a barrier that other CTAs of the cluster arrive on:
+// acquires at cluster scope what their arrivals released.
+__device__ __forceinline__ bool mbar_wait_suspend_cluster(uint32_t bar, uint32_t parity, const volatile int* abort) {
+  for (uint32_t it = 0; it < kSuspendPolls; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63) == 63 && *abort) return false;
+  }
+  return false;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Lets the next kernel on the stream (launched with programmatic stream
 // serialisation) begin before this grid completes.
