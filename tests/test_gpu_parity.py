@@ -41,6 +41,10 @@ ENCODE_CASES = [
     (128, 1, 40000, torch.float32, 4, "mse", True),
     (384, 1, 200, torch.float16, 2, "mse", False),
     (1536, 1, 130, torch.float32, 3, "mse", False),
+    # the wide kernel's clusters over many tiles each: four CTAs per tile at
+    # d = 512 (about ten tiles per cluster), two at d = 256
+    (512, 2, 20000, torch.bfloat16, 3, "prod", False),
+    (256, 1, 40000, torch.float16, 4, "prod", True),
 ]
 
 
@@ -59,6 +63,30 @@ def test_encode_matches_oracle(cuda, d, G, N, dtype, bits, mode, outliers):
     torch.cuda.synchronize()
     assert plan.status() == 0
     compare_encode(inp, packed.cpu().numpy(), keys)
+
+
+def test_wide_encode_concurrent_streams(cuda):
+    """One plan, two streams, two wide encodes at once (fp32, d = 1536, 150 tiles
+    each): the residual scratch is chosen per SM, so concurrent launches of the
+    kernel never share a slot and each result equals the same call alone."""
+    w, inp = _case_inputs(1536, 1, 19200, torch.float32, 4, "prod", False)
+    plan = inp.plan()
+    ka = tq_synth.keys(w, device=cuda)
+    kb = tq_synth.keys(w, device=cuda, seed_offset=5)
+    want_a = tq.tq_encode(plan, ka)
+    want_b = tq.tq_encode(plan, kb)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    pa, pb = torch.empty_like(want_a), torch.empty_like(want_b)
+    for _ in range(3):
+        pa.zero_()
+        pb.zero_()
+        torch.cuda.synchronize()
+        tq.tq_encode(plan, ka, packed=pa, stream=sa)
+        tq.tq_encode(plan, kb, packed=pb, stream=sb)
+        torch.cuda.synchronize()
+        assert plan.status() == 0
+        assert torch.equal(pa, want_a) and torch.equal(pb, want_b)
 
 
 def test_encode_special_keys(cuda):
