@@ -77,7 +77,7 @@ constexpr int kARing = 256;        // first TMEM column of the E2 key operand, o
 constexpr int kAPartCols = 32;     // TMEM columns of one A part per stage (64 16-bit values)
 constexpr int kSliceCols = 128;    // output columns of a job (two partial accumulators of 128 columns)
 constexpr int kSliceStages = 2;    // stages (128 coordinates of K) per partial accumulator
-constexpr int kMaxCluster = 4;     // CTAs per cluster at most (a power of two)
+constexpr int kMaxCluster = 4;     // CTAs per cluster at most
 
 enum {
   BAR_FULL = 0,                       // E5 stage landed: B operand and residual tile (only E5 fills advance it)
@@ -641,8 +641,9 @@ size_t enc_wide_smem(int) {
 // tile's chunks, so that a key or residual tile, re-read once per chunk, is
 // shared by them and the tiles being worked on fit in L2
 int enc_wide_cluster(int J) {
-  for (int c = kMaxCluster; c > 1; c >>= 1)
-    if (J % c == 0) return c;
+  static constexpr int kPrefer[] = {4, 3, 2};
+  for (int c : kPrefer)
+    if (c <= kMaxCluster && J % c == 0) return c;
   return 1;
 }
 
