@@ -619,7 +619,12 @@ def run_ours(args, world, rank):
         e2e_ms = None
     else:
         e2e_ms = _e2e(args, world, plan, keys, q, packed, logits, ws, flush, top_k, stream, ev)
-    launches_per_step = 1 + 2 + (2 if top_k else 0)   # encode; query prep + score; top-k
+    # our kernels per step: the encode (encode_tc_kernel, or key_norm_kernel +
+    # encode_wide_kernel), the score (score_tc_prep_kernel + score_tc_kernel, or
+    # the query projections + wide_split_kernel + score_wide_kernel) and top-k
+    enc_launches = 1 if plan.encode_path(w.key_dtype) == "tensor_d128" else 2
+    sc_launches = 2 if plan.score_path(H) == "tensor_d128" else 3
+    launches_per_step = enc_launches + sc_launches + (2 if top_k else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
