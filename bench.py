@@ -58,7 +58,9 @@ def kernel_traffic(kernel: str, source: str, workload: str):
     this workload and the current source of the kernel; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
-            t = json.load(f).get(kernel)
+            tj = json.load(f)
+        # an entry for this kernel on this workload, else the kernel's own
+        t = tj.get(f"{kernel}@{workload}") or tj.get(kernel)
         with open(os.path.join(ROOT, "vector_quantization_02_b300", "csrc", source), "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
         if t and t.get("source_sha") == sha and t.get("workload") == workload:
