@@ -314,6 +314,34 @@ def test_decode_and_score_agree():
     assert np.max(np.abs(q @ xh.T - s)) <= 1e-12 * np.max(np.abs(s))
 
 
+@pytest.mark.parametrize("m", [32, 48])
+def test_decode_prod_is_unbiased_over_projections(m):
+    # The QJL stage reconstructs the residual without bias: for S with i.i.d.
+    # N(0, 1) entries (m rows), E[s sign(s . r)] = sqrt(2/pi) r / ||r|| per row,
+    # so E[sqrt(pi/2)/m * rho * S^T sign(S r)] = r and E_S[x_hat] = x exactly
+    # (Pi fixed).  Per coordinate, Var[x_hat_j] = ((pi/2) rho^2 - r_j^2) / m.
+    # Independent of score_prod: a wrong constant, a missing rho, S in place
+    # of S^T (m = d, where the shapes allow it) or a flipped sign moves the
+    # mean; dividing by d instead of m (m != d) moves it too.
+    d, T = 32, 4000
+    rng = _rng(33 + m)
+    Pi = _haar(d, 34)
+    c = o.codebook_f32(4, d)
+    x = rng.standard_normal((1, d))
+    base = o.encode_mse(x, Pi, c)
+    r = (x - o.mse_reconstruct(base["idx"], base["n"], Pi, c))[0]
+    rho = np.linalg.norm(r)
+    xh = np.empty((T, d))
+    for s in range(T):
+        S = rng.standard_normal((m, d))
+        e = o.encode_prod(x, Pi, S, c)
+        xh[s] = o.decode_prod(e["idx"], e["z"], e["n"], e["rho"], Pi, S, c)[0]
+    var = ((math.pi / 2) * rho ** 2 - r ** 2) / m
+    z = (xh.mean(axis=0) - x[0]) / np.sqrt(var / T)
+    assert np.all(np.abs(z) <= 4.5), np.abs(z).max()
+    assert np.all(np.abs(xh.var(axis=0) / var - 1.0) <= 0.15)
+
+
 def test_score_fp32_is_the_plain_dot_product():
     rng = _rng(32)
     q = rng.standard_normal((2, 3, 8))
