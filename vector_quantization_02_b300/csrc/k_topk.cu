@@ -62,16 +62,36 @@ __device__ void block_merge(float* cs, int64_t* ci, int* cnt, int K, float* out_
   }
 }
 
+// Elements of a row per split: rows of a multiple of 4 elements are split on
+// multiples of 4, so that every split starts on a 16-byte boundary.
+__host__ __device__ inline int64_t topk_per(int64_t N, int splits) {
+  const int64_t per = (N + splits - 1) / splits;
+  return (N & 3) == 0 ? (per + 3) & ~(int64_t)3 : per;
+}
+
+// Order-preserving code of a float (unsigned order = float order, -0 as +0):
+// a value whose code is below another's is strictly smaller.
+__device__ __forceinline__ uint32_t order_code(float v) {
+  const uint32_t b = __float_as_uint(v + 0.f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 __global__ void __launch_bounds__(kTopkThreads)
 topk_stage1(const float* __restrict__ x, int64_t N, int K, int splits, float* ws_s, int64_t* ws_i) {
   extern __shared__ unsigned char tk_sm[];
   float* cs = reinterpret_cast<float*>(tk_sm);
   int64_t* ci = reinterpret_cast<int64_t*>(cs + kTopkThreads * K + (kTopkThreads * K) % 2);
   __shared__ int cnt[kTopkThreads];
+  // a lower bound on the split's k-th best: the best of the full threads'
+  // k-th bests (such a thread holds K values at least as good), as a code
+  __shared__ uint32_t s_bound;
+  if (threadIdx.x == 0) s_bound = 0u;
+  __syncthreads();
+  volatile uint32_t* bound = &s_bound;
   const int64_t row = blockIdx.x / splits;
   const int sp = blockIdx.x % splits;
-  const int64_t per = (N + splits - 1) / splits;
-  const int64_t lo = sp * per, hi = min(N, lo + per);
+  const int64_t per = topk_per(N, splits);
+  const int64_t lo = min(N, sp * per), hi = min(N, lo + per);
   const float* xr = x + row * N;
   const int t = threadIdx.x;
   float* my_s = cs + t * K;
@@ -80,32 +100,68 @@ topk_stage1(const float* __restrict__ x, int64_t N, int K, int splits, float* ws
   // the thread's current k-th best, kept in registers (most values fail the test)
   float th_s = 0.f;
   int64_t th_i = 0;
-  // eight independent loads in flight per step, then the tests in order
-  constexpr int kU = 8;
-  for (int64_t i0 = lo + t; i0 < hi; i0 += kU * kTopkThreads) {
-    float vs[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t i = i0 + (int64_t)u * kTopkThreads;
-      vs[u] = i < hi ? __ldg(xr + i) : 0.f;
+  auto consider = [&](float v, int64_t i, uint32_t lb) {
+    // below the split's bound (strictly), or not better than this thread's k-th
+    if (order_code(v) < lb || (n == K && !better(v, i, th_s, th_i))) return;
+    int pos = n < K ? n : K - 1;
+    while (pos > 0 && better(v, i, my_s[pos - 1], my_i[pos - 1])) {
+      my_s[pos] = my_s[pos - 1];
+      my_i[pos] = my_i[pos - 1];
+      --pos;
     }
+    my_s[pos] = v;
+    my_i[pos] = i;
+    if (n < K) ++n;
+    if (n == K) {
+      th_s = my_s[K - 1];
+      th_i = my_i[K - 1];
+      if (th_s == th_s) atomicMax(&s_bound, order_code(th_s));  // (a NaN bounds nothing)
+    }
+  };
+  if ((N & 3) == 0) {
+    // the row and the split start on 16-byte boundaries: four values per load,
+    // four loads in flight per step, and four values rejected by one test of
+    // their maximum against this thread's k-th best and the split's bound (a
+    // value equal to either is still tested alone, for the lower-index rule;
+    // a NaN never enters)
+    const float4* xr4 = reinterpret_cast<const float4*>(xr);
+    const int64_t lo4 = lo >> 2, hi4 = hi >> 2;
+    constexpr int kU = 4;
+    for (int64_t j0 = lo4 + t; j0 < hi4; j0 += kU * kTopkThreads) {
+      float4 vs[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t i = i0 + (int64_t)u * kTopkThreads;
-      const float v = vs[u];
-      if (i >= hi || (n == K && !better(v, i, th_s, th_i))) continue;
-      int pos = n < K ? n : K - 1;
-      while (pos > 0 && better(v, i, my_s[pos - 1], my_i[pos - 1])) {
-        my_s[pos] = my_s[pos - 1];
-        my_i[pos] = my_i[pos - 1];
-        --pos;
+      for (int u = 0; u < kU; ++u) {
+        const int64_t j = j0 + (int64_t)u * kTopkThreads;
+        vs[u] = j < hi4 ? __ldg(xr4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      my_s[pos] = v;
-      my_i[pos] = i;
-      if (n < K) ++n;
-      if (n == K) {
-        th_s = my_s[K - 1];
-        th_i = my_i[K - 1];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t j = j0 + (int64_t)u * kTopkThreads;
+        if (j >= hi4) continue;
+        const float4 v = vs[u];
+        const float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+        const uint32_t lb = *bound;
+        if ((n == K && m < th_s) || order_code(m) < lb) continue;
+        consider(v.x, 4 * j, lb);
+        consider(v.y, 4 * j + 1, lb);
+        consider(v.z, 4 * j + 2, lb);
+        consider(v.w, 4 * j + 3, lb);
+      }
+    }
+  } else {
+    // eight independent loads in flight per step, then the tests in order
+    constexpr int kU = 8;
+    for (int64_t i0 = lo + t; i0 < hi; i0 += kU * kTopkThreads) {
+      float vs[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t i = i0 + (int64_t)u * kTopkThreads;
+        vs[u] = i < hi ? __ldg(xr + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t i = i0 + (int64_t)u * kTopkThreads;
+        if (i < hi) consider(vs[u], i, *bound);
       }
     }
   }
