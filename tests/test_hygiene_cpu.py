@@ -73,6 +73,14 @@ def test_traffic_is_reported_only_for_the_captured_source_and_workload(tmp_path,
     f.write_text(json.dumps({"score_tc": {"dram_bytes_per_launch": 123, "source_sha": "0" * 16,
                                           "workload": "qwen25_3b_decode"}}))
     assert bench.kernel_traffic("score_tc", src, "qwen25_3b_decode") is None
+    # an entry kernel@workload serves that workload; the kernel's own entry the one it names
+    f.write_text(json.dumps({
+        "score_tc": {"dram_bytes_per_launch": 123, "source_sha": sha, "workload": "qwen25_3b_decode"},
+        "score_tc@llama31_8b_prefill": {"dram_bytes_per_launch": 456, "source_sha": sha,
+                                        "workload": "llama31_8b_prefill"}}))
+    assert bench.kernel_traffic("score_tc", src, "qwen25_3b_decode") == 123
+    assert bench.kernel_traffic("score_tc", src, "llama31_8b_prefill") == 456
+    assert bench.kernel_traffic("score_tc", src, "long_context_131k") is None
 
 
 def test_committed_traffic_entries_name_existing_summaries():
