@@ -118,54 +118,145 @@ topk_stage1(const float* __restrict__ x, int64_t N, int K, int splits, float* ws
       if (th_s == th_s) atomicMax(&s_bound, order_code(th_s));  // (a NaN bounds nothing)
     }
   };
-  if ((N & 3) == 0) {
-    // the row and the split start on 16-byte boundaries: four values per load,
-    // four loads in flight per step, and four values rejected by one test of
-    // their maximum against this thread's k-th best and the split's bound (a
-    // value equal to either is still tested alone, for the lower-index rule;
-    // a NaN never enters)
-    const float4* xr4 = reinterpret_cast<const float4*>(xr);
-    const int64_t lo4 = lo >> 2, hi4 = hi >> 2;
-    constexpr int kU = 4;
-    for (int64_t j0 = lo4 + t; j0 < hi4; j0 += kU * kTopkThreads) {
-      float4 vs[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int64_t j = j0 + (int64_t)u * kTopkThreads;
-        vs[u] = j < hi4 ? __ldg(xr4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (K <= 32) {
+    // one list per warp, held in registers: lane l < K has the warp's l-th
+    // best.  A value enters when it beats the warp's k-th best (lane K - 1)
+    // and is not below the split's bound; the lanes offering one are taken in
+    // turn (a ballot), and each insertion is a count of the entries ahead of
+    // it and a shift of those behind (shuffles): a few warp instructions, not
+    // every lane's insertion loop.  Every shuffle and ballot takes the whole
+    // warp, so the loops below run on warp-uniform bounds; lanes past the end
+    // offer nothing.
+    constexpr unsigned kAll = 0xffffffffu;
+    const int lane = t & 31, wid = t >> 5;
+    float ls = -INFINITY;
+    int64_t li = INT64_MAX;  // this lane's entry (an empty entry loses to every value)
+    float tv = -INFINITY;
+    int64_t tix = INT64_MAX;  // the warp's k-th best
+    auto passes = [&](float v, int64_t i, uint32_t lb) { return order_code(v) >= lb && better(v, i, tv, tix); };
+    auto offer = [&](float v, int64_t i, bool cand) {
+      unsigned m = __ballot_sync(kAll, cand);
+      while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const float cv = __shfl_sync(kAll, v, src);
+        const int64_t cx = __shfl_sync(kAll, i, src);
+        if (better(cv, cx, tv, tix)) {  // (the list may have improved since it was offered)
+          const int pos = __popc(__ballot_sync(kAll, lane < K && better(ls, li, cv, cx)));
+          const float us = __shfl_up_sync(kAll, ls, 1);
+          const int64_t ux = __shfl_up_sync(kAll, li, 1);
+          if (lane > pos) {
+            ls = us;
+            li = ux;
+          } else if (lane == pos) {
+            ls = cv;
+            li = cx;
+          }
+          tv = __shfl_sync(kAll, ls, K - 1);
+          tix = __shfl_sync(kAll, li, K - 1);
+          if (lane == 0 && tix != INT64_MAX && tv == tv) atomicMax(&s_bound, order_code(tv));
+        }
       }
+    };
+    if ((N & 3) == 0) {
+      const float4* xr4 = reinterpret_cast<const float4*>(xr);
+      const int64_t lo4 = lo >> 2, hi4 = hi >> 2;
+      constexpr int kU = 4;
+      for (int64_t jw = lo4 + wid * 32; jw < hi4; jw += kU * kTopkThreads) {
+        float4 vs[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int64_t j = j0 + (int64_t)u * kTopkThreads;
-        if (j >= hi4) continue;
-        const float4 v = vs[u];
-        const float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-        const uint32_t lb = *bound;
-        if ((n == K && m < th_s) || order_code(m) < lb) continue;
-        consider(v.x, 4 * j, lb);
-        consider(v.y, 4 * j + 1, lb);
-        consider(v.z, 4 * j + 2, lb);
-        consider(v.w, 4 * j + 3, lb);
+        for (int u = 0; u < kU; ++u) {
+          const int64_t j = jw + lane + (int64_t)u * kTopkThreads;
+          vs[u] = j < hi4 ? __ldg(xr4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t j = jw + lane + (int64_t)u * kTopkThreads;
+          const bool ok = j < hi4;
+          const float4 v = vs[u];
+          const uint32_t lb = *bound;
+          if (!__any_sync(kAll, ok && passes(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)), -1, lb))) continue;
+          offer(v.x, 4 * j, ok && passes(v.x, 4 * j, lb));
+          offer(v.y, 4 * j + 1, ok && passes(v.y, 4 * j + 1, lb));
+          offer(v.z, 4 * j + 2, ok && passes(v.z, 4 * j + 2, lb));
+          offer(v.w, 4 * j + 3, ok && passes(v.w, 4 * j + 3, lb));
+        }
+      }
+    } else {
+      constexpr int kU = 8;
+      for (int64_t iw = lo + wid * 32; iw < hi; iw += kU * kTopkThreads) {
+        float vs[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t i = iw + lane + (int64_t)u * kTopkThreads;
+          vs[u] = i < hi ? __ldg(xr + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t i = iw + lane + (int64_t)u * kTopkThreads;
+          offer(vs[u], i, i < hi && passes(vs[u], i, *bound));
+        }
       }
     }
+    // the warp's list becomes list number wid of the block merge
+    if (lane < K) {
+      cs[wid * K + lane] = ls;
+      ci[wid * K + lane] = li;
+    }
+    const int filled = __popc(__ballot_sync(kAll, lane < K && li != INT64_MAX));
+    cnt[t] = 0;
+    __syncthreads();
+    if (lane == 0) cnt[wid] = filled;
   } else {
-    // eight independent loads in flight per step, then the tests in order
-    constexpr int kU = 8;
-    for (int64_t i0 = lo + t; i0 < hi; i0 += kU * kTopkThreads) {
-      float vs[kU];
+    if ((N & 3) == 0) {
+      // the row and the split start on 16-byte boundaries: four values per load,
+      // four loads in flight per step, and four values rejected by one test of
+      // their maximum against this thread's k-th best and the split's bound (a
+      // value equal to either is still tested alone, for the lower-index rule;
+      // a NaN never enters)
+      const float4* xr4 = reinterpret_cast<const float4*>(xr);
+      const int64_t lo4 = lo >> 2, hi4 = hi >> 2;
+      constexpr int kU = 4;
+      for (int64_t j0 = lo4 + t; j0 < hi4; j0 += kU * kTopkThreads) {
+        float4 vs[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int64_t i = i0 + (int64_t)u * kTopkThreads;
-        vs[u] = i < hi ? __ldg(xr + i) : 0.f;
+        for (int u = 0; u < kU; ++u) {
+          const int64_t j = j0 + (int64_t)u * kTopkThreads;
+          vs[u] = j < hi4 ? __ldg(xr4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t j = j0 + (int64_t)u * kTopkThreads;
+          if (j >= hi4) continue;
+          const float4 v = vs[u];
+          const float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+          const uint32_t lb = *bound;
+          if ((n == K && m < th_s) || order_code(m) < lb) continue;
+          consider(v.x, 4 * j, lb);
+          consider(v.y, 4 * j + 1, lb);
+          consider(v.z, 4 * j + 2, lb);
+          consider(v.w, 4 * j + 3, lb);
+        }
       }
+    } else {
+      // eight independent loads in flight per step, then the tests in order
+      constexpr int kU = 8;
+      for (int64_t i0 = lo + t; i0 < hi; i0 += kU * kTopkThreads) {
+        float vs[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int64_t i = i0 + (int64_t)u * kTopkThreads;
-        if (i < hi) consider(vs[u], i, *bound);
+        for (int u = 0; u < kU; ++u) {
+          const int64_t i = i0 + (int64_t)u * kTopkThreads;
+          vs[u] = i < hi ? __ldg(xr + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t i = i0 + (int64_t)u * kTopkThreads;
+          if (i < hi) consider(vs[u], i, *bound);
+        }
       }
     }
+    cnt[t] = n;
   }
-  cnt[t] = n;
   __syncthreads();
   const int64_t o = (row * splits + sp) * K;
   block_merge(cs, ci, cnt, K, ws_s + o, ws_i + o);
